@@ -1,0 +1,183 @@
+"""Float64 CPU oracle for the tensor-parallel MLP  Y = GeLU(X A) B.
+
+TEST INFRASTRUCTURE ONLY. This module is the slow, plainly written checker
+that the CUDA library is compared against. Only the tests, the smoke check of
+the package entry file and the benchmark's CPU-baseline leg may import it; the
+library itself never calls it and has no CPU fallback. It shares no code,
+constant or helper with the CUDA sources.
+
+Everything is float64 numpy. Matrix products use numpy's matmul as a library
+step; nothing is blocked, fused or reordered beyond what the formulas state.
+
+Notation (scratchllm.com "Tensor-Parallel MLP (Megatron)", section "The
+problem"): X is [T, D] (one row per token), A is [D, F], B is [F, D], and
+there are n shards with F divisible by n.
+
+Every function below is pinned by tests in tests/test_oracle_pins.py against
+values printed on the pages, closed forms or brute force; none is "parity
+unpinned".
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# Constants of the GPT-2 GeLU approximation, scratchllm.com "Tensor-Parallel
+# MLP (Megatron)", section "GeLU": u = sqrt(2/pi) * (x + 0.044715 x^3).
+SQRT_2_OVER_PI = math.sqrt(2.0 / math.pi)
+CUBIC_COEF = 0.044715
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def gelu(x):
+    """GeLU(x) ~= 1/2 x (1 + tanh u), u = sqrt(2/pi)(x + 0.044715 x^3), elementwise.
+
+    scratchllm.com "Tensor-Parallel MLP (Megatron)", section "GeLU".
+    """
+    x = _f64(x)
+    u = SQRT_2_OVER_PI * (x + CUBIC_COEF * x * x * x)
+    return 0.5 * x * (1.0 + np.tanh(u))
+
+
+def gelu_grad(x):
+    """d/dx of the tanh GeLU above, by the product and chain rules.
+
+    With t = tanh(u):  d/dx [1/2 x (1+t)] = 1/2 (1+t) + 1/2 x (1 - t^2) du/dx,
+    du/dx = sqrt(2/pi) (1 + 3 * 0.044715 x^2).  (The pages give the forward
+    formula only; this is its derivative, needed for the backward pass of the
+    column-then-row MLP that duoan.github.io "Tensor Parallelism in
+    Megatron-LM" section 3 describes.)
+    """
+    x = _f64(x)
+    u = SQRT_2_OVER_PI * (x + CUBIC_COEF * x * x * x)
+    t = np.tanh(u)
+    du = SQRT_2_OVER_PI * (1.0 + 3.0 * CUBIC_COEF * x * x)
+    return 0.5 * (1.0 + t) + 0.5 * x * (1.0 - t * t) * du
+
+
+def shard_mlp(A, B, n: int):
+    """Split A by columns and B by the matching rows into n pairs (A_i, B_i).
+
+    Shard i gets columns i*F/n .. (i+1)*F/n - 1 of A and the same range of
+    rows of B (scratchllm.com "Tensor-Parallel MLP (Megatron)", sections "The
+    split" and "Requirements"). F must be divisible by n ("What to implement").
+    """
+    A = _f64(A)
+    B = _f64(B)
+    D, F = A.shape
+    if B.shape != (F, D):
+        raise ValueError(f"B must be [F, D] = [{F}, {D}], got {B.shape}")
+    if n <= 0 or F % n != 0:
+        raise ValueError(f"F={F} is not divisible by n={n}")
+    Fs = F // n
+    return [(A[:, i * Fs:(i + 1) * Fs], B[i * Fs:(i + 1) * Fs, :]) for i in range(n)]
+
+
+def mlp(X, A, B):
+    """The unsplit MLP  Y = GeLU(X A) B  (scratchllm.com, section "The problem")."""
+    return gelu(_f64(X) @ _f64(A)) @ _f64(B)
+
+
+def shard_partial(X, A_i, B_i):
+    """One shard's work: H_i = GeLU(X A_i) and the partial output Y_i = H_i B_i.
+
+    scratchllm.com "Tensor-Parallel MLP (Megatron)", section "The split"
+    (first two bullets). Returns (H_i, Y_i).
+    """
+    H_i = gelu(_f64(X) @ _f64(A_i))
+    return H_i, H_i @ _f64(B_i)
+
+
+def tp_mlp(X, shards, return_partials: bool = False):
+    """Each shard's partial from its own (A_i, B_i), then the sum Y = sum_i Y_i.
+
+    The sum is the simulated all-reduce (scratchllm.com, section "The split",
+    third bullet, and "What to implement"), taken in shard order
+    ((Y_0 + Y_1) + Y_2) + ... .
+    """
+    partials = [shard_partial(X, A_i, B_i) for (A_i, B_i) in shards]
+    Y = partials[0][1].copy()
+    for _, Y_i in partials[1:]:
+        Y = Y + Y_i
+    if return_partials:
+        return Y, partials
+    return Y
+
+
+def tp_mlp_backward(X, dY, shards):
+    """Gradients of L = sum(Y * dY) for Y = sum_i GeLU(X A_i) B_i.
+
+    Per shard (the column/row algebra of duoan.github.io "Tensor Parallelism
+    in Megatron-LM", sections 2-3; the upstream gradient dY reaches every
+    shard unchanged because the forward reduction is a plain sum):
+        P_i  = X A_i
+        H_i  = GeLU(P_i)
+        dH_i = dY B_i^T
+        dP_i = dH_i * GeLU'(P_i)
+        dB_i = H_i^T dY
+        dA_i = X^T dP_i
+    and dX = sum_i dP_i A_i^T, summed in shard order (the one reduction the
+    backward pass needs). Returns (dX, [dA_i], [dB_i]).
+    """
+    X = _f64(X)
+    dY = _f64(dY)
+    dX = None
+    dA, dB = [], []
+    for A_i, B_i in shards:
+        A_i = _f64(A_i)
+        B_i = _f64(B_i)
+        P_i = X @ A_i
+        H_i = gelu(P_i)
+        dH_i = dY @ B_i.T
+        dP_i = dH_i * gelu_grad(P_i)
+        dB.append(H_i.T @ dY)
+        dA.append(X.T @ dP_i)
+        dX_i = dP_i @ A_i.T
+        dX = dX_i if dX is None else dX + dX_i
+    return dX, dA, dB
+
+
+# ---------------------------------------------------------------------------
+# Sampled entries, for workloads too large to run whole in float64. Each is
+# the same formula restricted to the rows or columns that the sampled outputs
+# depend on, so it gives exactly the entries the full functions would.
+# ---------------------------------------------------------------------------
+
+def tp_mlp_rows(X, shards, rows):
+    """Rows `rows` of tp_mlp(X, shards): each output row needs only its X row."""
+    return tp_mlp(_f64(X)[rows], shards)
+
+
+def shard_partial_rows(X, A_i, B_i, rows):
+    """Rows `rows` of (H_i, Y_i) for one shard."""
+    return shard_partial(_f64(X)[rows], A_i, B_i)
+
+
+def tp_mlp_backward_dx_rows(X, dY, shards, rows):
+    """Rows `rows` of dX: row t of dX needs only rows t of X and dY."""
+    dX, _, _ = tp_mlp_backward(_f64(X)[rows], _f64(dY)[rows], shards)
+    return dX
+
+
+def grad_A_cols(X, dY, A_i, B_i, cols):
+    """Columns `cols` of dA_i = X^T (dH_i * GeLU'(P_i)).
+
+    Column j of dA_i needs column j of P_i = X A_i and of dH_i = dY B_i^T,
+    i.e. column j of A_i and row j of B_i, over all tokens.
+    """
+    X = _f64(X)
+    dY = _f64(dY)
+    P = X @ _f64(A_i)[:, cols]
+    dH = dY @ _f64(B_i)[cols, :].T
+    return X.T @ (dH * gelu_grad(P))
+
+
+def grad_B_rows(X, dY, A_i, rows):
+    """Rows `rows` of dB_i = H_i^T dY: row j needs column j of H_i = GeLU(X A_i)."""
+    H = gelu(_f64(X) @ _f64(A_i)[:, rows])
+    return H.T @ _f64(dY)

@@ -1,0 +1,304 @@
+"""Pins for the float64 oracle, checked against facts fixed outside the oracle.
+
+Sources of truth:
+  * the worked example printed on scratchllm.com "Tensor-Parallel MLP
+    (Megatron)" (section "The split", Example; stored in
+    tests/golden/worked_example.json);
+  * the GeLU values and the row-split counterexample printed on that page;
+  * closed forms of the tanh GeLU (Taylor series at 0, odd-part identity,
+    limits), and its closeness to the exact erf GeLU from Python's math.erf;
+  * brute force with Python scalars on tiny inputs;
+  * central finite differences for every gradient.
+
+The last test plants plausible mistakes in a copy of the oracle and checks
+that the pins catch each of them.
+"""
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import tpmlp_oracle as orc
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_example.json")))
+
+
+def _rounded(v, d=3):
+    # Round half away from zero to d decimals, as the page prints; map -0.0 to 0.0.
+    return [float(np.round(x + 0.0, d)) + 0.0 for x in np.ravel(v)]
+
+
+# ---------------------------------------------------------------- worked example
+
+def worked_example_mismatches(mod=orc):
+    """List of (what, got, printed) for every printed value the oracle misses."""
+    g = GOLD
+    X, A, B, n, d = np.array(g["X"], float), np.array(g["A"], float), np.array(g["B"], float), g["n"], g["decimals"]
+    bad = []
+
+    def cmp(what, got, printed):
+        if _rounded(got, d) != [float(p) for p in printed]:
+            bad.append((what, np.ravel(got).tolist(), printed))
+
+    cmp("XA", X @ A, g["XA"])
+    cmp("H", mod.gelu(X @ A), g["H"])
+    cmp("Y", mod.mlp(X, A, B), g["Y"])
+    shards = mod.shard_mlp(A, B, n)
+    Y, parts = mod.tp_mlp(X, shards, return_partials=True)
+    for i, s in enumerate(g["shards"]):
+        cmp(f"A_{i}", shards[i][0], A[:, s["A_cols"]].ravel())
+        cmp(f"B_{i}", shards[i][1], B[s["B_rows"], :].ravel())
+        cmp(f"H_{i}", parts[i][0], s["H"])
+        cmp(f"Y_{i}", parts[i][1], s["Y"])
+    cmp("allreduce", Y, g["allreduce"])
+    for x, v in g["gelu_points"].items():
+        cmp(f"gelu({x})", mod.gelu(float(x)), [v])
+    cmp("gelu(1+1)", mod.gelu(2.0), [g["counterexample"]["gelu_of_sum_1_plus_1"]])
+    cmp("gelu(1)+gelu(1)", mod.gelu(1.0) + mod.gelu(1.0), [g["counterexample"]["sum_of_gelus_1_and_1"]])
+    return bad
+
+
+def test_worked_example_matches_printed_values():
+    assert worked_example_mismatches() == []
+
+
+def test_gelu_zero_is_exactly_zero():
+    assert oracle.gelu(0.0) == 0.0
+
+
+def test_row_split_counterexample():
+    # GeLU of a sum is not the sum of GeLUs (the reason A is split by columns).
+    assert abs(oracle.gelu(2.0) - 2 * oracle.gelu(1.0)) > 0.25
+
+
+# ---------------------------------------------------------------- GeLU closed forms
+
+def test_gelu_taylor_series_at_zero():
+    # GeLU(x) = x/2 + (c/2) x^2 + (c a/2 - c^3/6) x^4 + O(x^6), c = sqrt(2/pi), a = 0.044715,
+    # from tanh(u) = u - u^3/3 + ... with u = c (x + a x^3).
+    c, a = math.sqrt(2 / math.pi), 0.044715
+    for x in [1e-2, 2e-2, 4e-2]:
+        g = float(oracle.gelu(x))
+        c2 = (g - x / 2) / x**2
+        assert abs(c2 - c / 2) < 1e-2 * x  # x^2 coefficient; next term is O(x^2)
+        c4 = (g - x / 2 - c / 2 * x**2) / x**4
+        assert abs(c4 - (c * a / 2 - c**3 / 6)) < 5 * x**2
+
+
+def test_gelu_odd_part_identity():
+    # tanh is odd, so GeLU(x) - GeLU(-x) = x exactly in real arithmetic.
+    x = np.linspace(-9, 9, 4001)
+    np.testing.assert_allclose(oracle.gelu(x) - oracle.gelu(-x), x, rtol=0, atol=4e-15 * 9)
+
+
+def test_gelu_limits():
+    assert float(oracle.gelu(30.0)) == 30.0
+    assert abs(float(oracle.gelu(-30.0))) < 1e-300
+
+
+def test_gelu_close_to_exact_erf_gelu():
+    # The tanh form approximates x * Phi(x); its largest gap on the real line is below 5e-4.
+    xs = np.linspace(-8, 8, 3201)
+    exact = np.array([0.5 * x * (1 + math.erf(x / math.sqrt(2))) for x in xs])
+    gap = np.max(np.abs(oracle.gelu(xs) - exact))
+    assert 1e-4 < gap < 5e-4
+
+
+def test_gelu_grad_matches_central_differences():
+    x = np.linspace(-6, 6, 241)
+    h = 1e-5
+    fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+    np.testing.assert_allclose(oracle.gelu_grad(x), fd, rtol=0, atol=1e-9)
+    assert abs(float(oracle.gelu_grad(0.0)) - 0.5) < 1e-15
+
+
+# ---------------------------------------------------------------- sharding
+
+def test_shard_slices_follow_the_index_rule():
+    D, F = 3, 12
+    A = np.array([[1000 * r + c for c in range(F)] for r in range(D)], float)
+    B = np.array([[1000 * r + c for c in range(D)] for r in range(F)], float)
+    for n in [1, 2, 3, 4, 6, 12]:
+        Fs = F // n
+        for i, (A_i, B_i) in enumerate(oracle.shard_mlp(A, B, n)):
+            assert A_i.shape == (D, Fs) and B_i.shape == (Fs, D)
+            for r in range(D):
+                for c in range(Fs):
+                    assert A_i[r, c] == 1000 * r + (i * Fs + c)
+            for r in range(Fs):
+                for c in range(D):
+                    assert B_i[r, c] == 1000 * (i * Fs + r) + c
+
+
+@pytest.mark.parametrize("n", [0, 5, 7, -2])
+def test_shard_rejects_non_divisor(n):
+    with pytest.raises(ValueError):
+        oracle.shard_mlp(np.zeros((2, 12)), np.zeros((12, 2)), n)
+
+
+def test_sharded_equals_unsplit_for_every_divisor():
+    rng = np.random.default_rng(1)
+    T, D, F = 5, 4, 24
+    X, A, B = rng.normal(size=(T, D)), rng.normal(size=(D, F)), rng.normal(size=(F, D))
+    Y = oracle.mlp(X, A, B)
+    for n in [d for d in range(1, F + 1) if F % d == 0]:
+        np.testing.assert_allclose(oracle.tp_mlp(X, oracle.shard_mlp(A, B, n)), Y, rtol=1e-13, atol=1e-13)
+
+
+def _brute_force_mlp(X, A, B):
+    T, D = len(X), len(X[0])
+    F = len(A[0])
+    c = math.sqrt(2 / math.pi)
+    Y = [[0.0] * D for _ in range(T)]
+    for t in range(T):
+        for f in range(F):
+            p = 0.0
+            for d in range(D):
+                p += X[t][d] * A[d][f]
+            h = 0.5 * p * (1 + math.tanh(c * (p + 0.044715 * p**3)))
+            for d in range(D):
+                Y[t][d] += h * B[f][d]
+    return Y
+
+
+def test_brute_force_tiny():
+    rng = np.random.default_rng(2)
+    T, D, F = 3, 5, 6
+    X, A, B = rng.normal(size=(T, D)), rng.normal(size=(D, F)), rng.normal(size=(F, D))
+    ref = np.array(_brute_force_mlp(X.tolist(), A.tolist(), B.tolist()))
+    for n in [1, 2, 3, 6]:
+        np.testing.assert_allclose(oracle.tp_mlp(X, oracle.shard_mlp(A, B, n)), ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(X, A, B, dY):
+    return float(np.sum(oracle.mlp(X, A, B) * dY))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3])
+def test_backward_matches_finite_differences(n):
+    rng = np.random.default_rng(3 + n)
+    T, D, F = 4, 3, 6
+    X, A, B, dY = (rng.normal(size=s) for s in [(T, D), (D, F), (F, D), (T, D)])
+    dX, dA, dB = oracle.tp_mlp_backward(X, dY, oracle.shard_mlp(A, B, n))
+    h = 1e-6
+
+    def fd(M, idx):
+        Mp, Mm = M.copy(), M.copy()
+        Mp[idx] += h
+        Mm[idx] -= h
+        args_p = {"X": X, "A": A, "B": B}
+        args_m = dict(args_p)
+        key = [k for k, v in args_p.items() if v is M][0]
+        args_p[key], args_m[key] = Mp, Mm
+        return (_loss(args_p["X"], args_p["A"], args_p["B"], dY) - _loss(args_m["X"], args_m["A"], args_m["B"], dY)) / (2 * h)
+
+    Fs = F // n
+    for idx in np.ndindex(T, D):
+        assert abs(dX[idx] - fd(X, idx)) < 1e-7
+    for r, c in np.ndindex(D, F):
+        assert abs(dA[c // Fs][r, c % Fs] - fd(A, (r, c))) < 1e-7
+    for r, c in np.ndindex(F, D):
+        assert abs(dB[r // Fs][r % Fs, c] - fd(B, (r, c))) < 1e-7
+
+
+def test_sharded_gradients_reassemble_the_unsplit_ones():
+    rng = np.random.default_rng(7)
+    T, D, F = 6, 4, 12
+    X, A, B, dY = (rng.normal(size=s) for s in [(T, D), (D, F), (F, D), (T, D)])
+    dX1, (dA1,), (dB1,) = oracle.tp_mlp_backward(X, dY, oracle.shard_mlp(A, B, 1))
+    for n in [2, 3, 4, 6, 12]:
+        dX, dA, dB = oracle.tp_mlp_backward(X, dY, oracle.shard_mlp(A, B, n))
+        np.testing.assert_allclose(dX, dX1, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(np.concatenate(dA, axis=1), dA1, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(np.concatenate(dB, axis=0), dB1, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- sampled entries
+
+def test_sampled_entries_equal_full_results():
+    rng = np.random.default_rng(11)
+    T, D, F, n = 9, 5, 8, 2
+    X, A, B, dY = (rng.normal(size=s) for s in [(T, D), (D, F), (F, D), (T, D)])
+    shards = oracle.shard_mlp(A, B, n)
+    Y, parts = oracle.tp_mlp(X, shards, return_partials=True)
+    dX, dA, dB = oracle.tp_mlp_backward(X, dY, shards)
+    rows, cols = [0, 3, 8], [1, 3]
+    np.testing.assert_allclose(oracle.tp_mlp_rows(X, shards, rows), Y[rows], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(oracle.tp_mlp_backward_dx_rows(X, dY, shards, rows), dX[rows], rtol=1e-13, atol=1e-13)
+    for i, (A_i, B_i) in enumerate(shards):
+        H_r, Y_r = oracle.shard_partial_rows(X, A_i, B_i, rows)
+        np.testing.assert_allclose(H_r, parts[i][0][rows], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(Y_r, parts[i][1][rows], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(oracle.grad_A_cols(X, dY, A_i, B_i, cols), dA[i][:, cols], rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(oracle.grad_B_rows(X, dY, A_i, cols), dB[i][cols, :], rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- planted mistakes
+
+class _Mutant:
+    """A copy of the oracle's public functions with one plausible mistake planted."""
+
+    def __init__(self, **over):
+        for k in ["gelu", "gelu_grad", "shard_mlp", "mlp", "shard_partial", "tp_mlp"]:
+            setattr(self, k, getattr(orc, k))
+        self.__dict__.update(over)
+
+
+def _erf_gelu(x):
+    x = np.asarray(x, float)
+    return 0.5 * x * (1 + np.vectorize(math.erf)(x / math.sqrt(2)))
+
+
+def _gelu_no_cubic(x):
+    x = np.asarray(x, float)
+    return 0.5 * x * (1 + np.tanh(math.sqrt(2 / math.pi) * x))
+
+
+def _shard_off_by_one(A, B, n):
+    s = orc.shard_mlp(A, B, n)
+    return [(a, s[(i + 1) % n][1]) for i, (a, _) in enumerate(s)]
+
+
+def _shard_interleaved(A, B, n):
+    A, B = np.asarray(A, float), np.asarray(B, float)
+    return [(A[:, i::n], B[i::n, :]) for i in range(n)]
+
+
+def _tp_mlp_last_only(X, shards, return_partials=False):
+    Y, parts = orc.tp_mlp(X, shards, return_partials=True)
+    Y = parts[-1][1]
+    return (Y, parts) if return_partials else Y
+
+
+def _mlp_rows_of_B_reversed(X, A, B):
+    return orc.gelu(np.asarray(X, float) @ np.asarray(A, float)) @ np.asarray(B, float)[::-1]
+
+
+@pytest.mark.parametrize(
+    "name,mut",
+    [
+        ("erf GeLU instead of tanh", dict(gelu=_erf_gelu)),
+        ("cubic term dropped", dict(gelu=_gelu_no_cubic)),
+        ("B rows of the wrong shard", dict(shard_mlp=_shard_off_by_one)),
+        ("interleaved instead of contiguous slices", dict(shard_mlp=_shard_interleaved)),
+        ("all-reduce drops partials", dict(tp_mlp=_tp_mlp_last_only)),
+        ("rows of B reversed", dict(mlp=_mlp_rows_of_B_reversed)),
+    ],
+)
+def test_pins_catch_planted_mistakes(name, mut):
+    assert worked_example_mismatches(_Mutant(**mut)) != [], name
+
+
+def test_gradient_pins_catch_a_wrong_gelu_grad():
+    # A gelu' missing its second term must fail the central-difference pin.
+    bad = lambda x: 0.5 * (1 + np.tanh(math.sqrt(2 / math.pi) * (x + 0.044715 * x**3)))
+    x = np.linspace(-3, 3, 61)
+    h = 1e-5
+    fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
+    assert np.max(np.abs(bad(x) - fd)) > 1e-2

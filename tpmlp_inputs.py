@@ -1,0 +1,109 @@
+"""Seeded synthetic inputs for the tensor-parallel MLP workloads.
+
+This module only draws random tensors of the right shapes, distributions and
+dtypes. It contains none of the MLP's arithmetic, so that both the CUDA path
+(through the tests and the benchmark) and the float64 oracle can be fed the
+very same values without sharing any code beyond this.
+
+Workloads (T tokens, hidden D, MLP width F, N shards; the MLP is
+Y = GeLU(X A) B with A of shape (D, F) and B of shape (F, D), as set out on
+scratchllm.com "Tensor-Parallel MLP (Megatron)", section "The problem"):
+
+  tiny_fp32   T=64,    D=64,   F=256,   N=4  fp32   X~N(0,1), A~N(0,1/sqrt(D)), B~N(0,1/sqrt(F))
+  gpt2_small  T=4096,  D=768,  F=3072,  N=4  bf16   X~N(0,1), A,B~N(0,0.02)
+  seq128      T=1024,  D=1024, F=4096,  N=4  bf16   (batch 8 x seq 128)
+  seq256      T=2048,  D=1024, F=4096,  N=4  bf16   (batch 8 x seq 256)
+  seq512      T=4096,  D=1024, F=4096,  N=4  bf16   (batch 8 x seq 512)
+  large       T=16384, D=4096, F=16384, N=8  bf16   X~N(0,1), A,B~N(0,0.02)
+  fwd_bwd     T=8192,  D=8192, F=32768, N=8  bf16   X~N(0,1), A,B~N(0,0.01), dY~N(0,1)
+
+"N(0, s)" means a normal with standard deviation s. Each tensor gets its own
+CPU torch.Generator: X uses seed+0, A seed+1, B seed+2, dY seed+3. Values are
+drawn in float32, scaled, then rounded once to the workload's dtype; the
+rounded tensors are what both sides receive (the oracle widens them exactly
+to float64).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    D: int
+    F: int
+    N: int
+    dtype: str          # "f32" or "bf16": storage type of X, A, B, dY
+    x_std: float
+    a_std: float
+    b_std: float
+    dy_std: float = 1.0
+    backward: bool = False
+
+    @property
+    def Fs(self) -> int:
+        return self.F // self.N
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def fwd_flops(self) -> int:
+        """4*T*D*F: two GEMMs of 2*T*D*F each."""
+        return 4 * self.T * self.D * self.F
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("tiny_fp32", 64, 64, 256, 4, "f32", 1.0, 1.0 / math.sqrt(64), 1.0 / math.sqrt(256)),
+        Workload("gpt2_small", 4096, 768, 3072, 4, "bf16", 1.0, 0.02, 0.02),
+        Workload("seq128", 8 * 128, 1024, 4096, 4, "bf16", 1.0, 0.02, 0.02),
+        Workload("seq256", 8 * 256, 1024, 4096, 4, "bf16", 1.0, 0.02, 0.02),
+        Workload("seq512", 8 * 512, 1024, 4096, 4, "bf16", 1.0, 0.02, 0.02),
+        Workload("large", 8 * 2048, 4096, 16384, 8, "bf16", 1.0, 0.02, 0.02),
+        Workload("fwd_bwd", 8192, 8192, 32768, 8, "bf16", 1.0, 0.01, 0.01, 1.0, True),
+    ]
+}
+
+
+def _draw(shape, std: float, seed: int, dtype: torch.dtype) -> torch.Tensor:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    t = torch.randn(shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def make_inputs(w: Workload, seed: int = 0, with_dy: bool | None = None) -> dict[str, torch.Tensor]:
+    """Return CPU tensors X [T,D], A [D,F], B [F,D] (and dY [T,D]) in w's dtype."""
+    dt = w.torch_dtype
+    out = {
+        "X": _draw((w.T, w.D), w.x_std, seed + 0, dt),
+        "A": _draw((w.D, w.F), w.a_std, seed + 1, dt),
+        "B": _draw((w.F, w.D), w.b_std, seed + 2, dt),
+    }
+    if with_dy if with_dy is not None else w.backward:
+        out["dY"] = _draw((w.T, w.D), w.dy_std, seed + 3, dt)
+    return out
+
+
+def sample_indices(n: int, k: int, seed: int) -> list[int]:
+    """k distinct sorted indices in [0, n), always including the first and last."""
+    if k >= n:
+        return list(range(n))
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    idx = set(torch.randperm(n, generator=g)[: max(k - 2, 0)].tolist())
+    idx.update({0, n - 1})
+    return sorted(idx)
