@@ -1,0 +1,406 @@
+"""Benchmark of the tensor-parallel MLP forward on GB300.
+
+One step = one pass over every forward row of the hot path on the large
+workload (T=16384 tokens, D=4096, F=16384, N=8 shards, bf16 operands, fp32
+accumulation), with inputs resident in HBM:
+    faithful:  H_i = GeLU(X A_i) -> Y_i = H_i B_i -> Y = sum_i Y_i (shard order)
+    fused:     H_i = GeLU(X A_i) -> Y = sum_i H_i B_i accumulated on chip
+i.e. 2 x 4*T*D*F FLOP. `value` is TFLOP/s over the whole step. Every kernel
+is timed with CUDA events on the stream it is launched on.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tpmlp|reference]
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (host cores). With N > 1 (torchrun), every rank runs its own replica
+(the path has no cross-GPU step here) and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "TP-MLP fwd TFLOP/s on 1 GB300 (% BF16 peak); partial-sum reduce GB/s (% HBM)"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = float(d.get("hbm_gbs") or d.get("hbm_GBps") or 0)
+            bf = float(d.get("bf16_tflops") or 0)
+            bfs = float(d.get("bf16_tflops_sustained") or bf or 0)
+            if hbm > 0 and bf > 0:
+                return {"hbm_gbs": hbm, "bf16_tflops": bf, "bf16_tflops_sustained": bfs, "source": "measured"}
+        except Exception:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def _oracle_worker(target_s: float, reps: int, out_path: str):
+    """Runs in a fresh interpreter: times the float64 oracle on token-row samples.
+
+    Inputs are generated once (seeded like the large workload); a 16-row call
+    calibrates the rate, then `reps` calls each on as many rows as take about
+    target_s seconds are timed.
+    """
+    import numpy as np
+    import torch
+
+    import oracle
+    from tpmlp_inputs import WORKLOADS, make_inputs
+
+    w = WORKLOADS["large"]
+    inp = make_inputs(w, seed=0)
+    X = inp["X"].to(torch.float64).numpy()
+    shards = oracle.shard_mlp(inp["A"].to(torch.float64).numpy(), inp["B"].to(torch.float64).numpy(), w.N)
+    t0 = time.perf_counter()
+    oracle.tp_mlp_rows(X, shards, list(range(16)))
+    per_row = (time.perf_counter() - t0) / 16
+    rows = int(max(16, min(w.T, target_s / max(per_row, 1e-9))))
+    times, check = [], 0.0
+    for r in range(reps):
+        sel = list(range((r * rows) % (w.T - rows + 1), (r * rows) % (w.T - rows + 1) + rows))
+        t0 = time.perf_counter()
+        Y = oracle.tp_mlp_rows(X, shards, sel)
+        times.append(time.perf_counter() - t0)
+        check += float(np.sum(Y))
+    json.dump({"seconds": times, "rows": rows, "checksum": check}, open(out_path, "w"))
+
+
+def run_oracle(target_s: float, reps: int, cores: int) -> dict:
+    out = os.path.join("/tmp", f"tpmlp_oracle_{os.getpid()}.json")
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    code = f"import bench; bench._oracle_worker({target_s}, {reps}, {out!r})"
+    subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, check=True)
+    r = json.load(open(out))
+    os.remove(out)
+    return r
+
+
+def cpu_baseline(target_s: float = 12.0) -> dict:
+    """The oracle as it stands on a bounded sample (token rows of the large workload)."""
+    from tpmlp_inputs import WORKLOADS
+
+    w = WORKLOADS["large"]
+    cores = len(os.sched_getaffinity(0))
+    r = run_oracle(target_s, 1, cores)
+    flops = 4.0 * r["rows"] * w.D * w.F
+    return {"value": flops / r["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{r['rows']} of {w.T} token rows of the large workload, one float64 forward "
+                      f"(numpy, {r['seconds'][0]:.1f} s)"}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def bench_tpmlp(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = WORKLOADS[args.workload]
+    inp = make_inputs(w, seed=rank)
+    X = inp["X"].to(dev)
+    A = inp["A"].to(dev)
+    B = inp["B"].to(dev)
+    sh = tp.tpmlp_shard(A, B, w.N)
+    del A, B
+    T, D, F, N, Fs = w.T, w.D, w.F, w.N, w.Fs
+    H = torch.empty((N, T, Fs), dtype=w.torch_dtype, device=dev)
+    Yp = torch.empty((N, T, D), dtype=torch.float32, device=dev)
+    Y1 = torch.empty((T, D), dtype=torch.float32, device=dev)
+    Y2 = torch.empty((T, D), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    kernels = ["gemm1_gelu(faithful)", "gemm2_partials", "allreduce", "gemm1_gelu(fused)", "gemm2_fused_sum"]
+
+    def step(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+        mark(0)
+        tp.tpmlp_hidden(X, sh, H)
+        mark(1)
+        tp.tpmlp_partials(H, sh, Yp)
+        mark(2)
+        tp.tpmlp_allreduce(Yp, Y1)
+        mark(3)
+        tp.tpmlp_hidden(X, sh, H)
+        mark(4)
+        tp.tpmlp_fused_sum(H, sh, Y2)
+        mark(5)
+
+    for _ in range(args.warmup):
+        step()
+    tp.tpmlp_check_status(stream)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(events[k])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    tp.tpmlp_check_status(stream)
+    total_ms = t0.elapsed_time(t1)
+    per_kernel = {name: [] for name in kernels}
+    for evs in events:
+        for i, name in enumerate(kernels):
+            per_kernel[name].append(evs[i].elapsed_time(evs[i + 1]))
+    avg = {k: sum(v) / len(v) for k, v in per_kernel.items()}
+
+    # ---- end to end through the public API, host buffers, copies inside the timed region
+    Xh = inp["X"].pin_memory()
+    Yh1 = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    Yh2 = torch.empty((T, D), dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(X)
+    ws_f = torch.empty(tp.tpmlp_workspace_bytes(T, sh, "faithful"), dtype=torch.uint8, device=dev)
+    ws_u = torch.empty(tp.tpmlp_workspace_bytes(T, sh, "fused"), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        tp.tpmlp_forward(Xd, sh, "faithful", Y1, ws_f)
+        Yh1.copy_(Y1, non_blocking=True)
+        tp.tpmlp_forward(Xd, sh, "fused", Y2, ws_u)
+        Yh2.copy_(Y2, non_blocking=True)
+
+    for _ in range(max(1, min(args.warmup, 3))):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    tp.tpmlp_check_status(stream)
+
+    res = {
+        "total_ms": total_ms, "avg": avg, "clocks": clk, "e2e_ms": e2e_ms,
+        "h2d": Xh.numel() * Xh.element_size(), "d2h": 2 * Yh1.numel() * 4,
+        "launches": 5 * args.steps,
+    }
+    sh.free()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["tpmlp", "reference"], default="tpmlp")
+    ap.add_argument("--workload", default="large")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from tpmlp_inputs import WORKLOADS
+
+    w = WORKLOADS[args.workload]
+    step_flops = 2 * w.fwd_flops()
+    config = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16 operands, fp32 accumulate; "
+                          "step = faithful forward + fused forward",
+              "T": w.T, "D": w.D, "F": w.F, "N": w.N,
+              "l2": "inputs larger than L2 (X + A + B = 402 MB, H = 537 MB per pass); no flush",
+              "parallelism": "replicas" if args.gpus > 1 else "single GPU"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cores = len(os.sched_getaffinity(0))
+        per_step = max(1.0, min(8.0, 150.0 / (args.warmup + args.steps)))
+        r = run_oracle(per_step, args.warmup + args.steps, cores)
+        rows = r["rows"]
+        times = r["seconds"][args.warmup:]
+        sample_flops = 4.0 * rows * w.D * w.F
+        v = sample_flops * len(times) / sum(times) / 1e12
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded normal inputs of the large workload's shapes)", "config": config,
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows} token rows of the large workload per step (one float64 forward)"},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group("nccl", rank=rank, world_size=world,
+                                             device_id=torch.device("cuda", local_rank))
+    res = bench_tpmlp(args, rank, world, local_rank)
+    ms_step = res["total_ms"] / args.steps
+    e2e_ms = res["e2e_ms"]
+    if world > 1:
+        t = torch.tensor([ms_step, e2e_ms], device=torch.device("cuda", local_rank))
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step, e2e_ms = t.tolist()
+    if rank != 0:
+        torch.distributed.destroy_process_group() if world > 1 else None
+        return
+
+    peaks = load_peaks()
+    avg = res["avg"]
+    T, D, F, N = w.T, w.D, w.F, w.N
+    gemm_flops = 2.0 * T * D * F
+    flops_of = {"gemm1_gelu(faithful)": gemm_flops, "gemm2_partials": gemm_flops,
+                "gemm1_gelu(fused)": gemm_flops, "gemm2_fused_sum": gemm_flops}
+    reduce_bytes = (N + 1) * T * D * 4.0
+    kernel_report = {}
+    for k, ms in avg.items():
+        if k == "allreduce":
+            gbs = reduce_bytes / (ms * 1e-3) / 1e9
+            kernel_report[k] = {"ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        else:
+            tf = flops_of[k] / (ms * 1e-3) / 1e12
+            kernel_report[k] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                                "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4)}
+    step_ms_sum = sum(avg.values())
+    dominant = max(avg, key=lambda k: avg[k])
+    if dominant == "allreduce":
+        ach = reduce_bytes / (avg[dominant] * 1e-3) / 1e9
+        roof = {"kernel": dominant, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": peaks["source"]}
+    else:
+        ach = flops_of[dominant] / (avg[dominant] * 1e-3) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(ach / pk, 4), "traffic": None,
+                "peak_source": peaks["source"] + " (sustained bf16, kernel timed inside a long step)"}
+    red_gbs = reduce_bytes / (avg["allreduce"] * 1e-3) / 1e9
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded normal inputs, A,B ~ N(0, 0.02), X ~ N(0, 1))", "config": config,
+        "frac_bf16_peak": round(value / world / peaks["bf16_tflops_sustained"], 4),
+        "reduce": {"GB/s": round(red_gbs, 1), "peak": peaks["hbm_gbs"],
+                   "frac_hbm": round(red_gbs / peaks["hbm_gbs"], 4), "bytes": reduce_bytes},
+        "modes": {
+            "faithful": {"ms": round(avg["gemm1_gelu(faithful)"] + avg["gemm2_partials"] + avg["allreduce"], 4)},
+            "fused": {"ms": round(avg["gemm1_gelu(fused)"] + avg["gemm2_fused_sum"], 4)},
+        },
+        "kernels": kernel_report, "kernel_ms_sum": round(step_ms_sum, 4),
+        "roofline": roof,
+        "clocks": res["clocks"],
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": res["launches"],
+        "peaks": peaks,
+    }
+    for m in ("faithful", "fused"):
+        ms = line["modes"][m]["ms"]
+        tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+        line["modes"][m]["TFLOP/s"] = round(tf, 1)
+        line["modes"][m]["frac_bf16"] = round(tf / peaks["bf16_tflops_sustained"], 4)
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

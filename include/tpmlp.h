@@ -1,0 +1,190 @@
+/*
+ * tpmlp.h — C ABI of the GB300 (sm_103a) tensor-parallel MLP library.
+ *
+ * The library computes the Megatron tensor-parallel MLP
+ *
+ *     Y = GeLU(X A) B,     X [T, D],  A [D, F],  B [F, D],
+ *
+ * with A split by columns and B by the matching rows into n shards, every
+ * shard's partial output computed on its own and the partials summed (the
+ * simulated all-reduce). All n shards run on the one GPU that is current when
+ * a call is made. Sources for each call are given beside it:
+ *   [P4] scratchllm.com "Tensor-Parallel MLP (Megatron)"
+ *   [P3] duoan.github.io "Tensor Parallelism in Megatron-LM"
+ *   [P1] ai-hpc.org "LLM Lab Notes 06: Megatron-style Transformer Block"
+ *
+ * Conventions that hold for every call:
+ *   - Matrices are dense and row-major (the last index is contiguous).
+ *   - Pointers named as "device" point to CUDA device memory on the current
+ *     device; the caller owns it unless stated otherwise. They must be 16-byte
+ *     aligned (TPMLP_ERR_ALIGN otherwise).
+ *   - Every call that takes a stream only enqueues work on it and returns; the
+ *     results are ready when that stream has reached the point of the call.
+ *   - The return value is TPMLP_OK (0) or a negative tpmlp_status. On error
+ *     nothing has been enqueued, and tpmlp_last_error() gives a message.
+ *   - Kernels never trap. A device-side wait that runs past its time limit
+ *     makes the kernel stop early and record TPMLP_ERR_TIMEOUT in a per-device
+ *     status word, which tpmlp_check_status() reads and clears.
+ *   - In bf16 (TPMLP_BF16) mode the operands X, A, B, dY are bf16, products are
+ *     accumulated in fp32, H_i and the backward's dP_i are rounded to bf16 when
+ *     they become operands of the next product, and every output (Y, dX, dA_i,
+ *     dB_i) is fp32. In fp32 (TPMLP_F32) mode everything is fp32.
+ */
+#ifndef TPMLP_H
+#define TPMLP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* tpmlp_stream_t;
+
+typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
+
+/* How the shard partials are summed ([P4] "The split", third bullet).
+ * FAITHFUL: every partial Y_i is written to memory, then one kernel adds them
+ *           in shard order ((Y_0 + Y_1) + Y_2) + ... .
+ * FUSED:    the second product walks its contraction shard by shard, 0..n-1,
+ *           into one on-chip accumulator, so no partial is ever written. */
+typedef enum { TPMLP_FAITHFUL = 0, TPMLP_FUSED = 1 } tpmlp_mode;
+
+typedef enum {
+  TPMLP_OK = 0,
+  TPMLP_ERR_ARG = -1,          /* null pointer, non-positive size, bad enum   */
+  TPMLP_ERR_DIVISIBILITY = -2, /* F not divisible by n ([P4] "What to implement") */
+  TPMLP_ERR_ALIGN = -3,        /* a pointer is not 16-byte aligned            */
+  TPMLP_ERR_SHAPE = -4,        /* bf16: D or F/n not a multiple of 8          */
+  TPMLP_ERR_CUDA = -5,         /* a CUDA runtime call failed                  */
+  TPMLP_ERR_TIMEOUT = -6,      /* a device-side wait ran out of time          */
+  TPMLP_ERR_WORKSPACE = -7,    /* workspace missing or smaller than required  */
+  TPMLP_ERR_UNSUPPORTED = -8,  /* e.g. bf16 with more than TPMLP_MAX_SHARDS   */
+  TPMLP_ERR_DEVICE = -9        /* current device is not sm_103 / shards handle
+                                  belongs to another device                   */
+} tpmlp_status;
+
+/* Largest shard count of the bf16 tensor-core path (the fp32 path has none). */
+#define TPMLP_MAX_SHARDS 16
+
+/* Opaque handle: the n shard pairs (A_i, B_i) and their descriptor table. */
+typedef struct tpmlp_shards tpmlp_shards;
+
+/* Library version, (major << 16) | minor. */
+int tpmlp_version(void);
+
+/* Message for the last error returned on the calling thread ("" if none). */
+const char* tpmlp_last_error(void);
+
+/* Waits for `stream`, then reads and clears the current device's status word.
+ * Returns TPMLP_OK, TPMLP_ERR_TIMEOUT if a kernel gave up on a wait since the
+ * last check, or TPMLP_ERR_CUDA if the stream reports an error. */
+int tpmlp_check_status(tpmlp_stream_t stream);
+
+/* gelu(x), elementwise: GeLU(x) = 1/2 x (1 + tanh u), u = sqrt(2/pi)(x + 0.044715 x^3)
+ * ([P4] section "GeLU"; "What to implement", first bullet).
+ *   x, y  device arrays of n elements of type dt (y may equal x).
+ *   n     element count, >= 0 (0 enqueues nothing).
+ * Computed in fp32; the bf16 variant rounds the result once to bf16. */
+int tpmlp_gelu(const void* x, void* y, int64_t n, tpmlp_dtype dt, tpmlp_stream_t stream);
+
+/* shard_mlp(A, B, n): split A [D, F] by columns and B [F, D] by rows into n
+ * pairs; shard i receives columns i*F/n .. (i+1)*F/n - 1 of A and the same
+ * rows of B ([P4] "What to implement", second bullet, and "Requirements").
+ *   A, B   device, row-major, of type dt; only read (the copies are enqueued
+ *          on `stream`, so A and B must stay valid until it reaches them).
+ *   n      1 <= n; F % n == 0 (TPMLP_ERR_DIVISIBILITY); bf16 needs n <=
+ *          TPMLP_MAX_SHARDS and D, F/n multiples of 8 (TPMLP_ERR_SHAPE).
+ *   out    receives the handle. The handle owns device copies of every A_i and
+ *          B_i (and, for bf16, their transposes, the operand layouts of the
+ *          tensor-core kernels) plus the device descriptor table, all made
+ *          with cudaMalloc on the current device; release them with
+ *          tpmlp_shards_free(). */
+int tpmlp_shard(const void* A, const void* B, int64_t D, int64_t F, int n, tpmlp_dtype dt,
+                tpmlp_stream_t stream, tpmlp_shards** out);
+
+/* Shape of a handle. Any output pointer may be NULL. */
+int tpmlp_shard_info(const tpmlp_shards* shards, int64_t* D, int64_t* F, int* n, tpmlp_dtype* dt);
+
+/* Device pointers to shard i's A_i [D, F/n] and B_i [F/n, D] (row-major,
+ * owned by the handle, valid until tpmlp_shards_free). */
+int tpmlp_shard_get(const tpmlp_shards* shards, int i, const void** A_i, const void** B_i);
+
+/* bf16 handles only: shard i's transposed copies A_i^T [F/n, D] and
+ * B_i^T [D, F/n] (row-major, owned by the handle). TPMLP_ERR_UNSUPPORTED for
+ * fp32 handles, which keep no transposes. */
+int tpmlp_shard_get_transposed(const tpmlp_shards* shards, int i, const void** At_i, const void** Bt_i);
+
+/* Releases everything the handle owns (synchronises the device first). NULL is a no-op. */
+void tpmlp_shards_free(tpmlp_shards* shards);
+
+/* Bytes of workspace that tpmlp_forward (backward = 0) or tpmlp_backward
+ * (backward = 1) needs for T tokens, these shards and this mode; 0 on bad
+ * arguments. The workspace holds the shards' H_i (and, in FAITHFUL mode, the
+ * partials), so it grows with T * F and, for FAITHFUL, with n * T * D. */
+size_t tpmlp_workspace_bytes(int64_t T, const tpmlp_shards* shards, tpmlp_mode mode, int backward);
+
+/* tp_mlp(X, shards): Y = sum_i GeLU(X A_i) B_i ([P4] "What to implement",
+ * third bullet; [P3] §3 "The MLP Block").
+ *   X    device [T, D] of the handle's dtype.
+ *   T    >= 1 tokens.
+ *   Y    device [T, D] fp32, written (not accumulated).
+ *   workspace, workspace_bytes  device scratch of at least
+ *        tpmlp_workspace_bytes(T, shards, mode, 0) bytes, caller-owned; its
+ *        contents are undefined afterwards.
+ * FAITHFUL sums the partials in shard order and is bitwise reproducible from
+ * run to run; FUSED gives the same sum to within rounding. */
+int tpmlp_forward(const void* X, int64_t T, const tpmlp_shards* shards, void* Y, tpmlp_mode mode,
+                  void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* The steps of tpmlp_forward, one call each, for callers that keep the
+ * intermediates.
+ *
+ * tpmlp_hidden: H_i = GeLU(X A_i) for every shard i ([P4] "The split", first
+ * bullet; [P3] §3 steps 1-2). X device [T, D]; H device [n][T][F/n] of the
+ * handle's dtype (shard i's block starts at H + i*T*(F/n) elements). */
+int tpmlp_hidden(const void* X, int64_t T, const tpmlp_shards* shards, void* H, tpmlp_stream_t stream);
+
+/* tpmlp_partials: Y_i = H_i B_i for every shard i ([P4] "The split", second
+ * bullet; [P3] §3 step 3). H as written by tpmlp_hidden; Yp device
+ * [n][T][D] fp32 (shard i's partial starts at Yp + i*T*D). */
+int tpmlp_partials(const void* H, int64_t T, const tpmlp_shards* shards, void* Yp, tpmlp_stream_t stream);
+
+/* tpmlp_allreduce: the simulated all-reduce Y = ((Y_0 + Y_1) + ...) + Y_{n-1}
+ * in fp32, in shard order ([P4] "The split", third bullet; [P1] §2 note 6).
+ * Yp device [n][count] fp32; Y device [count] fp32 (must not overlap Yp). */
+int tpmlp_allreduce(const void* Yp, int n, int64_t count, void* Y, tpmlp_stream_t stream);
+
+/* tpmlp_fused_sum: Y = sum_i H_i B_i accumulated shard by shard (0..n-1) on
+ * chip, with no partial written ([P3] §3: reduce where partial linear
+ * outputs must be summed). H as written by tpmlp_hidden; Y device [T, D] fp32. */
+int tpmlp_fused_sum(const void* H, int64_t T, const tpmlp_shards* shards, void* Y, tpmlp_stream_t stream);
+
+/* Backward of Y = sum_i GeLU(X A_i) B_i for the upstream gradient dY, i.e. the
+ * gradients of L = sum(Y * dY) ([P3] §3, the f/g operators; [P1] §2 note 8):
+ *   P_i = X A_i (recomputed), dH_i = dY B_i^T, dP_i = dH_i * GeLU'(P_i),
+ *   dB_i = H_i^T dY, dA_i = X^T dP_i, dX = sum_i dP_i A_i^T (shard order in
+ *   FAITHFUL mode, on-chip accumulation in FUSED mode).
+ * dY reaches every shard unchanged; only dX is summed over shards.
+ *   X, dY  device [T, D] of the handle's dtype.
+ *   dX     device [T, D] fp32.
+ *   dA     host array of n device pointers, dA[i] -> fp32 [D, F/n].
+ *   dB     host array of n device pointers, dB[i] -> fp32 [F/n, D].
+ *   workspace  at least tpmlp_workspace_bytes(T, shards, mode, 1) bytes. */
+int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards* shards, void* dX,
+                   void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
+                   size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Test hook for the time limits: launches one block that waits on a device
+ * barrier nobody ever completes, with the library's bounded wait and a limit
+ * of limit_ms milliseconds (1..10000). The block then stops and records
+ * TPMLP_ERR_TIMEOUT, which the next tpmlp_check_status() returns. */
+int tpmlp_selftest_wait_timeout(int limit_ms, tpmlp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H */

@@ -1,0 +1,276 @@
+"""tensor_transformer_mlp_column_gb300 — Python binding of libtpmlp (include/tpmlp.h).
+
+The tensor-parallel MLP  Y = GeLU(X A) B  with A split by columns and B by
+rows into n shards, each shard's partial computed on its own and the partials
+summed (scratchllm.com "Tensor-Parallel MLP (Megatron)"), on one GB300.
+
+This module only marshals arguments: torch tensors supply device memory and
+the current CUDA stream, and every step runs in the library's CUDA kernels.
+There is no CPU fallback; if libtpmlp.so is missing the first call raises.
+Function names are those of the C ABI.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp.so")
+
+TPMLP_F32, TPMLP_BF16 = 0, 1
+TPMLP_FAITHFUL, TPMLP_FUSED = 0, 1
+TPMLP_MAX_SHARDS = 16
+
+STATUS_NAMES = {
+    0: "TPMLP_OK",
+    -1: "TPMLP_ERR_ARG",
+    -2: "TPMLP_ERR_DIVISIBILITY",
+    -3: "TPMLP_ERR_ALIGN",
+    -4: "TPMLP_ERR_SHAPE",
+    -5: "TPMLP_ERR_CUDA",
+    -6: "TPMLP_ERR_TIMEOUT",
+    -7: "TPMLP_ERR_WORKSPACE",
+    -8: "TPMLP_ERR_UNSUPPORTED",
+    -9: "TPMLP_ERR_DEVICE",
+}
+globals().update({v: k for k, v in STATUS_NAMES.items()})
+
+# Every entry point of include/tpmlp.h with its ctypes signature.
+_P, _I, _I64, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "tpmlp_version": (_I, []),
+    "tpmlp_last_error": (ctypes.c_char_p, []),
+    "tpmlp_check_status": (_I, [_P]),
+    "tpmlp_gelu": (_I, [_P, _P, _I64, _I, _P]),
+    "tpmlp_shard": (_I, [_P, _P, _I64, _I64, _I, _I, _P, ctypes.POINTER(_P)]),
+    "tpmlp_shard_info": (_I, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "tpmlp_shard_get": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+    "tpmlp_shard_get_transposed": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+    "tpmlp_shards_free": (None, [_P]),
+    "tpmlp_workspace_bytes": (_SZ, [_I64, _P, _I, _I]),
+    "tpmlp_forward": (_I, [_P, _I64, _P, _P, _I, _P, _SZ, _P]),
+    "tpmlp_hidden": (_I, [_P, _I64, _P, _P, _P]),
+    "tpmlp_partials": (_I, [_P, _I64, _P, _P, _P]),
+    "tpmlp_allreduce": (_I, [_P, _I, _I64, _P, _P]),
+    "tpmlp_fused_sum": (_I, [_P, _I64, _P, _P, _P]),
+    "tpmlp_backward": (_I, [_P, _P, _I64, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
+    "tpmlp_selftest_wait_timeout": (_I, [_I, _P]),
+}
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class TpmlpError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where} -> {STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
+            )
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise TpmlpError(code, where, lib().tpmlp_last_error().decode())
+
+
+def _stream(stream=None) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return TPMLP_BF16
+    if t.dtype == torch.float32:
+        return TPMLP_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use torch.float32 or torch.bfloat16")
+
+
+def _dev(t: torch.Tensor, name: str) -> int:
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t.data_ptr()
+
+
+def _mode(mode) -> int:
+    if mode in (TPMLP_FAITHFUL, "faithful"):
+        return TPMLP_FAITHFUL
+    if mode in (TPMLP_FUSED, "fused"):
+        return TPMLP_FUSED
+    raise ValueError(f"unknown mode {mode!r}")
+
+
+class _DeviceArray:
+    """Exposes library-owned device memory to torch without copying."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _alias(ptr: int, shape, dtype: torch.dtype) -> torch.Tensor:
+    if dtype == torch.bfloat16:
+        return torch.as_tensor(_DeviceArray(ptr, shape, "<i2"), device="cuda").view(torch.bfloat16)
+    return torch.as_tensor(_DeviceArray(ptr, shape, "<f4"), device="cuda")
+
+
+# ----------------------------------------------------------------- API
+
+def tpmlp_version() -> int:
+    return lib().tpmlp_version()
+
+
+def tpmlp_last_error() -> str:
+    return lib().tpmlp_last_error().decode()
+
+
+def tpmlp_check_status(stream=None) -> None:
+    """Waits for the stream and raises TpmlpError if a kernel timed out on a wait."""
+    _check(lib().tpmlp_check_status(_stream(stream)), "tpmlp_check_status")
+
+
+def tpmlp_gelu(x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """GeLU(x) elementwise (GPT-2 tanh form), same dtype as x."""
+    y = torch.empty_like(x) if out is None else out
+    _check(lib().tpmlp_gelu(_dev(x, "x"), _dev(y, "y"), x.numel(), _dt(x), _stream(stream)), "tpmlp_gelu")
+    return y
+
+
+class Shards:
+    """The n shard pairs (A_i, B_i) owned by the library (tpmlp_shards handle)."""
+
+    def __init__(self, handle: int, D: int, F: int, n: int, dtype: torch.dtype):
+        self.handle, self.D, self.F, self.n, self.dtype = handle, D, F, n, dtype
+        self.Fs = F // n
+
+    def get(self, i: int):
+        """(A_i [D, F/n], B_i [F/n, D]) as tensors aliasing the library's copies."""
+        a, b = ctypes.c_void_p(), ctypes.c_void_p()
+        _check(lib().tpmlp_shard_get(self.handle, i, ctypes.byref(a), ctypes.byref(b)), "tpmlp_shard_get")
+        return _alias(a.value, (self.D, self.Fs), self.dtype), _alias(b.value, (self.Fs, self.D), self.dtype)
+
+    def get_transposed(self, i: int):
+        """(A_i^T [F/n, D], B_i^T [D, F/n]) for bf16 shards."""
+        a, b = ctypes.c_void_p(), ctypes.c_void_p()
+        _check(lib().tpmlp_shard_get_transposed(self.handle, i, ctypes.byref(a), ctypes.byref(b)),
+               "tpmlp_shard_get_transposed")
+        return _alias(a.value, (self.Fs, self.D), self.dtype), _alias(b.value, (self.D, self.Fs), self.dtype)
+
+    def free(self) -> None:
+        if self.handle:
+            lib().tpmlp_shards_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def tpmlp_shard(A: torch.Tensor, B: torch.Tensor, n: int, stream=None) -> Shards:
+    """shard_mlp(A, B, n): the library's own copies of every (A_i, B_i)."""
+    D, F = A.shape
+    h = ctypes.c_void_p()
+    _check(lib().tpmlp_shard(_dev(A, "A"), _dev(B, "B"), D, F, n, _dt(A), _stream(stream), ctypes.byref(h)),
+           "tpmlp_shard")
+    return Shards(h.value, D, F, n, A.dtype)
+
+
+def tpmlp_workspace_bytes(T: int, shards: Shards, mode="faithful", backward: bool = False) -> int:
+    return int(lib().tpmlp_workspace_bytes(T, shards.handle, _mode(mode), int(backward)))
+
+
+def _workspace(nbytes: int, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace too small: need {nbytes} bytes")
+        return workspace
+    return torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+
+
+def tpmlp_forward(X: torch.Tensor, shards: Shards, mode="faithful", Y: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """tp_mlp(X, shards): Y = sum_i GeLU(X A_i) B_i, fp32 [T, D]."""
+    T = X.shape[0]
+    Y = torch.empty((T, shards.D), dtype=torch.float32, device=X.device) if Y is None else Y
+    nb = tpmlp_workspace_bytes(T, shards, mode, False)
+    ws = _workspace(nb, workspace)
+    _check(lib().tpmlp_forward(_dev(X, "X"), T, shards.handle, _dev(Y, "Y"), _mode(mode), ws.data_ptr(),
+                               ws.numel() * ws.element_size(), _stream(stream)), "tpmlp_forward")
+    return Y
+
+
+def tpmlp_hidden(X: torch.Tensor, shards: Shards, H: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """H_i = GeLU(X A_i) for all shards: [n, T, F/n] in the shards' dtype."""
+    T = X.shape[0]
+    H = torch.empty((shards.n, T, shards.Fs), dtype=shards.dtype, device=X.device) if H is None else H
+    _check(lib().tpmlp_hidden(_dev(X, "X"), T, shards.handle, _dev(H, "H"), _stream(stream)), "tpmlp_hidden")
+    return H
+
+
+def tpmlp_partials(H: torch.Tensor, shards: Shards, Yp: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y_i = H_i B_i for all shards: [n, T, D] fp32."""
+    T = H.shape[1]
+    Yp = torch.empty((shards.n, T, shards.D), dtype=torch.float32, device=H.device) if Yp is None else Yp
+    _check(lib().tpmlp_partials(_dev(H, "H"), T, shards.handle, _dev(Yp, "Yp"), _stream(stream)), "tpmlp_partials")
+    return Yp
+
+
+def tpmlp_allreduce(Yp: torch.Tensor, Y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Simulated all-reduce: Y = ((Yp[0] + Yp[1]) + ...) + Yp[n-1], fp32."""
+    n = Yp.shape[0]
+    Y = torch.empty(Yp.shape[1:], dtype=torch.float32, device=Yp.device) if Y is None else Y
+    _check(lib().tpmlp_allreduce(_dev(Yp, "Yp"), n, Y.numel(), _dev(Y, "Y"), _stream(stream)), "tpmlp_allreduce")
+    return Y
+
+
+def tpmlp_fused_sum(H: torch.Tensor, shards: Shards, Y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Y = sum_i H_i B_i accumulated on chip in shard order: [T, D] fp32."""
+    T = H.shape[1]
+    Y = torch.empty((T, shards.D), dtype=torch.float32, device=H.device) if Y is None else Y
+    _check(lib().tpmlp_fused_sum(_dev(H, "H"), T, shards.handle, _dev(Y, "Y"), _stream(stream)), "tpmlp_fused_sum")
+    return Y
+
+
+def tpmlp_backward(X: torch.Tensor, dY: torch.Tensor, shards: Shards, mode="faithful",
+                   dX: Optional[torch.Tensor] = None, dA: Optional[Sequence[torch.Tensor]] = None,
+                   dB: Optional[Sequence[torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                   stream=None):
+    """Gradients of sum(Y * dY): (dX [T, D], [dA_i [D, F/n]], [dB_i [F/n, D]]), all fp32."""
+    T, D, Fs, n = X.shape[0], shards.D, shards.Fs, shards.n
+    dev = X.device
+    dX = torch.empty((T, D), dtype=torch.float32, device=dev) if dX is None else dX
+    dA = [torch.empty((D, Fs), dtype=torch.float32, device=dev) for _ in range(n)] if dA is None else list(dA)
+    dB = [torch.empty((Fs, D), dtype=torch.float32, device=dev) for _ in range(n)] if dB is None else list(dB)
+    pa = (ctypes.c_void_p * n)(*[_dev(t, "dA_i") for t in dA])
+    pb = (ctypes.c_void_p * n)(*[_dev(t, "dB_i") for t in dB])
+    nb = tpmlp_workspace_bytes(T, shards, mode, True)
+    ws = _workspace(nb, workspace)
+    _check(lib().tpmlp_backward(_dev(X, "X"), _dev(dY, "dY"), T, shards.handle, _dev(dX, "dX"), pa, pb,
+                                _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpmlp_backward")
+    return dX, dA, dB
+
+
+def tpmlp_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
+    _check(lib().tpmlp_selftest_wait_timeout(limit_ms, _stream(stream)), "tpmlp_selftest_wait_timeout")

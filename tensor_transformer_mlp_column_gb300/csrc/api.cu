@@ -1,0 +1,570 @@
+// api.cu — the library's C ABI (include/tpmlp.h): argument checks, the shards
+// handle with its descriptor table and tensor maps, workspace planning, and
+// the sequence of kernel launches for each call. Nothing here computes on the
+// host: every step of the MLP runs in the kernels of gemm_tc.cu, simt.cu and
+// elementwise.cu.
+#include "tpmlp.h"
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include "internal.h"
+
+using namespace tpmlp;
+
+struct tpmlp_shards {
+  int device = 0;
+  int64_t D = 0, F = 0, Fs = 0;
+  int n = 0;
+  tpmlp_dtype dt = TPMLP_F32;
+  void* mem = nullptr;
+  ShardDesc* d_table = nullptr;
+  std::vector<ShardDesc> desc;  // host copy of the descriptor table
+  // bf16 only: TMA maps of the shard-owned operands, all used as the "N x K"
+  // operand of a tensor-core product.
+  std::vector<CUtensorMap> map_At;  // A_i^T [Fs, D]: X A_i        (N = Fs, K = D)
+  std::vector<CUtensorMap> map_Bt;  // B_i^T [D, Fs]: H_i B_i      (N = D,  K = Fs)
+  std::vector<CUtensorMap> map_B;   // B_i   [Fs, D]: dY B_i^T     (N = Fs, K = D)
+  std::vector<CUtensorMap> map_A;   // A_i   [D, Fs]: dP_i A_i^T   (N = D,  K = Fs)
+};
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+#define TRY_CUDA(expr)                                                                        \
+  do {                                                                                        \
+    cudaError_t e_ = (expr);                                                                  \
+    if (e_ != cudaSuccess) return fail(TPMLP_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t round_up8(int64_t x) { return (x + 7) / 8 * 8; }
+size_t esize(tpmlp_dtype dt) { return dt == TPMLP_BF16 ? 2 : 4; }
+
+uint64_t wait_limit_ns() {
+  static uint64_t v = 0;
+  if (!v) {
+    const char* s = getenv("TPMLP_WAIT_LIMIT_MS");
+    long ms = s ? atol(s) : 0;
+    if (ms <= 0 || ms > 600000) ms = 4000;
+    v = static_cast<uint64_t>(ms) * 1000000ull;
+  }
+  return v;
+}
+
+// The kernels are built for sm_103a only.
+int check_device(int* dev_out) {
+  int dev = -1;
+  TRY_CUDA(cudaGetDevice(&dev));
+  int major = 0, minor = 0;
+  TRY_CUDA(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+  TRY_CUDA(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+  if (major != 10 || minor != 3)
+    return fail(TPMLP_ERR_DEVICE, "device %d is sm_%d%d; this library is built for sm_103a (GB300)", dev, major,
+                minor);
+  if (dev_out) *dev_out = dev;
+  return TPMLP_OK;
+}
+
+int check_handle_device(const tpmlp_shards* sh) {
+  int dev = -1;
+  int rc = check_device(&dev);
+  if (rc) return rc;
+  if (dev != sh->device)
+    return fail(TPMLP_ERR_DEVICE, "shards live on device %d but device %d is current", sh->device, dev);
+  return TPMLP_OK;
+}
+
+// Workspace plan: byte offsets of every scratch buffer, 256-byte aligned.
+struct WsPlan {
+  size_t H = 0, Yp = 0, Xt = 0, dYt = 0, P = 0, dH = 0, Ht = 0, dP = 0, dPt = 0, dXp = 0;
+  size_t total = 0;
+};
+
+WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  WsPlan w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = round_up(off + bytes, 256);
+    return at;
+  };
+  const size_t n = sh->n, D = sh->D, Fs = sh->Fs, t = T, tp = round_up8(T), es = esize(sh->dt);
+  if (!backward) {
+    w.H = take(n * t * Fs * es);
+    if (mode == TPMLP_FAITHFUL) w.Yp = take(n * t * D * 4);
+  } else {
+    w.P = take(n * t * Fs * 4);
+    w.dH = take(n * t * Fs * 4);
+    if (sh->dt == TPMLP_BF16) {
+      w.Xt = take(D * tp * 2);
+      w.dYt = take(D * tp * 2);
+      w.Ht = take(n * Fs * tp * 2);
+      w.dP = take(n * t * Fs * 2);
+      w.dPt = take(n * Fs * tp * 2);
+    }
+    if (mode == TPMLP_FAITHFUL) w.dXp = take(n * t * D * 4);
+  }
+  w.total = off;
+  return w;
+}
+
+template <typename T>
+T* at(void* base, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+int map_or_fail(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t pitch, int box_rows,
+                const char* what) {
+  if (!make_operand_map(m, base, rows, cols, pitch, box_rows))
+    return fail(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the map of %s [%lld x %lld]", what,
+                static_cast<long long>(rows), static_cast<long long>(cols));
+  return TPMLP_OK;
+}
+
+// ----------------------------------------------------------- step launchers
+
+// H_i = GeLU(X A_i) for every shard.
+int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaStream_t s) {
+  const int64_t D = sh->D, Fs = sh->Fs;
+  if (sh->dt == TPMLP_BF16) {
+    CUtensorMap mx;
+    int rc = map_or_fail(&mx, X, T, D, D, kTcBoxRowsA, "X");
+    if (rc) return rc;
+    TcGemm g{};
+    g.groups = sh->n;
+    for (int i = 0; i < sh->n; ++i) {
+      g.map_a[i] = &mx;
+      g.map_b[i] = &sh->map_At[i];
+      g.out[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
+    }
+    g.ldo = Fs;
+    g.M = static_cast<int>(T);
+    g.N = static_cast<int>(Fs);
+    g.K = static_cast<int>(D);
+    g.epi = kEpiGeluBf16;
+    TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
+    return TPMLP_OK;
+  }
+  for (int i = 0; i < sh->n; ++i) {
+    SimtGemm g{static_cast<const float*>(X), D, 1, static_cast<const float*>(sh->desc[i].A), Fs, 1,
+               static_cast<float*>(H) + static_cast<size_t>(i) * T * Fs, Fs, static_cast<int>(T),
+               static_cast<int>(Fs), static_cast<int>(D), kSimtGelu};
+    TRY_CUDA(launch_simt_gemm(g, s));
+  }
+  return TPMLP_OK;
+}
+
+// Y_i = H_i B_i into Yp (chain = 0), or Y = sum_i H_i B_i into Y (chain = 1).
+int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int chain, cudaStream_t s) {
+  const int64_t D = sh->D, Fs = sh->Fs;
+  if (sh->dt == TPMLP_BF16) {
+    std::vector<CUtensorMap> mh(sh->n);
+    TcGemm g{};
+    g.groups = sh->n;
+    for (int i = 0; i < sh->n; ++i) {
+      int rc = map_or_fail(&mh[i], at<uint16_t>(const_cast<void*>(H), 0) + static_cast<size_t>(i) * T * Fs, T, Fs,
+                           Fs, kTcBoxRowsA, "H_i");
+      if (rc) return rc;
+      g.map_a[i] = &mh[i];
+      g.map_b[i] = &sh->map_Bt[i];
+      g.out[i] = chain ? out : static_cast<void*>(static_cast<float*>(out) + static_cast<size_t>(i) * T * D);
+    }
+    g.ldo = D;
+    g.M = static_cast<int>(T);
+    g.N = static_cast<int>(D);
+    g.K = static_cast<int>(Fs);
+    g.chain = chain;
+    g.epi = kEpiF32;
+    TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
+    return TPMLP_OK;
+  }
+  for (int i = 0; i < sh->n; ++i) {
+    float* C = chain ? static_cast<float*>(out) : static_cast<float*>(out) + static_cast<size_t>(i) * T * D;
+    SimtGemm g{static_cast<const float*>(H) + static_cast<size_t>(i) * T * Fs, Fs, 1,
+               static_cast<const float*>(sh->desc[i].B), D, 1, C, D, static_cast<int>(T), static_cast<int>(D),
+               static_cast<int>(Fs), (chain && i > 0) ? kSimtAccumulate : kSimtStore};
+    TRY_CUDA(launch_simt_gemm(g, s));
+  }
+  return TPMLP_OK;
+}
+
+int check_common(const tpmlp_shards* sh, int64_t T) {
+  if (!sh) return fail(TPMLP_ERR_ARG, "shards handle is NULL");
+  if (T < 1) return fail(TPMLP_ERR_ARG, "T = %lld must be >= 1", static_cast<long long>(T));
+  if (T > (int64_t(1) << 30)) return fail(TPMLP_ERR_ARG, "T = %lld is too large", static_cast<long long>(T));
+  return TPMLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tpmlp_version(void) { return (1 << 16) | 0; }
+
+const char* tpmlp_last_error(void) { return g_msg; }
+
+int tpmlp_check_status(tpmlp_stream_t stream) {
+  int v = 0;
+  TRY_CUDA(read_and_clear_status(&v, stream));
+  if (v) return fail(TPMLP_ERR_TIMEOUT, "a device-side wait ran out of time (site %d)", v);
+  return TPMLP_OK;
+}
+
+int tpmlp_gelu(const void* x, void* y, int64_t n, tpmlp_dtype dt, tpmlp_stream_t stream) {
+  if (n < 0) return fail(TPMLP_ERR_ARG, "n = %lld must be >= 0", static_cast<long long>(n));
+  if (dt != TPMLP_F32 && dt != TPMLP_BF16) return fail(TPMLP_ERR_ARG, "unknown dtype %d", int(dt));
+  if (n == 0) return TPMLP_OK;
+  if (!x || !y) return fail(TPMLP_ERR_ARG, "x and y must not be NULL");
+  if (!aligned16(x) || !aligned16(y)) return fail(TPMLP_ERR_ALIGN, "x and y must be 16-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  TRY_CUDA(launch_gelu(x, y, n, dt == TPMLP_BF16, stream));
+  return TPMLP_OK;
+}
+
+int tpmlp_shard(const void* A, const void* B, int64_t D, int64_t F, int n, tpmlp_dtype dt, tpmlp_stream_t stream,
+                tpmlp_shards** out) {
+  if (!out) return fail(TPMLP_ERR_ARG, "out must not be NULL");
+  *out = nullptr;
+  if (!A || !B) return fail(TPMLP_ERR_ARG, "A and B must not be NULL");
+  if (D < 1 || F < 1) return fail(TPMLP_ERR_ARG, "D and F must be >= 1");
+  if (n < 1) return fail(TPMLP_ERR_ARG, "n = %d must be >= 1", n);
+  if (dt != TPMLP_F32 && dt != TPMLP_BF16) return fail(TPMLP_ERR_ARG, "unknown dtype %d", int(dt));
+  if (F % n != 0)
+    return fail(TPMLP_ERR_DIVISIBILITY, "F = %lld is not divisible by n = %d", static_cast<long long>(F), n);
+  const int64_t Fs = F / n;
+  if (dt == TPMLP_BF16) {
+    if (n > TPMLP_MAX_SHARDS)
+      return fail(TPMLP_ERR_UNSUPPORTED, "bf16 supports at most %d shards, got %d", TPMLP_MAX_SHARDS, n);
+    if (D % 8 != 0 || Fs % 8 != 0)
+      return fail(TPMLP_ERR_SHAPE, "bf16 needs D and F/n to be multiples of 8 (D = %lld, F/n = %lld)",
+                  static_cast<long long>(D), static_cast<long long>(Fs));
+    if (D > (int64_t(1) << 30) || Fs > (int64_t(1) << 30)) return fail(TPMLP_ERR_SHAPE, "D or F/n too large");
+  }
+  if (!aligned16(A) || !aligned16(B)) return fail(TPMLP_ERR_ALIGN, "A and B must be 16-byte aligned");
+  int dev = -1;
+  int rc = check_device(&dev);
+  if (rc) return rc;
+
+  tpmlp_shards* sh = new tpmlp_shards();
+  sh->device = dev;
+  sh->D = D;
+  sh->F = F;
+  sh->Fs = Fs;
+  sh->n = n;
+  sh->dt = dt;
+  const size_t es = esize(dt), blk = round_up(static_cast<size_t>(D) * Fs * es, 256);
+  const int layouts = dt == TPMLP_BF16 ? 4 : 2;
+  cudaError_t e = cudaMalloc(&sh->mem, blk * layouts * n);
+  if (e == cudaSuccess) e = cudaMalloc(&sh->d_table, sizeof(ShardDesc) * n);
+  if (e != cudaSuccess) {
+    tpmlp_shards_free(sh);
+    return fail(TPMLP_ERR_CUDA, "cudaMalloc of the shards failed: %s", cudaGetErrorString(e));
+  }
+  sh->desc.resize(n);
+  for (int i = 0; i < n; ++i) {
+    char* base = static_cast<char*>(sh->mem) + blk * layouts * i;  // shard i's own block
+    sh->desc[i].A = base;
+    sh->desc[i].B = base + blk;
+    sh->desc[i].At = layouts == 4 ? base + 2 * blk : nullptr;
+    sh->desc[i].Bt = layouts == 4 ? base + 3 * blk : nullptr;
+    sh->desc[i].f0 = i * Fs;
+  }
+  e = cudaMemcpyAsync(sh->d_table, sh->desc.data(), sizeof(ShardDesc) * n, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = launch_shard_copy(A, B, sh->d_table, D, F, Fs, static_cast<int>(es), stream);
+  if (dt == TPMLP_BF16) {
+    for (int i = 0; i < n && e == cudaSuccess; ++i) {
+      e = launch_transpose_u16(sh->desc[i].A, D, Fs, Fs, sh->desc[i].At, D, stream);  // A_i^T [Fs, D]
+      if (e == cudaSuccess) e = launch_transpose_u16(sh->desc[i].B, Fs, D, D, sh->desc[i].Bt, Fs, stream);  // B_i^T
+    }
+  }
+  if (e != cudaSuccess) {
+    cudaStreamSynchronize(stream);
+    tpmlp_shards_free(sh);
+    return fail(TPMLP_ERR_CUDA, "shard copy failed: %s", cudaGetErrorString(e));
+  }
+  if (dt == TPMLP_BF16) {
+    sh->map_At.resize(n);
+    sh->map_Bt.resize(n);
+    sh->map_B.resize(n);
+    sh->map_A.resize(n);
+    for (int i = 0; i < n; ++i) {
+      const ShardDesc& d = sh->desc[i];
+      rc = map_or_fail(&sh->map_At[i], d.At, Fs, D, D, tc_box_rows_b(static_cast<int>(Fs)), "A_i^T");
+      if (!rc) rc = map_or_fail(&sh->map_Bt[i], d.Bt, D, Fs, Fs, tc_box_rows_b(static_cast<int>(D)), "B_i^T");
+      if (!rc) rc = map_or_fail(&sh->map_B[i], d.B, Fs, D, D, tc_box_rows_b(static_cast<int>(Fs)), "B_i");
+      if (!rc) rc = map_or_fail(&sh->map_A[i], d.A, D, Fs, Fs, tc_box_rows_b(static_cast<int>(D)), "A_i");
+      if (rc) {
+        cudaStreamSynchronize(stream);
+        tpmlp_shards_free(sh);
+        return rc;
+      }
+    }
+  }
+  *out = sh;
+  return TPMLP_OK;
+}
+
+int tpmlp_shard_info(const tpmlp_shards* sh, int64_t* D, int64_t* F, int* n, tpmlp_dtype* dt) {
+  if (!sh) return fail(TPMLP_ERR_ARG, "shards handle is NULL");
+  if (D) *D = sh->D;
+  if (F) *F = sh->F;
+  if (n) *n = sh->n;
+  if (dt) *dt = sh->dt;
+  return TPMLP_OK;
+}
+
+int tpmlp_shard_get(const tpmlp_shards* sh, int i, const void** A_i, const void** B_i) {
+  if (!sh) return fail(TPMLP_ERR_ARG, "shards handle is NULL");
+  if (i < 0 || i >= sh->n) return fail(TPMLP_ERR_ARG, "shard index %d out of range [0, %d)", i, sh->n);
+  if (A_i) *A_i = sh->desc[i].A;
+  if (B_i) *B_i = sh->desc[i].B;
+  return TPMLP_OK;
+}
+
+int tpmlp_shard_get_transposed(const tpmlp_shards* sh, int i, const void** At_i, const void** Bt_i) {
+  if (!sh) return fail(TPMLP_ERR_ARG, "shards handle is NULL");
+  if (i < 0 || i >= sh->n) return fail(TPMLP_ERR_ARG, "shard index %d out of range [0, %d)", i, sh->n);
+  if (sh->dt != TPMLP_BF16) return fail(TPMLP_ERR_UNSUPPORTED, "fp32 shards keep no transposed copies");
+  if (At_i) *At_i = sh->desc[i].At;
+  if (Bt_i) *Bt_i = sh->desc[i].Bt;
+  return TPMLP_OK;
+}
+
+void tpmlp_shards_free(tpmlp_shards* sh) {
+  if (!sh) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != sh->device) cudaSetDevice(sh->device);
+  cudaDeviceSynchronize();
+  if (sh->mem) cudaFree(sh->mem);
+  if (sh->d_table) cudaFree(sh->d_table);
+  if (prev >= 0 && prev != sh->device) cudaSetDevice(prev);
+  delete sh;
+}
+
+size_t tpmlp_workspace_bytes(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  if (!sh || T < 1 || (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED)) return 0;
+  return plan_workspace(T, sh, mode, backward).total;
+}
+
+int tpmlp_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (!X || !H) return fail(TPMLP_ERR_ARG, "X and H must not be NULL");
+  if (!aligned16(X) || !aligned16(H)) return fail(TPMLP_ERR_ALIGN, "X and H must be 16-byte aligned");
+  if ((rc = check_handle_device(sh))) return rc;
+  return run_hidden(X, T, sh, H, stream);
+}
+
+int tpmlp_partials(const void* H, int64_t T, const tpmlp_shards* sh, void* Yp, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (!H || !Yp) return fail(TPMLP_ERR_ARG, "H and Yp must not be NULL");
+  if (!aligned16(H) || !aligned16(Yp)) return fail(TPMLP_ERR_ALIGN, "H and Yp must be 16-byte aligned");
+  if ((rc = check_handle_device(sh))) return rc;
+  return run_second(H, T, sh, Yp, 0, stream);
+}
+
+int tpmlp_allreduce(const void* Yp, int n, int64_t count, void* Y, tpmlp_stream_t stream) {
+  if (n < 1) return fail(TPMLP_ERR_ARG, "n = %d must be >= 1", n);
+  if (count < 0) return fail(TPMLP_ERR_ARG, "count must be >= 0");
+  if (count == 0) return TPMLP_OK;
+  if (!Yp || !Y) return fail(TPMLP_ERR_ARG, "Yp and Y must not be NULL");
+  if (!aligned16(Yp) || !aligned16(Y)) return fail(TPMLP_ERR_ALIGN, "Yp and Y must be 16-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  TRY_CUDA(launch_allreduce(static_cast<const float*>(Yp), n, count, static_cast<float*>(Y), stream));
+  return TPMLP_OK;
+}
+
+int tpmlp_fused_sum(const void* H, int64_t T, const tpmlp_shards* sh, void* Y, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (!H || !Y) return fail(TPMLP_ERR_ARG, "H and Y must not be NULL");
+  if (!aligned16(H) || !aligned16(Y)) return fail(TPMLP_ERR_ALIGN, "H and Y must be 16-byte aligned");
+  if ((rc = check_handle_device(sh))) return rc;
+  return run_second(H, T, sh, Y, 1, stream);
+}
+
+int tpmlp_forward(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, tpmlp_mode mode, void* ws,
+                  size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if (!X || !Y || !ws) return fail(TPMLP_ERR_ARG, "X, Y and workspace must not be NULL");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "X, Y and workspace must be 16-byte aligned");
+  const WsPlan w = plan_workspace(T, sh, mode, 0);
+  if (ws_bytes < w.total)
+    return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  void* H = at<char>(ws, w.H);
+  if ((rc = run_hidden(X, T, sh, H, stream))) return rc;
+  if (mode == TPMLP_FUSED) return run_second(H, T, sh, Y, 1, stream);
+  float* Yp = at<float>(ws, w.Yp);
+  if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
+  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
+  return TPMLP_OK;
+}
+
+int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards* sh, void* dX, void* const* dA,
+                   void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if (!X || !dY || !dX || !dA || !dB || !ws) return fail(TPMLP_ERR_ARG, "a required pointer is NULL");
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(dX) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "X, dY, dX and workspace must be 16-byte aligned");
+  for (int i = 0; i < sh->n; ++i) {
+    if (!dA[i] || !dB[i]) return fail(TPMLP_ERR_ARG, "dA[%d] or dB[%d] is NULL", i, i);
+    if (!aligned16(dA[i]) || !aligned16(dB[i])) return fail(TPMLP_ERR_ALIGN, "dA[%d], dB[%d] must be 16-byte aligned", i, i);
+  }
+  const WsPlan w = plan_workspace(T, sh, mode, 1);
+  if (ws_bytes < w.total)
+    return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  const int n = sh->n;
+  const int64_t D = sh->D, Fs = sh->Fs;
+  float* P = at<float>(ws, w.P);
+  float* dH = at<float>(ws, w.dH);
+  float* dXp = mode == TPMLP_FAITHFUL ? at<float>(ws, w.dXp) : nullptr;
+  cudaStream_t s = stream;
+
+  if (sh->dt == TPMLP_F32) {
+    const float* x = static_cast<const float*>(X);
+    const float* dy = static_cast<const float*>(dY);
+    for (int i = 0; i < n; ++i) {
+      const float* Ai = static_cast<const float*>(sh->desc[i].A);
+      const float* Bi = static_cast<const float*>(sh->desc[i].B);
+      float* Pi = P + static_cast<size_t>(i) * T * Fs;
+      float* dHi = dH + static_cast<size_t>(i) * T * Fs;
+      const int t = static_cast<int>(T), d = static_cast<int>(D), fs = static_cast<int>(Fs);
+      // P_i = X A_i ; dH_i = dY B_i^T
+      TRY_CUDA(launch_simt_gemm(SimtGemm{x, D, 1, Ai, Fs, 1, Pi, Fs, t, fs, d, kSimtStore}, s));
+      TRY_CUDA(launch_simt_gemm(SimtGemm{dy, D, 1, Bi, 1, D, dHi, Fs, t, fs, d, kSimtStore}, s));
+    }
+    // P <- H = GeLU(P), dH <- dP = dH * GeLU'(P)
+    TRY_CUDA(launch_bwd_act_f32(P, dH, static_cast<int64_t>(n) * T * Fs, s));
+    for (int i = 0; i < n; ++i) {
+      const float* Ai = static_cast<const float*>(sh->desc[i].A);
+      const float* Hi = P + static_cast<size_t>(i) * T * Fs;
+      const float* dPi = dH + static_cast<size_t>(i) * T * Fs;
+      const int t = static_cast<int>(T), d = static_cast<int>(D), fs = static_cast<int>(Fs);
+      // dB_i = H_i^T dY ; dA_i = X^T dP_i ; dX_i = dP_i A_i^T
+      TRY_CUDA(launch_simt_gemm(SimtGemm{Hi, 1, Fs, dy, D, 1, static_cast<float*>(dB[i]), D, fs, d, t, kSimtStore}, s));
+      TRY_CUDA(launch_simt_gemm(SimtGemm{x, 1, D, dPi, Fs, 1, static_cast<float*>(dA[i]), Fs, d, fs, t, kSimtStore}, s));
+      float* C = dXp ? dXp + static_cast<size_t>(i) * T * D : static_cast<float*>(dX);
+      const int epi = (!dXp && i > 0) ? kSimtAccumulate : kSimtStore;
+      TRY_CUDA(launch_simt_gemm(SimtGemm{dPi, Fs, 1, Ai, 1, Fs, C, D, t, d, fs, epi}, s));
+    }
+    if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
+    return TPMLP_OK;
+  }
+
+  // bf16: tensor-core products on K-major operands.
+  const int64_t Tp = round_up8(T);
+  void* Xt = at<char>(ws, w.Xt);
+  void* dYt = at<char>(ws, w.dYt);
+  uint16_t* Ht = at<uint16_t>(ws, w.Ht);
+  uint16_t* dP = at<uint16_t>(ws, w.dP);
+  uint16_t* dPt = at<uint16_t>(ws, w.dPt);
+  TRY_CUDA(launch_transpose_u16(X, T, D, D, Xt, Tp, s));    // X^T  [D, Tp]
+  TRY_CUDA(launch_transpose_u16(dY, T, D, D, dYt, Tp, s));  // dY^T [D, Tp]
+
+  CUtensorMap mX, mdY, mXt, mdYt;
+  if ((rc = map_or_fail(&mX, X, T, D, D, kTcBoxRowsA, "X"))) return rc;
+  if ((rc = map_or_fail(&mdY, dY, T, D, D, kTcBoxRowsA, "dY"))) return rc;
+  if ((rc = map_or_fail(&mXt, Xt, D, T, Tp, kTcBoxRowsA, "X^T"))) return rc;
+  if ((rc = map_or_fail(&mdYt, dYt, D, T, Tp, tc_box_rows_b(static_cast<int>(D)), "dY^T"))) return rc;
+  std::vector<CUtensorMap> mHt(n), mdPt(n), mdP(n);
+  for (int i = 0; i < n; ++i) {
+    if ((rc = map_or_fail(&mHt[i], Ht + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp, kTcBoxRowsA, "H_i^T"))) return rc;
+    if ((rc = map_or_fail(&mdPt[i], dPt + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp,
+                          tc_box_rows_b(static_cast<int>(Fs)), "dP_i^T")))
+      return rc;
+    if ((rc = map_or_fail(&mdP[i], dP + static_cast<size_t>(i) * T * Fs, T, Fs, Fs, kTcBoxRowsA, "dP_i"))) return rc;
+  }
+  const uint64_t wl = wait_limit_ns();
+  TcGemm g{};
+  g.groups = n;
+  // P_i = X A_i (recompute) and dH_i = dY B_i^T, fp32.
+  for (int i = 0; i < n; ++i) {
+    g.map_a[i] = &mX;
+    g.map_b[i] = &sh->map_At[i];
+    g.out[i] = P + static_cast<size_t>(i) * T * Fs;
+  }
+  g.ldo = Fs;
+  g.M = static_cast<int>(T);
+  g.N = static_cast<int>(Fs);
+  g.K = static_cast<int>(D);
+  g.epi = kEpiF32;
+  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  for (int i = 0; i < n; ++i) {
+    g.map_a[i] = &mdY;
+    g.map_b[i] = &sh->map_B[i];
+    g.out[i] = dH + static_cast<size_t>(i) * T * Fs;
+  }
+  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  // H_i^T, dP_i, dP_i^T in bf16.
+  TRY_CUDA(launch_bwd_act_bf16(P, dH, n, T, Fs, Tp, Ht, dP, dPt, s));
+  // dB_i = H_i^T dY: [Fs, D], K = T.
+  for (int i = 0; i < n; ++i) {
+    g.map_a[i] = &mHt[i];
+    g.map_b[i] = &mdYt;
+    g.out[i] = dB[i];
+  }
+  g.ldo = D;
+  g.M = static_cast<int>(Fs);
+  g.N = static_cast<int>(D);
+  g.K = static_cast<int>(T);
+  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  // dA_i = X^T dP_i: [D, Fs], K = T.
+  for (int i = 0; i < n; ++i) {
+    g.map_a[i] = &mXt;
+    g.map_b[i] = &mdPt[i];
+    g.out[i] = dA[i];
+  }
+  g.ldo = Fs;
+  g.M = static_cast<int>(D);
+  g.N = static_cast<int>(Fs);
+  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  // dX = sum_i dP_i A_i^T: [T, D], K = Fs.
+  for (int i = 0; i < n; ++i) {
+    g.map_a[i] = &mdP[i];
+    g.map_b[i] = &sh->map_A[i];
+    g.out[i] = dXp ? static_cast<void*>(dXp + static_cast<size_t>(i) * T * D) : dX;
+  }
+  g.ldo = D;
+  g.M = static_cast<int>(T);
+  g.N = static_cast<int>(D);
+  g.K = static_cast<int>(Fs);
+  g.chain = dXp ? 0 : 1;
+  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
+  return TPMLP_OK;
+}
+
+int tpmlp_selftest_wait_timeout(int limit_ms, tpmlp_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 10000) return fail(TPMLP_ERR_ARG, "limit_ms = %d outside 1..10000", limit_ms);
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  TRY_CUDA(launch_wait_selftest(static_cast<uint64_t>(limit_ms) * 1000000ull, stream));
+  return TPMLP_OK;
+}
+
+}  // extern "C"

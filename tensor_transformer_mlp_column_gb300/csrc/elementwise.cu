@@ -1,0 +1,269 @@
+// elementwise.cu — the memory-bound kernels of the path: standalone GeLU, the
+// shard-ordered partial-sum reduction (the simulated all-reduce), the shard
+// slicing copies, 2-byte transposes, the backward activation step, and the
+// bounded-wait self test.
+#include "device.cuh"
+#include "internal.h"
+
+namespace tpmlp {
+
+namespace {
+
+constexpr int kEwThreads = 256;
+
+int ew_grid(int64_t work_items, int per_thread) {
+  const int64_t want = (work_items + int64_t(kEwThreads) * per_thread - 1) / (int64_t(kEwThreads) * per_thread);
+  const int64_t cap = int64_t(num_sms()) * 8;  // 8 resident blocks of 256 per SM
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+// ------------------------------------------------------------------ GeLU
+
+__global__ void gelu_f32_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t n4 = n / 4;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 v = reinterpret_cast<const float4*>(x)[i];
+    v.x = gelu_fast(v.x);
+    v.y = gelu_fast(v.y);
+    v.z = gelu_fast(v.z);
+    v.w = gelu_fast(v.w);
+    reinterpret_cast<float4*>(y)[i] = v;
+  }
+  for (int64_t i = n4 * 4 + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) y[i] = gelu_fast(x[i]);
+}
+
+__global__ void gelu_bf16_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloat16* __restrict__ y, int64_t n) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t n8 = n / 8;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
+    uint4 w = reinterpret_cast<const uint4*>(x)[i];
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float2 f = __bfloat1622float2(h[j]);
+      h[j] = __floats2bfloat162_rn(gelu_fast(f.x), gelu_fast(f.y));
+    }
+    reinterpret_cast<uint4*>(y)[i] = w;
+  }
+  for (int64_t i = n8 * 8 + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    y[i] = __float2bfloat16_rn(gelu_fast(__bfloat162float(x[i])));
+}
+
+// ------------------------------------------------------------------ all-reduce
+
+// Y[j] = ((Yp[0][j] + Yp[1][j]) + Yp[2][j]) + ... in fp32, shard order fixed.
+// Each thread owns float4 columns of the [n][count] block; the n loads of one
+// float4 are issued before the adds so n*16 bytes per thread are in flight.
+// Partials are read once (streaming loads), Y is written once.
+template <int NMAX>
+__global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __restrict__ Yp, int n, int64_t count,
+                                                               float* __restrict__ Y) {
+  const int64_t n4 = count / 4;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const float4* P = reinterpret_cast<const float4*>(Yp);
+  const int64_t shard_stride4 = count / 4;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 v[NMAX];
+#pragma unroll
+    for (int s = 0; s < NMAX; ++s)
+      if (s < n) v[s] = __ldcs(P + s * shard_stride4 + i);
+    float4 acc = v[0];
+#pragma unroll
+    for (int s = 1; s < NMAX; ++s) {
+      if (s < n) {
+        acc.x += v[s].x;
+        acc.y += v[s].y;
+        acc.z += v[s].z;
+        acc.w += v[s].w;
+      }
+    }
+    __stcs(reinterpret_cast<float4*>(Y) + i, acc);
+  }
+  // Tail of count % 4 elements (never reached when count is a multiple of 4).
+  for (int64_t j = n4 * 4 + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
+    float acc = Yp[j];
+    for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + j];
+    Y[j] = acc;
+  }
+}
+
+// Any n: the same order, shards taken from memory one by one.
+__global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, float* __restrict__ Y) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
+    float acc = Yp[j];
+    for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + j];
+    Y[j] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ shard copies
+
+// A_i[r, c] = A[r, f0 + c] and B_i[r, c] = B[f0 + r, c]; one element per thread
+// step, grid-stride over the D*F elements of A and of B. Every shard reads its
+// destinations from the device descriptor table.
+template <typename E>
+__global__ void shard_copy_kernel(const E* __restrict__ A, const E* __restrict__ B, const ShardDesc* __restrict__ tab,
+                                  int64_t D, int64_t F, int64_t Fs) {
+  const int64_t total = D * F;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += stride) {
+    {  // A: element (r, f) of [D, F]
+      const int64_t r = e / F, f = e % F;
+      const int64_t i = f / Fs, c = f % Fs;
+      static_cast<E*>(tab[i].A)[r * Fs + c] = A[e];
+    }
+    {  // B: element (f, c) of [F, D]
+      const int64_t f = e / D, c = e % D;
+      const int64_t i = f / Fs, r = f % Fs;
+      static_cast<E*>(tab[i].B)[r * D + c] = B[e];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ transpose
+
+// out[c, r] = in[r, c] for 2-byte elements, 64 x 64 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_u16_kernel(const uint16_t* __restrict__ in, int64_t rows,
+                                                            int64_t cols, int64_t ldi, uint16_t* __restrict__ out,
+                                                            int64_t ldo) {
+  __shared__ uint16_t tile[64][66];
+  const int64_t r0 = int64_t(blockIdx.y) * 64, c0 = int64_t(blockIdx.x) * 64;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  // Read 64 rows x 64 columns: each thread moves 2 adjacent columns per row.
+  for (int rr = ty; rr < 64; rr += 8) {
+    const int64_t r = r0 + rr, c = c0 + 2 * tx;
+    uint16_t a = 0, b = 0;
+    if (r < rows) {
+      if (c < cols) a = in[r * ldi + c];
+      if (c + 1 < cols) b = in[r * ldi + c + 1];
+    }
+    tile[rr][2 * tx] = a;
+    tile[rr][2 * tx + 1] = b;
+  }
+  __syncthreads();
+  for (int cc = ty; cc < 64; cc += 8) {
+    const int64_t c = c0 + cc, r = r0 + 2 * tx;
+    if (c < cols) {
+      if (r < rows) out[c * ldo + r] = tile[2 * tx][cc];
+      if (r + 1 < rows) out[c * ldo + r + 1] = tile[2 * tx + 1][cc];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ backward activation
+
+// For element (i, t, f): p = P, g = dH; H = GeLU(p), dP = g * GeLU'(p).
+// Writes dP row-major and H^T, dP^T transposed ([i][f][t], row pitch ldt),
+// through a 32 x 32 shared tile so both layouts are written coalesced.
+__global__ void __launch_bounds__(256) bwd_act_bf16_kernel(const float* __restrict__ P, const float* __restrict__ dH,
+                                                           int64_t T, int64_t Fs, int64_t ldt,
+                                                           __nv_bfloat16* __restrict__ Ht, __nv_bfloat16* __restrict__ dP,
+                                                           __nv_bfloat16* __restrict__ dPt) {
+  __shared__ __nv_bfloat16 sh[32][33];
+  __shared__ __nv_bfloat16 sd[32][33];
+  const int i = blockIdx.z;
+  const int64_t t0 = int64_t(blockIdx.y) * 32, f0 = int64_t(blockIdx.x) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const float* Pi = P + int64_t(i) * T * Fs;
+  const float* dHi = dH + int64_t(i) * T * Fs;
+  for (int tt = ty; tt < 32; tt += 8) {
+    const int64_t t = t0 + tt, f = f0 + tx;
+    __nv_bfloat16 hv = __float2bfloat16_rn(0.f), dv = hv;
+    if (t < T && f < Fs) {
+      float g, dg;
+      gelu_and_grad_fast(Pi[t * Fs + f], g, dg);
+      hv = __float2bfloat16_rn(g);
+      dv = __float2bfloat16_rn(dHi[t * Fs + f] * dg);
+      dP[int64_t(i) * T * Fs + t * Fs + f] = dv;
+    }
+    sh[tt][tx] = hv;
+    sd[tt][tx] = dv;
+  }
+  __syncthreads();
+  for (int ff = ty; ff < 32; ff += 8) {
+    const int64_t f = f0 + ff, t = t0 + tx;
+    if (t < T && f < Fs) {
+      const int64_t o = int64_t(i) * Fs * ldt + f * ldt + t;
+      Ht[o] = sh[tx][ff];
+      dPt[o] = sd[tx][ff];
+    }
+  }
+}
+
+__global__ void bwd_act_f32_kernel(float* __restrict__ P, float* __restrict__ dH, int64_t count) {
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
+    float g, dg;
+    gelu_and_grad_fast(P[j], g, dg);
+    P[j] = g;
+    dH[j] = dH[j] * dg;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (is_bf16) {
+    gelu_bf16_kernel<<<ew_grid(n, 8), kEwThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(x),
+                                                         static_cast<__nv_bfloat16*>(y), n);
+  } else {
+    gelu_f32_kernel<<<ew_grid(n, 4), kEwThreads, 0, s>>>(static_cast<const float*>(x), static_cast<float*>(y), n);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s) {
+  if (count <= 0) return cudaSuccess;
+  const int g = ew_grid(count, 4);
+  if (count % 4 != 0)  // shard blocks would not be 16-byte aligned
+    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, Y);
+  else if (n <= 4)
+    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+  else if (n <= 8)
+    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+  else if (n <= 16)
+    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+  else
+    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, Y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_table, int64_t D, int64_t F,
+                              int64_t Fs, int elem_bytes, cudaStream_t s) {
+  const int g = ew_grid(D * F, 1);
+  if (elem_bytes == 2)
+    shard_copy_kernel<uint16_t><<<g, kEwThreads, 0, s>>>(static_cast<const uint16_t*>(A),
+                                                          static_cast<const uint16_t*>(B), d_table, D, F, Fs);
+  else
+    shard_copy_kernel<uint32_t><<<g, kEwThreads, 0, s>>>(static_cast<const uint32_t*>(A),
+                                                          static_cast<const uint32_t*>(B), d_table, D, F, Fs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int64_t ldi, void* out, int64_t ldo,
+                                 cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+  transpose_u16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), rows, cols, ldi,
+                                            static_cast<uint16_t*>(out), ldo);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_act_bf16(const float* P, const float* dH, int n, int64_t T, int64_t Fs, int64_t ldt, void* Ht,
+                                void* dP, void* dPt, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>((Fs + 31) / 32), static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>(n));
+  bwd_act_bf16_kernel<<<grid, 256, 0, s>>>(P, dH, T, Fs, ldt, static_cast<__nv_bfloat16*>(Ht),
+                                           static_cast<__nv_bfloat16*>(dP), static_cast<__nv_bfloat16*>(dPt));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_act_f32(float* P, float* dH, int64_t count, cudaStream_t s) {
+  if (count <= 0) return cudaSuccess;
+  bwd_act_f32_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(P, dH, count);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

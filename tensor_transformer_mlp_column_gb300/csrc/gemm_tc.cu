@@ -1,0 +1,376 @@
+// gemm_tc.cu — persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// Serves every product of the tensor-parallel MLP in bf16 (X A_i with the
+// GeLU fused into the epilogue; H_i B_i as fp32 partials; the shard-ordered
+// fused sum; the backward products). One CTA per SM loops over output tiles
+// of BM x BN:
+//   warp 0, lane 0 : TMA producer — fills a STAGES-deep ring of shared-memory
+//                    stages (A box 128 x 64, B box BN x 64, 128-byte swizzle)
+//   warp 1         : allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN,
+//                    K=16 per instruction) into one of two TMEM accumulators
+//   warps 2..5     : epilogue — tcgen05.ld the accumulator (warp w reads TMEM
+//                    lanes 32*(w%4)..+31 = tile rows), apply the output
+//                    treatment and store to global memory
+// The two accumulators let the epilogue of tile j overlap the mainloop of
+// tile j+1. Every mbarrier wait is bounded; on a timeout the CTA raises an
+// abort flag, all roles leave their loops, in-flight copies and MMAs are
+// drained and TMEM is freed before the CTA exits.
+#include "device.cuh"
+#include "internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+namespace tpmlp {
+
+// Per-device status word: a kernel whose bounded wait ran out of time stores
+// the wait's site code here. Read and cleared by read_and_clear_status().
+__device__ int g_status = 0;
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;
+
+struct KParams {
+  CUtensorMap map_a[kMaxGroups];
+  CUtensorMap map_b[kMaxGroups];
+  void* out[kMaxGroups];
+  int64_t ldo;
+  int M, N;
+  int groups;
+  int chain;
+  int m_blocks, n_blocks, k_blocks;
+  int tiles;
+  uint64_t wait_ns;
+  int inject;
+};
+
+template <int BN>
+struct Cfg {
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
+  static constexpr size_t SMEM = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + 256 /*barriers*/;
+};
+
+__device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
+  const int per_group = p.m_blocks * p.n_blocks;
+  g = p.chain ? 0 : tile / per_group;
+  const int r = p.chain ? tile : tile % per_group;
+  mb = r / p.n_blocks;  // consecutive tiles walk N first, so CTAs running together share A panels
+  nb = r % p.n_blocks;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);
+      mbar_init(acc_empty + b, 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    const int ng = p.groups;
+    for (int g = 0; g < ng; ++g) {
+      tma_prefetch_desc(&p.map_a[g]);
+      tma_prefetch_desc(&p.map_b[g]);
+    }
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.wait_ns, &g_status};
+  const int kb_per_tile = p.chain ? p.groups * p.k_blocks : p.k_blocks;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, parity_bits = 0;
+      int fill = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+        int g, mb, nb;
+        decode_tile(p, tile, g, mb, nb);
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
+            ok = false;
+            break;
+          }
+          const int gg = p.chain ? kb / p.k_blocks : g;
+          const int kk = p.chain ? kb % p.k_blocks : kb;
+          ++fill;
+          if (fill != p.inject) {
+            mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
+            tma_load_2d(sA + stage * C::A_BYTES, &p.map_a[gg], kk * BK, mb * BM, full + stage);
+            tma_load_2d(sB + stage * C::B_BYTES, &p.map_b[gg], kk * BK, nb * BN, full + stage);
+            issued |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Leave no copy in flight into this CTA's shared memory.
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued >> s & 1u) wait_drain(full + s, (parity_bits >> s) & 1u, p.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+        if (!wait_bounded(acc_empty + acc, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+                        (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty + stage);  // frees the stage once these MMAs have read it
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(acc_full + acc);  // accumulator complete
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // Let every MMA already issued finish before TMEM is released.
+        tc_commit(drain);
+        wait_drain(drain, 0, p.wait_ns);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;  // the TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
+      int g, mb, nb;
+      decode_tile(p, tile, g, mb, nb);
+      bool ok = wait_bounded(acc_full + acc, acc_phase, guard, kSiteEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after_sync();
+      const int64_t m = int64_t(mb) * BM + row;
+      const bool row_ok = m < p.M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        __syncwarp();  // tcgen05.ld is warp-collective
+        tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
+        if (c + 32 == BN) {
+          tc_fence_before_sync();
+          mbar_arrive(acc_empty + acc);  // accumulator may be overwritten now
+        }
+        const int n0 = nb * BN + c;
+        if (!row_ok || n0 >= p.N) continue;
+        if constexpr (EPI == kEpiGeluBf16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j + 8 <= p.N) {
+              uint4 w;
+              w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
+              w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
+              w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
+              w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
+              *reinterpret_cast<uint4*>(out + 8 * j) = w;
+            }
+          }
+        } else {
+          float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (n0 + 4 * j + 4 <= p.N)
+              *reinterpret_cast<float4*>(out + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int EPI>
+cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
+  using C = Cfg<BN>;
+  auto kern = tc_gemm_kernel<BN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const int grid = kp.tiles < num_sms() ? kp.tiles : num_sms();
+  kern<<<grid, kThreads, C::SMEM, s>>>(kp);
+  return cudaGetLastError();
+}
+
+// Waits on a barrier that expects one arrival that never comes; the bounded
+// wait gives up after limit_ns and records kSiteSelftest.
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitGuard g{&abort_flag, limit_ns, &g_status};
+    wait_bounded(&bar, 0, g, kSiteSelftest);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
+  int zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(s);  // `zero` and `value` are host stack memory
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
+int tc_box_rows_b(int N) { return N <= 128 ? 128 : 256; }
+
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
+                      int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  for (int i = 0; i < g.groups; ++i) {
+    kp.map_a[i] = *g.map_a[i];
+    kp.map_b[i] = *g.map_b[i];
+    kp.out[i] = g.out[i];
+  }
+  const int BN = tc_box_rows_b(g.N);
+  kp.ldo = g.ldo;
+  kp.M = g.M;
+  kp.N = g.N;
+  kp.groups = g.groups;
+  kp.chain = g.chain;
+  kp.m_blocks = (g.M + BM - 1) / BM;
+  kp.n_blocks = (g.N + BN - 1) / BN;
+  kp.k_blocks = (g.K + BK - 1) / BK;
+  kp.tiles = kp.m_blocks * kp.n_blocks * (g.chain ? 1 : g.groups);
+  kp.wait_ns = wait_ns;
+  kp.inject = g.inject;
+  if (kp.tiles == 0) return cudaSuccess;
+  if (BN == 256) return g.epi == kEpiGeluBf16 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<256, kEpiF32>(kp, s);
+  return g.epi == kEpiGeluBf16 ? launch_impl<128, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiF32>(kp, s);
+}
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 1;
+  }
+  return cached[dev];
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,109 @@
+// internal.h — declarations shared by the library's translation units
+// (kernel launchers and the tensor-map helper). Not part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tpmlp {
+
+constexpr int kMaxGroups = 16;  // shards per tensor-core launch (TPMLP_MAX_SHARDS)
+
+// Status codes of the bounded waits (stored in the device status word).
+enum WaitSite : int {
+  kSiteProducer = 1,
+  kSiteMmaFull = 2,
+  kSiteMmaAcc = 3,
+  kSiteEpilogue = 4,
+  kSiteSelftest = 5,
+};
+
+// Output treatment of the tensor-core GEMM.
+enum TcEpilogue : int {
+  kEpiGeluBf16 = 0,  // out bf16 = GeLU(acc)
+  kEpiF32 = 1,       // out fp32 = acc
+};
+
+// One grouped GEMM on the tensor cores: for every group g,
+//   out[g][m, n] = sum_k Aop_g[m, k] * Bop_g[n, k]        (chain == 0)
+// or, with chain == 1, a single output
+//   out[0][m, n] = sum_g sum_k Aop_g[m, k] * Bop_g[n, k]  (groups in order 0..G-1).
+// Both operands are bf16, K-major (row-major with K contiguous), described by
+// 2-D TMA maps made with make_operand_map().
+struct TcGemm {
+  const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
+  const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
+  void* out[kMaxGroups];                 // row-major outputs, row stride ldo
+  int64_t ldo;
+  int M, N, K;
+  int groups;
+  int chain;
+  int epi;     // TcEpilogue
+  int inject;  // test hook, 0 = off
+};
+
+// Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
+// `pitch_elems` (cols contiguous), boxes of 64 columns x box_rows rows and
+// 128-byte swizzling. Returns false if the driver rejects it.
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
+                      int box_rows);
+
+// Box heights of the two operands used by the tensor-core kernel.
+constexpr int kTcBoxRowsA = 128;
+int tc_box_rows_b(int N);
+
+cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s);
+
+// fp32 CUDA-core GEMM with arbitrary element strides:
+//   C[m, n] (op)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]
+enum SimtEpilogue : int { kSimtStore = 0, kSimtGelu = 1, kSimtAccumulate = 2 };
+struct SimtGemm {
+  const float* A;
+  int64_t sam, sak;
+  const float* B;
+  int64_t sbk, sbn;
+  float* C;
+  int64_t ldc;
+  int M, N, K;
+  int epi;
+};
+cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
+
+cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStream_t s);
+cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s);
+
+// Per-shard descriptor kept in device memory by the shards handle.
+struct ShardDesc {
+  void* A;   // A_i  [D, Fs]
+  void* B;   // B_i  [Fs, D]
+  void* At;  // A_i^T [Fs, D] (bf16 only, else null)
+  void* Bt;  // B_i^T [D, Fs] (bf16 only, else null)
+  int64_t f0;  // first column of A (row of B) owned by the shard
+};
+// Copies every shard's slices A_i, B_i out of A [D, F] and B [F, D]; the
+// destinations come from the device descriptor table.
+cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_table, int64_t D, int64_t F,
+                              int64_t Fs, int elem_bytes, cudaStream_t s);
+
+// out[c, r] = in[r, c] for 2-byte elements; in has row pitch ldi, out ldo.
+cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int64_t ldi, void* out, int64_t ldo,
+                                 cudaStream_t s);
+
+// Backward elementwise step of the bf16 path, for n shards at once:
+//   from P [n][T][Fs] and dH [n][T][Fs] (fp32) write H^T [n][Fs][ldt] (bf16),
+//   dP [n][T][Fs] (bf16) and dP^T [n][Fs][ldt] (bf16), where
+//   H = GeLU(P), dP = dH * GeLU'(P).
+cudaError_t launch_bwd_act_bf16(const float* P, const float* dH, int n, int64_t T, int64_t Fs, int64_t ldt,
+                                void* Ht, void* dP, void* dPt, cudaStream_t s);
+// fp32 path: in place, P <- GeLU(P) and dH <- dH * GeLU'(P), count elements.
+cudaError_t launch_bwd_act_f32(float* P, float* dH, int64_t count, cudaStream_t s);
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+
+// Reads and clears the device status word.
+cudaError_t read_and_clear_status(int* value, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace tpmlp

@@ -1,0 +1,126 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library is built (nvcc cross-compiles for sm_103a without a GPU) and
+loaded; every symbol that include/tpmlp.h declares must be exported, and the
+argument checks that run before any CUDA call must return their documented
+status codes. Fake, never-dereferenced device addresses stand in for buffers.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+
+
+@pytest.fixture(scope="module")
+def tp():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import tensor_transformer_mlp_column_gb300 as tp
+
+    return tp
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tpmlp_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls_of_the_problem():
+    names = declared_functions()
+    for required in ["tpmlp_gelu", "tpmlp_shard", "tpmlp_forward", "tpmlp_backward"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(tp):
+    l = tp.lib()
+    names = declared_functions()
+    missing = [n for n in names if not hasattr(l, n)]
+    assert missing == []
+    # and the binding knows the signature of each one
+    assert sorted(tp.SIGNATURES) == names
+
+
+def test_version(tp):
+    assert tp.tpmlp_version() == (1 << 16)
+
+
+FAKE = 0x7F0000000000  # 16-byte aligned, never dereferenced
+
+
+def _shard(tp, A=FAKE, B=FAKE, D=64, F=256, n=4, dt=1):
+    h = ctypes.c_void_p()
+    rc = tp.lib().tpmlp_shard(A, B, D, F, n, dt, None, ctypes.byref(h))
+    return rc, h.value
+
+
+@pytest.mark.parametrize(
+    "kw,code",
+    [
+        (dict(F=256, n=3), "TPMLP_ERR_DIVISIBILITY"),
+        (dict(F=10, n=4, dt=0), "TPMLP_ERR_DIVISIBILITY"),
+        (dict(n=0), "TPMLP_ERR_ARG"),
+        (dict(n=-1), "TPMLP_ERR_ARG"),
+        (dict(D=0), "TPMLP_ERR_ARG"),
+        (dict(A=0), "TPMLP_ERR_ARG"),
+        (dict(B=0), "TPMLP_ERR_ARG"),
+        (dict(dt=7), "TPMLP_ERR_ARG"),
+        (dict(A=FAKE + 2), "TPMLP_ERR_ALIGN"),
+        (dict(D=60), "TPMLP_ERR_SHAPE"),
+        (dict(F=4 * 12, n=4), "TPMLP_ERR_SHAPE"),
+        (dict(F=32 * 8, n=32), "TPMLP_ERR_UNSUPPORTED"),
+    ],
+)
+def test_shard_argument_errors(tp, kw, code):
+    rc, h = _shard(tp, **kw)
+    assert tp.STATUS_NAMES[rc] == code, tp.tpmlp_last_error()
+    assert h is None
+    assert tp.tpmlp_last_error() != ""
+
+
+def test_null_out_pointer(tp):
+    assert tp.lib().tpmlp_shard(FAKE, FAKE, 64, 256, 4, 1, None, None) == tp.TPMLP_ERR_ARG
+
+
+def test_calls_reject_null_handles(tp):
+    l = tp.lib()
+    assert l.tpmlp_forward(FAKE, 4, None, FAKE, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_hidden(FAKE, 4, None, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_partials(FAKE, 4, None, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_fused_sum(FAKE, 4, None, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_backward(FAKE, FAKE, 4, None, FAKE, None, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_shard_info(None, None, None, None, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_shard_get(None, 0, None, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_workspace_bytes(16, None, 0, 0) == 0
+    l.tpmlp_shards_free(None)  # no-op
+
+
+def test_gelu_and_allreduce_argument_errors(tp):
+    l = tp.lib()
+    assert l.tpmlp_gelu(FAKE, FAKE, -1, 0, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_gelu(FAKE, FAKE, 0, 0, None) == tp.TPMLP_OK  # empty input enqueues nothing
+    assert l.tpmlp_gelu(None, FAKE, 8, 0, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_gelu(FAKE + 4, FAKE, 8, 0, None) == tp.TPMLP_ERR_ALIGN
+    assert l.tpmlp_gelu(FAKE, FAKE, 8, 5, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_allreduce(FAKE, 0, 8, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_allreduce(FAKE, 2, 0, FAKE, None) == tp.TPMLP_OK
+    assert l.tpmlp_allreduce(FAKE, 2, 8, FAKE + 8, None) == tp.TPMLP_ERR_ALIGN
+    assert l.tpmlp_selftest_wait_timeout(0, None) == tp.TPMLP_ERR_ARG
+
+
+def test_calls_without_a_gpu_report_cuda_or_device_errors(tp):
+    # With valid arguments the first CUDA call fails on a GPU-less host; the
+    # library must say so with a status code, never crash.
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = tp.lib().tpmlp_gelu(FAKE, FAKE, 8, 0, None)
+    assert rc in (tp.TPMLP_ERR_CUDA, tp.TPMLP_ERR_DEVICE)
+    assert tp.tpmlp_last_error()
