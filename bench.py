@@ -69,7 +69,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
             return
@@ -78,7 +78,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -92,7 +95,10 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30)
+        for ts, ln in self.lines:
+            if not (t0 <= ts <= t1 + 0.15):  # samples taken during the timed region
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -181,6 +187,8 @@ def bench_tpmlp(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     w = WORKLOADS[args.workload]
+    if args.T:
+        w = w.with_(T=args.T)
     inp = make_inputs(w, seed=rank)
     X = inp["X"].to(dev)
     A = inp["A"].to(dev)
@@ -212,15 +220,16 @@ def bench_tpmlp(args, rank, world, local_rank):
         tp.tpmlp_fused_sum(H, sh, Y2)
         mark(5)
 
+    clocks = ClockSampler(local_rank)
+    clocks.start()  # before the warm-up, so its start-up does not overlap the timed region
     for _ in range(args.warmup):
         step()
     tp.tpmlp_check_status(stream)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    clocks.start()
+    clocks.mark("t_begin")
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -228,6 +237,7 @@ def bench_tpmlp(args, rank, world, local_rank):
         step(events[k])
     t1.record(stream)
     torch.cuda.synchronize(dev)
+    clocks.mark("t_end")
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
@@ -280,10 +290,11 @@ def bench_tpmlp(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tpmlp", "reference"], default="tpmlp")
     ap.add_argument("--workload", default="large")
+    ap.add_argument("--T", type=int, default=0, help="override the token count (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -294,6 +305,8 @@ def main():
     from tpmlp_inputs import WORKLOADS
 
     w = WORKLOADS[args.workload]
+    if args.T:
+        w = w.with_(T=args.T)
     step_flops = 2 * w.fwd_flops()
     config = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16 operands, fp32 accumulate; "
                           "step = faithful forward + fused forward",
