@@ -177,6 +177,27 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
                    void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
                    size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* tpmlp_forward without any allocation: the same Y, but the scratch lives in
+ * a fixed 64 MiB array of device memory that the library reserves on every
+ * GPU where its device code is loaded and keeps until the process exits. (The
+ * pages have no counterpart to this call; it exists for the library's users.)
+ * For callers that cannot allocate device memory at call time — runtimes that
+ * own all GPU memory through their own pool and forbid allocations outside
+ * it, or loops that cannot take the device synchronisation of cudaMalloc /
+ * cudaFree — and so cannot pass the workspace tpmlp_forward needs.
+ *   X, T, shards, Y, mode, stream  as for tpmlp_forward.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * TPMLP_ERR_WORKSPACE if tpmlp_workspace_bytes(T, shards, mode, 0) exceeds
+ * 64 MiB (at D=4096, F=16384, n=8: above 2048 tokens in FUSED mode, above
+ * 409 tokens in FAITHFUL mode).
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any
+ * stream capture. All calls on a GPU share the one array, so calls whose work
+ * may overlap on the GPU race on it; order them on one stream. Nothing in the
+ * array needs to start at zero, and it keeps the last call's contents. */
+int tpmlp_forward_noalloc(const void* X, int64_t T, const tpmlp_shards* shards, void* Y, tpmlp_mode mode,
+                          tpmlp_stream_t stream);
+
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit
  * of limit_ms milliseconds (1..10000). The block then stops and records

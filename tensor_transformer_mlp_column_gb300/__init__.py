@@ -58,6 +58,7 @@ SIGNATURES = {
     "tpmlp_fused_sum": (_I, [_P, _I64, _P, _P, _P]),
     "tpmlp_backward": (_I, [_P, _P, _I64, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
     "tpmlp_selftest_wait_timeout": (_I, [_I, _P]),
+    "tpmlp_forward_noalloc": (_I, [_P, _I64, _P, _P, _I, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -270,6 +271,15 @@ def tpmlp_backward(X: torch.Tensor, dY: torch.Tensor, shards: Shards, mode="fait
                                 _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
            "tpmlp_backward")
     return dX, dA, dB
+
+
+def tpmlp_forward_noalloc(X: torch.Tensor, shards: Shards, Y: torch.Tensor, mode="faithful", stream=None) -> torch.Tensor:
+    """tp_mlp(X, shards) for callers that cannot allocate device memory: the
+    library's fixed 64 MiB scratch replaces the workspace, and the caller
+    passes the output Y [T, D] fp32 (nothing is allocated here either)."""
+    _check(lib().tpmlp_forward_noalloc(_dev(X, "X"), X.shape[0], shards.handle, _dev(Y, "Y"), _mode(mode),
+                                       _stream(stream)), "tpmlp_forward_noalloc")
+    return Y
 
 
 def tpmlp_selftest_wait_timeout(limit_ms: int, stream=None) -> None:

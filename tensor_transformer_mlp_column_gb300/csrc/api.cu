@@ -211,6 +211,14 @@ int check_common(const tpmlp_shards* sh, int64_t T) {
 
 }  // namespace
 
+int tpmlp::set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 extern "C" {
 
 int tpmlp_version(void) { return (1 << 16) | 0; }

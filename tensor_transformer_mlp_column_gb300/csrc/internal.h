@@ -106,4 +106,8 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s);
 
 int num_sms();
 
+// Records the calling thread's error message (what tpmlp_last_error returns)
+// and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 }  // namespace tpmlp

@@ -1,0 +1,81 @@
+"""tpmlp_forward_noalloc: the forward for callers that cannot allocate device
+memory at call time (their runtime owns all GPU memory through its own pool,
+or their loop cannot take cudaMalloc's synchronisation). It uses the library's
+fixed 64 MiB scratch array instead of a caller workspace.
+
+Checked through the C ABI against tpmlp_forward (which takes a workspace), on
+two calls in a row with different inputs, so the second call runs on scratch
+that still holds the first call's data. Same tolerances as the other parity
+tests. This file is collected last on purpose.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from tpmlp_inputs import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tp():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import tensor_transformer_mlp_column_gb300 as tp
+
+    torch.cuda.set_device(0)
+    return tp
+
+
+def _call_noalloc(tp, X, sh, Y, mode):
+    stream = torch.cuda.current_stream().cuda_stream
+    return tp.lib().tpmlp_forward_noalloc(X.data_ptr(), X.shape[0], sh.handle, Y.data_ptr(), mode, stream)
+
+
+def _close(got, ref, dtype):
+    got = got.double().cpu().numpy()
+    ref = ref.double().cpu().numpy()
+    err = got - ref
+    fro = np.linalg.norm(err) / np.linalg.norm(ref)
+    mx = np.abs(err).max() / np.abs(ref).max()
+    if dtype == "f32":
+        assert mx <= 1e-4, mx
+    else:
+        assert fro <= 5e-3 and mx <= 2e-2, (fro, mx)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", [0, 1], ids=["faithful", "fused"])
+def test_noalloc_forward_matches_forward_twice(tp, dtype, mode):
+    w = Workload("noalloc", 1000, 512, 2048, 4, dtype, 1.0, 0.04, 0.02)
+    first = {k: v.cuda() for k, v in make_inputs(w, seed=31).items()}
+    second_X = make_inputs(w, seed=32)["X"].cuda()
+    sh = tp.tpmlp_shard(first["A"], first["B"], w.N)
+    for X in (first["X"], second_X):  # two calls in a row on the shared scratch
+        Y = torch.full((w.T, w.D), float("nan"), dtype=torch.float32, device="cuda")
+        assert _call_noalloc(tp, X, sh, Y, mode) == tp.TPMLP_OK, tp.tpmlp_last_error()
+        ref = tp.tpmlp_forward(X, sh, "fused" if mode else "faithful")
+        torch.cuda.synchronize()
+        assert torch.isfinite(Y).all()
+        _close(Y, ref, dtype)
+        if mode == 0:  # faithful is bitwise reproducible, whichever scratch it uses
+            assert torch.equal(Y, ref)
+    tp.tpmlp_check_status()
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(tp):
+    w = Workload("big", 4096, 1024, 16384, 8, "bf16", 1.0, 0.02, 0.02)  # H alone is 128 MiB
+    d = {k: v.cuda() for k, v in make_inputs(w, seed=1).items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
+    Y = torch.zeros((w.T, w.D), dtype=torch.float32, device="cuda")
+    rc = _call_noalloc(tp, d["X"], sh, Y, 1)
+    assert rc == tp.TPMLP_ERR_WORKSPACE
+    assert "64 MiB" in tp.tpmlp_last_error()
+    torch.cuda.synchronize()
+    assert not Y.any()  # nothing was enqueued
