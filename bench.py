@@ -287,6 +287,49 @@ def bench_tpmlp(args, rank, world, local_rank):
     return res
 
 
+def bench_backward(args, local_rank, peaks):
+    """tpmlp_backward on the fwd+bwd workload (T=8192, D=8192, F=32768, N=8):
+    8*T*D*F algorithmic FLOP (plus 2*T*D*F to recompute P = X A_i)."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOADS["fwd_bwd"]
+    inp = make_inputs(w, seed=0)
+    X, dY = inp["X"].to(dev), inp["dY"].to(dev)
+    sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+    del inp
+    stream = torch.cuda.current_stream(dev)
+    out = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16"}
+    dX = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    dA = [torch.empty((w.D, w.Fs), dtype=torch.float32, device=dev) for _ in range(w.N)]
+    dB = [torch.empty((w.Fs, w.D), dtype=torch.float32, device=dev) for _ in range(w.N)]
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, mode, True), dtype=torch.uint8, device=dev)
+        for _ in range(3):
+            tp.tpmlp_backward(X, dY, sh, mode, dX, dA, dB, ws)
+        tp.tpmlp_check_status(stream)
+        reps = max(3, min(args.steps // 10, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            tp.tpmlp_backward(X, dY, sh, mode, dX, dA, dB, ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        tp.tpmlp_check_status(stream)
+        ms = e0.elapsed_time(e1) / reps
+        alg = 8.0 * w.T * w.D * w.F / (ms * 1e-3) / 1e12
+        out[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
+                     "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1),
+                     "frac_bf16_incl_recompute": round(alg * 10 / 8 / peaks["bf16_tflops_sustained"], 4)}
+        del ws
+    sh.free()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -296,6 +339,7 @@ def main():
     ap.add_argument("--workload", default="large")
     ap.add_argument("--T", type=int, default=0, help="override the token count (smaller profiling cases)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement (fwd+bwd workload)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -408,6 +452,8 @@ def main():
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         line["modes"][m]["TFLOP/s"] = round(tf, 1)
         line["modes"][m]["frac_bf16"] = round(tf / peaks["bf16_tflops_sustained"], 4)
+    if not args.no_backward and world == 1 and not args.T:
+        line["backward"] = bench_backward(args, local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

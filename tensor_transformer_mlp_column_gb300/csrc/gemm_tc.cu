@@ -20,6 +20,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <cstring>
 
 namespace tpmlp {
@@ -265,6 +266,281 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
 }
 
+// ============================================================================
+// CTA-pair variant (tcgen05 cta_group::2): a cluster of two CTAs on two SMs
+// computes one 256 x 256 tile. Each CTA loads its own 128 rows of the M x K
+// operand and its own 128 of the 256 rows of the N x K operand; the even CTA
+// issues M=256, N=256 MMAs that read both CTAs' shared memory and write each
+// CTA's TMEM (its 128 rows x 256 fp32 columns). Per SM this moves half the
+// N x K operand bytes of the single-CTA kernel for the same MMA work.
+//   both CTAs, warp 0 lane 0 : TMA producer for the CTA's halves; completion is
+//                              counted on the even CTA's full barrier, which
+//                              the even producer arms with both CTAs' bytes
+//   even CTA, warp 1 lane 0  : MMA issuer; commits free each stage and publish
+//                              each accumulator in BOTH CTAs (multicast)
+//   both CTAs, warps 2..5    : epilogue of the CTA's own 128 rows; release the
+//                              accumulator by arriving on the even CTA's barrier
+// ============================================================================
+
+struct PairCfg {
+  static constexpr int STAGES = 6;
+  static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
+  static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 N rows
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ KParams p) {
+  using C = PairCfg;
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0 = even CTA (issues the MMAs), 1 = odd
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int nclusters = static_cast<int>(cluster_count_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);   // even CTA: its producer's arrive (+ both CTAs' bytes)
+      mbar_init(empty + s, 1);  // one multicast commit per use
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);   // one multicast commit per tile
+      mbar_init(acc_empty + b, 8);  // even CTA: one arrival per epilogue warp of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.groups; ++g) {
+      tma_prefetch_desc(&p.map_a[g]);
+      tma_prefetch_desc(&p.map_b[g]);
+    }
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+  tc_fence_before_sync();
+  cluster_sync_all();  // barriers of both CTAs initialised, TMEM allocated in both
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.wait_ns, &g_status};
+  const uint32_t peer_abort = map_to_cta(smem_addr(const_cast<int*>(abort_flag)), rank ^ 1u);
+  const int kb_per_tile = p.chain ? p.groups * p.k_blocks : p.k_blocks;
+  bool aborted = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, parity_bits = 0;
+      int fill = 0;
+      for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        int g, mb, nb;
+        decode_tile(p, tile, g, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(rank) * 128;
+        const int n0 = nb * BN + static_cast<int>(rank) * 128;
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
+            aborted = true;
+            break;
+          }
+          const int gg = p.chain ? kb / p.k_blocks : g;
+          const int kk = p.chain ? kb % p.k_blocks : kb;
+          const uint32_t full_even = map_to_cta(smem_addr(full + stage), 0);
+          ++fill;
+          if (fill != p.inject) {
+            if (rank == 0) {
+              mbar_arrive_expect_tx(full + stage, 2 * C::STAGE_BYTES);
+              armed |= 1u << stage;
+              parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+            }
+            tma_load_2d_pair(sA + stage * C::A_BYTES, &p.map_a[gg], kk * BK, m0, full_even);
+            tma_load_2d_pair(sB + stage * C::B_BYTES, &p.map_b[gg], kk * BK, n0, full_even);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        st_cluster_u32(peer_abort, 1u);
+        if (rank == 0) {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (armed >> s & 1u) wait_drain(full + s, (parity_bits >> s) & 1u, p.wait_ns);
+        } else {
+          // The odd CTA's copies are counted on the even CTA's barriers; give
+          // any copy still in flight time to land before shared memory is released.
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA)
+      constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        if (!wait_bounded(acc_empty + acc, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+                             (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(empty + stage, 0x3);  // frees stage `stage` in both CTAs
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        tc_commit_pair_multicast(acc_full + acc, 0x3);  // accumulator complete in both CTAs
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (aborted) {
+        st_cluster_u32(peer_abort, 1u);
+        tc_commit_pair_multicast(drain, 0x1);
+        wait_drain(drain, 0, p.wait_ns);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 of both CTAs)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t acc_empty_even0 = map_to_cta(smem_addr(acc_empty), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = cluster; tile < p.tiles; tile += nclusters) {
+      int g, mb, nb;
+      decode_tile(p, tile, g, mb, nb);
+      bool ok = wait_bounded(acc_full + acc, acc_phase, guard, kSiteEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) st_cluster_u32(peer_abort, 1u);
+        break;
+      }
+      tc_fence_after_sync();
+      const int64_t m = int64_t(mb) * 256 + int64_t(rank) * 128 + row;
+      const bool row_ok = m < p.M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
+        if (c + 32 == BN) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_even0 + 8u * static_cast<uint32_t>(acc));
+        }
+        const int n0 = nb * BN + c;
+        if (!row_ok || n0 >= p.N) continue;
+        if constexpr (EPI == kEpiGeluBf16) {
+          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (n0 + 8 * j + 8 <= p.N) {
+              uint4 w;
+              w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
+              w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
+              w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
+              w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
+              *reinterpret_cast<uint4*>(out + 8 * j) = w;
+            }
+          }
+        } else {
+          float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (n0 + 4 * j + 4 <= p.N)
+              *reinterpret_cast<float4*>(out + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          }
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncwarp();
+  cluster_sync_all();  // both CTAs done: no MMA, copy or remote arrival still targets either CTA
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int EPI>
+cudaError_t launch_pair_impl(const KParams& kp, cudaStream_t s) {
+  auto kern = tc_gemm_pair_kernel<EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PairCfg::SMEM));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: as many CTA pairs as can be resident at once.
+  static int max_pairs[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!max_pairs[dev]) {
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs[dev] = n > 0 ? n : 1;
+  }
+  const int pairs = kp.tiles < max_pairs[dev] ? kp.tiles : max_pairs[dev];
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, kp);
+}
+
 template <int BN, int EPI>
 cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   using C = Cfg<BN>;
@@ -311,7 +587,21 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
   return cudaStreamSynchronize(s);
 }
 
-int tc_box_rows_b(int N) { return N <= 128 ? 128 : 256; }
+// The CTA-pair kernel is the default; TPMLP_TC_PAIR=0 selects the
+// single-CTA kernel (read once per process; kept for comparisons).
+static bool use_pair_kernel() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("TPMLP_TC_PAIR");
+    v = (e && e[0] == '0') ? 0 : 1;
+  }
+  return v == 1;
+}
+
+int tc_box_rows_b(int N) {
+  if (use_pair_kernel()) return 128;  // each CTA of a pair loads half of the 256 N rows
+  return N <= 128 ? 128 : 256;
+}
 
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
                       int box_rows) {
@@ -343,19 +633,22 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.map_b[i] = *g.map_b[i];
     kp.out[i] = g.out[i];
   }
-  const int BN = tc_box_rows_b(g.N);
+  const bool pair = use_pair_kernel();
+  const int BN = pair ? 256 : tc_box_rows_b(g.N);
+  const int TM = pair ? 256 : BM;
   kp.ldo = g.ldo;
   kp.M = g.M;
   kp.N = g.N;
   kp.groups = g.groups;
   kp.chain = g.chain;
-  kp.m_blocks = (g.M + BM - 1) / BM;
+  kp.m_blocks = (g.M + TM - 1) / TM;
   kp.n_blocks = (g.N + BN - 1) / BN;
   kp.k_blocks = (g.K + BK - 1) / BK;
   kp.tiles = kp.m_blocks * kp.n_blocks * (g.chain ? 1 : g.groups);
   kp.wait_ns = wait_ns;
   kp.inject = g.inject;
   if (kp.tiles == 0) return cudaSuccess;
+  if (pair) return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16>(kp, s) : launch_pair_impl<kEpiF32>(kp, s);
   if (BN == 256) return g.epi == kEpiGeluBf16 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<256, kEpiF32>(kp, s);
   return g.epi == kEpiGeluBf16 ? launch_impl<128, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiF32>(kp, s);
 }
