@@ -189,6 +189,8 @@ def bench_tpmlp(args, rank, world, local_rank):
     w = WORKLOADS[args.workload]
     if args.T:
         w = w.with_(T=args.T)
+    if args.N:
+        w = w.with_(N=args.N)
     inp = make_inputs(w, seed=rank)
     X = inp["X"].to(dev)
     A = inp["A"].to(dev)
@@ -338,6 +340,7 @@ def main():
     ap.add_argument("--impl", choices=["tpmlp", "reference"], default="tpmlp")
     ap.add_argument("--workload", default="large")
     ap.add_argument("--T", type=int, default=0, help="override the token count (smaller profiling cases)")
+    ap.add_argument("--N", type=int, default=0, help="override the shard count (experiments)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement (fwd+bwd workload)")
     args = ap.parse_args()
@@ -351,6 +354,8 @@ def main():
     w = WORKLOADS[args.workload]
     if args.T:
         w = w.with_(T=args.T)
+    if args.N:
+        w = w.with_(N=args.N)
     step_flops = 2 * w.fwd_flops()
     config = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16 operands, fp32 accumulate; "
                           "step = faithful forward + fused forward",
@@ -452,7 +457,7 @@ def main():
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         line["modes"][m]["TFLOP/s"] = round(tf, 1)
         line["modes"][m]["frac_bf16"] = round(tf / peaks["bf16_tflops_sustained"], 4)
-    if not args.no_backward and world == 1 and not args.T:
+    if not args.no_backward and world == 1 and not args.T and not args.N:
         line["backward"] = bench_backward(args, local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()

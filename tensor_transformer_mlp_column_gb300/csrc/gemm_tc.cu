@@ -47,6 +47,7 @@ struct KParams {
   int tiles;
   uint64_t wait_ns;
   int inject;
+  int group_m;  // tile order: 0 = N fastest within each M block; G > 0 = groups of G M blocks, M fastest
 };
 
 template <int BN>
@@ -63,8 +64,19 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
   const int per_group = p.m_blocks * p.n_blocks;
   g = p.chain ? 0 : tile / per_group;
   const int r = p.chain ? tile : tile % per_group;
-  mb = r / p.n_blocks;  // consecutive tiles walk N first, so CTAs running together share A panels
-  nb = r % p.n_blocks;
+  if (p.group_m <= 0) {
+    mb = r / p.n_blocks;  // consecutive tiles walk N first, so CTAs running together share A panels
+    nb = r % p.n_blocks;
+    return;
+  }
+  // Groups of group_m M blocks; inside a group M runs fastest, so the tiles in
+  // flight together cover about group_m M blocks x (tiles / group_m) N blocks.
+  const int span = p.group_m * p.n_blocks;
+  const int first = (r / span) * p.group_m;
+  const int rows = min(p.m_blocks - first, p.group_m);
+  const int q = r % span;
+  mb = first + q % rows;
+  nb = q / rows;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -129,13 +141,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
-        for (int kb = 0; kb < kb_per_tile; ++kb) {
+        int gg = g, kk = 0;  // group and K block of the next fill (chain mode walks the groups in order)
+        for (int kb = 0; kb < kb_per_tile; ++kb, ++kk) {
+          if (kk == p.k_blocks) {
+            kk = 0;
+            ++gg;
+          }
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
             ok = false;
             break;
           }
-          const int gg = p.chain ? kb / p.k_blocks : g;
-          const int kk = p.chain ? kb % p.k_blocks : kb;
           ++fill;
           if (fill != p.inject) {
             mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
@@ -282,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 //                              accumulator by arriving on the even CTA's barrier
 // ============================================================================
 
+template <int STAGES_>
 struct PairCfg {
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = STAGES_;
   static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
   static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 N rows
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -291,9 +307,9 @@ struct PairCfg {
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
 };
 
-template <int EPI>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ KParams p) {
-  using C = PairCfg;
+  using C = PairCfg<STAGES>;
   constexpr int BN = 256;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -354,13 +370,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         decode_tile(p, tile, g, mb, nb);
         const int m0 = mb * 256 + static_cast<int>(rank) * 128;
         const int n0 = nb * BN + static_cast<int>(rank) * 128;
-        for (int kb = 0; kb < kb_per_tile; ++kb) {
+        int gg = g, kk = 0;  // group and K block of the next fill (chain mode walks the groups in order)
+        for (int kb = 0; kb < kb_per_tile; ++kb, ++kk) {
+          if (kk == p.k_blocks) {
+            kk = 0;
+            ++gg;
+          }
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
             aborted = true;
             break;
           }
-          const int gg = p.chain ? kb / p.k_blocks : g;
-          const int kk = p.chain ? kb % p.k_blocks : kb;
           const uint32_t full_even = map_to_cta(smem_addr(full + stage), 0);
           ++fill;
           if (fill != p.inject) {
@@ -508,10 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   }
 }
 
-template <int EPI>
+template <int EPI, int STAGES>
 cudaError_t launch_pair_impl(const KParams& kp, cudaStream_t s) {
-  auto kern = tc_gemm_pair_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(PairCfg::SMEM));
+  using C = PairCfg<STAGES>;
+  auto kern = tc_gemm_pair_kernel<EPI, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -520,23 +540,24 @@ cudaError_t launch_pair_impl(const KParams& kp, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // Persistent grid: as many CTA pairs as can be resident at once.
-  static int max_pairs[64] = {0};
+  static int max_pairs[64][2] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!max_pairs[dev]) {
+  int& cached = max_pairs[dev][STAGES == 7 ? 1 : 0];
+  if (!cached) {
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     int n = 0;
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
-    max_pairs[dev] = n > 0 ? n : 1;
+    cached = n > 0 ? n : 1;
   }
-  const int pairs = kp.tiles < max_pairs[dev] ? kp.tiles : max_pairs[dev];
+  const int pairs = kp.tiles < cached ? kp.tiles : cached;
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, kp);
 }
@@ -585,6 +606,11 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
   e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return e;
   return cudaStreamSynchronize(s);
+}
+
+static int env_int(const char* name, int dflt) {
+  const char* e = getenv(name);
+  return e && *e ? atoi(e) : dflt;
 }
 
 // The CTA-pair kernel is the default; TPMLP_TC_PAIR=0 selects the
@@ -647,8 +673,13 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.tiles = kp.m_blocks * kp.n_blocks * (g.chain ? 1 : g.groups);
   kp.wait_ns = wait_ns;
   kp.inject = g.inject;
+  kp.group_m = env_int("TPMLP_GROUP_M", 0);
   if (kp.tiles == 0) return cudaSuccess;
-  if (pair) return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16>(kp, s) : launch_pair_impl<kEpiF32>(kp, s);
+  if (pair) {
+    if (env_int("TPMLP_PAIR_STAGES", 6) == 7)
+      return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16, 7>(kp, s) : launch_pair_impl<kEpiF32, 7>(kp, s);
+    return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16, 6>(kp, s) : launch_pair_impl<kEpiF32, 6>(kp, s);
+  }
   if (BN == 256) return g.epi == kEpiGeluBf16 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<256, kEpiF32>(kp, s);
   return g.epi == kEpiGeluBf16 ? launch_impl<128, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiF32>(kp, s);
 }
