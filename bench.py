@@ -289,6 +289,56 @@ def bench_tpmlp(args, rank, world, local_rank):
     return res
 
 
+def bench_small_workloads(local_rank):
+    """Forward time of the GPT-2-small and the sequence-sweep workloads (both
+    modes), and the linear fit of forward time against seq for the sweep."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name in ("gpt2_small", "seq128", "seq256", "seq512"):
+        w = WORKLOADS[name]
+        inp = make_inputs(w, seed=0)
+        X = inp["X"].to(dev)
+        sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+        Y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+        res = {"T": w.T, "D": w.D, "F": w.F, "N": w.N}
+        for mode in ("faithful", "fused"):
+            ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, mode), dtype=torch.uint8, device=dev)
+            for _ in range(5):
+                tp.tpmlp_forward(X, sh, mode, Y, ws)
+            reps = 50
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            e0.record(stream)
+            for _ in range(reps):
+                tp.tpmlp_forward(X, sh, mode, Y, ws)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / reps
+            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
+        tp.tpmlp_check_status(stream)
+        sh.free()
+        out[name] = res
+    # FFN time against sequence length (batch 8): a least-squares line and its R^2.
+    seqs = [128, 256, 512]
+    for mode in ("faithful", "fused"):
+        ys = [out[f"seq{s}"][mode]["ms"] for s in seqs]
+        mx, my = sum(seqs) / 3, sum(ys) / 3
+        sxy = sum((x - mx) * (y - my) for x, y in zip(seqs, ys))
+        sxx = sum((x - mx) ** 2 for x in seqs)
+        slope = sxy / sxx
+        ss_res = sum((y - (my + slope * (x - mx))) ** 2 for x, y in zip(seqs, ys))
+        ss_tot = sum((y - my) ** 2 for y in ys)
+        out[f"seq_sweep_{mode}"] = {"ms_per_unit_seq": round(slope, 6), "intercept_ms": round(my - slope * mx, 4),
+                                    "r2": round(1 - ss_res / ss_tot, 5) if ss_tot > 0 else None}
+    return out
+
+
 def bench_backward(args, local_rank, peaks):
     """tpmlp_backward on the fwd+bwd workload (T=8192, D=8192, F=32768, N=8):
     8*T*D*F algorithmic FLOP (plus 2*T*D*F to recompute P = X A_i)."""
@@ -459,6 +509,7 @@ def main():
         line["modes"][m]["frac_bf16"] = round(tf / peaks["bf16_tflops_sustained"], 4)
     if not args.no_backward and world == 1 and not args.T and not args.N:
         line["backward"] = bench_backward(args, local_rank, peaks)
+        line["other_workloads"] = bench_small_workloads(local_rank)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

@@ -108,7 +108,7 @@ WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int ba
     if (mode == TPMLP_FAITHFUL) w.Yp = take(n * t * D * 4);
   } else {
     w.P = take(n * t * Fs * 4);
-    w.dH = take(n * t * Fs * 4);
+    if (sh->dt == TPMLP_F32) w.dH = take(n * t * Fs * 4);  // bf16 applies the activation in the dH epilogue
     if (sh->dt == TPMLP_BF16) {
       w.Xt = take(D * tp * 2);
       w.dYt = take(D * tp * 2);
@@ -156,6 +156,9 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
     g.N = static_cast<int>(Fs);
     g.K = static_cast<int>(D);
     g.epi = kEpiGeluBf16;
+    g.shared = kSharedA;  // X feeds every shard
+    g.group_m = 8;        // bands of 8 M blocks: best measured at the large workload
+    g.stream_out = 1;
     TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
     return TPMLP_OK;
   }
@@ -189,6 +192,8 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
     g.K = static_cast<int>(Fs);
     g.chain = chain;
     g.epi = kEpiF32;
+    g.group_m = 8;
+    g.stream_out = 1;
     TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
     return TPMLP_OK;
   }
@@ -521,15 +526,24 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.N = static_cast<int>(Fs);
   g.K = static_cast<int>(D);
   g.epi = kEpiF32;
+  g.shared = kSharedA;  // X (then dY) feeds every shard
+  g.group_m = 8;
+  g.stream_out = 0;     // P and dH are read back right away by the activation step
   TRY_CUDA(launch_tc_gemm(g, wl, s));
+  // dH_i = dY B_i^T with the activation step in its epilogue: dP_i = dH_i *
+  // GeLU'(P_i) and the transposes H_i^T = GeLU(P_i)^T and dP_i^T, all bf16.
   for (int i = 0; i < n; ++i) {
     g.map_a[i] = &mdY;
     g.map_b[i] = &sh->map_B[i];
-    g.out[i] = dH + static_cast<size_t>(i) * T * Fs;
+    g.out[i] = dP + static_cast<size_t>(i) * T * Fs;
+    g.aux_p[i] = P + static_cast<size_t>(i) * T * Fs;
+    g.aux_ht[i] = Ht + static_cast<size_t>(i) * Fs * Tp;
+    g.aux_dpt[i] = dPt + static_cast<size_t>(i) * Fs * Tp;
   }
+  g.ldt = Tp;
+  g.epi = kEpiBwdAct;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
-  // H_i^T, dP_i, dP_i^T in bf16.
-  TRY_CUDA(launch_bwd_act_bf16(P, dH, n, T, Fs, Tp, Ht, dP, dPt, s));
+  g.epi = kEpiF32;
   // dB_i = H_i^T dY: [Fs, D], K = T.
   for (int i = 0; i < n; ++i) {
     g.map_a[i] = &mHt[i];
@@ -540,6 +554,9 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.M = static_cast<int>(Fs);
   g.N = static_cast<int>(D);
   g.K = static_cast<int>(T);
+  g.shared = kSharedB;  // dY^T feeds every shard
+  g.group_m = 8;
+  g.stream_out = 1;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dA_i = X^T dP_i: [D, Fs], K = T.
   for (int i = 0; i < n; ++i) {
@@ -550,6 +567,8 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.ldo = Fs;
   g.M = static_cast<int>(D);
   g.N = static_cast<int>(Fs);
+  g.shared = kSharedA;  // X^T feeds every shard
+  g.group_m = 8;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dX = sum_i dP_i A_i^T: [T, D], K = Fs.
   for (int i = 0; i < n; ++i) {
@@ -562,6 +581,8 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.N = static_cast<int>(D);
   g.K = static_cast<int>(Fs);
   g.chain = dXp ? 0 : 1;
+  g.shared = kSharedNone;
+  g.group_m = 8;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
   return TPMLP_OK;

@@ -152,46 +152,10 @@ __global__ void __launch_bounds__(256) transpose_u16_kernel(const uint16_t* __re
   }
 }
 
-// ------------------------------------------------------------------ backward activation
+// ------------------------------------------------------------------ backward activation (fp32 path)
 
-// For element (i, t, f): p = P, g = dH; H = GeLU(p), dP = g * GeLU'(p).
-// Writes dP row-major and H^T, dP^T transposed ([i][f][t], row pitch ldt),
-// through a 32 x 32 shared tile so both layouts are written coalesced.
-__global__ void __launch_bounds__(256) bwd_act_bf16_kernel(const float* __restrict__ P, const float* __restrict__ dH,
-                                                           int64_t T, int64_t Fs, int64_t ldt,
-                                                           __nv_bfloat16* __restrict__ Ht, __nv_bfloat16* __restrict__ dP,
-                                                           __nv_bfloat16* __restrict__ dPt) {
-  __shared__ __nv_bfloat16 sh[32][33];
-  __shared__ __nv_bfloat16 sd[32][33];
-  const int i = blockIdx.z;
-  const int64_t t0 = int64_t(blockIdx.y) * 32, f0 = int64_t(blockIdx.x) * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-  const float* Pi = P + int64_t(i) * T * Fs;
-  const float* dHi = dH + int64_t(i) * T * Fs;
-  for (int tt = ty; tt < 32; tt += 8) {
-    const int64_t t = t0 + tt, f = f0 + tx;
-    __nv_bfloat16 hv = __float2bfloat16_rn(0.f), dv = hv;
-    if (t < T && f < Fs) {
-      float g, dg;
-      gelu_and_grad_fast(Pi[t * Fs + f], g, dg);
-      hv = __float2bfloat16_rn(g);
-      dv = __float2bfloat16_rn(dHi[t * Fs + f] * dg);
-      dP[int64_t(i) * T * Fs + t * Fs + f] = dv;
-    }
-    sh[tt][tx] = hv;
-    sd[tt][tx] = dv;
-  }
-  __syncthreads();
-  for (int ff = ty; ff < 32; ff += 8) {
-    const int64_t f = f0 + ff, t = t0 + tx;
-    if (t < T && f < Fs) {
-      const int64_t o = int64_t(i) * Fs * ldt + f * ldt + t;
-      Ht[o] = sh[tx][ff];
-      dPt[o] = sd[tx][ff];
-    }
-  }
-}
-
+// In place: P <- GeLU(P), dH <- dH * GeLU'(P). (The bf16 path applies this
+// step in the epilogue of its dH product instead.)
 __global__ void bwd_act_f32_kernel(float* __restrict__ P, float* __restrict__ dH, int64_t count) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
@@ -249,14 +213,6 @@ cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int
   dim3 grid(static_cast<unsigned>((cols + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
   transpose_u16_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(in), rows, cols, ldi,
                                             static_cast<uint16_t*>(out), ldo);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_act_bf16(const float* P, const float* dH, int n, int64_t T, int64_t Fs, int64_t ldt, void* Ht,
-                                void* dP, void* dPt, cudaStream_t s) {
-  dim3 grid(static_cast<unsigned>((Fs + 31) / 32), static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>(n));
-  bwd_act_bf16_kernel<<<grid, 256, 0, s>>>(P, dH, T, Fs, ldt, static_cast<__nv_bfloat16*>(Ht),
-                                           static_cast<__nv_bfloat16*>(dP), static_cast<__nv_bfloat16*>(dPt));
   return cudaGetLastError();
 }
 

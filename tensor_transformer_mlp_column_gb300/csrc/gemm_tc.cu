@@ -39,7 +39,10 @@ struct KParams {
   CUtensorMap map_a[kMaxGroups];
   CUtensorMap map_b[kMaxGroups];
   void* out[kMaxGroups];
-  int64_t ldo;
+  const void* aux_p[kMaxGroups];  // kEpiBwdAct: P per group (fp32, row pitch ldo)
+  void* aux_ht[kMaxGroups];       // kEpiBwdAct: H^T per group (bf16, row pitch ldt)
+  void* aux_dpt[kMaxGroups];      // kEpiBwdAct: dP^T per group (bf16, row pitch ldt)
+  int64_t ldo, ldt;
   int M, N;
   int groups;
   int chain;
@@ -47,7 +50,9 @@ struct KParams {
   int tiles;
   uint64_t wait_ns;
   int inject;
-  int group_m;  // tile order: 0 = N fastest within each M block; G > 0 = groups of G M blocks, M fastest
+  int group_m;  // tile order: bands of group_m tile rows, rows fastest inside a band (1 = columns fastest)
+  int shared;   // kSharedNone / kSharedA / kSharedB: an operand that every group reads
+  int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
 };
 
 template <int BN>
@@ -60,28 +65,133 @@ struct Cfg {
   static constexpr size_t SMEM = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + 256 /*barriers*/;
 };
 
+// Maps a tile index to (group, M block, N block). The tiles form a grid of
+// `rows` x `cols`, walked in bands of group_m rows with rows fastest inside a
+// band, so the tiles in flight together (one per CTA pair) cover about
+// group_m rows x (pairs / group_m) columns and each operand panel is fetched
+// from DRAM about once per band instead of once per tile.
+//   shared A (every group reads the same M x K operand): rows = M blocks,
+//     cols = the groups' N blocks side by side;
+//   shared B (every group reads the same N x K operand): rows = the groups'
+//     M blocks stacked, cols = N blocks;
+//   otherwise each group's grid in turn (chain mode: the one output grid).
 __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
-  const int per_group = p.m_blocks * p.n_blocks;
-  g = p.chain ? 0 : tile / per_group;
-  const int r = p.chain ? tile : tile % per_group;
-  if (p.group_m <= 0) {
-    mb = r / p.n_blocks;  // consecutive tiles walk N first, so CTAs running together share A panels
-    nb = r % p.n_blocks;
-    return;
+  int rows_total, cols, base = 0;
+  if (p.chain || p.shared == kSharedNone) {
+    const int per_group = p.m_blocks * p.n_blocks;
+    g = p.chain ? 0 : tile / per_group;
+    base = g * per_group;
+    rows_total = p.m_blocks;
+    cols = p.n_blocks;
+  } else if (p.shared == kSharedA) {
+    rows_total = p.m_blocks;
+    cols = p.groups * p.n_blocks;
+  } else {
+    rows_total = p.groups * p.m_blocks;
+    cols = p.n_blocks;
   }
-  // Groups of group_m M blocks; inside a group M runs fastest, so the tiles in
-  // flight together cover about group_m M blocks x (tiles / group_m) N blocks.
-  const int span = p.group_m * p.n_blocks;
-  const int first = (r / span) * p.group_m;
-  const int rows = min(p.m_blocks - first, p.group_m);
-  const int q = r % span;
-  mb = first + q % rows;
-  nb = q / rows;
+  const int t = tile - base;
+  const int gm = p.group_m > 0 ? p.group_m : 1;
+  const int span = gm * cols;
+  const int first = (t / span) * gm;
+  const int band = min(rows_total - first, gm);
+  const int q = t % span;
+  const int row = first + q % band;
+  const int col = q / band;
+  if (p.chain || p.shared == kSharedNone) {
+    mb = row;
+    nb = col;
+  } else if (p.shared == kSharedA) {
+    mb = row;
+    g = col / p.n_blocks;
+    nb = col % p.n_blocks;
+  } else {
+    g = row / p.m_blocks;
+    mb = row % p.m_blocks;
+    nb = col;
+  }
+}
+
+// 16-byte global stores; `stream` marks them evict-first so results that are
+// not read again soon do not push the operands out of L2.
+__device__ __forceinline__ void store16(void* dst, uint4 v, bool stream) {
+  if (stream)
+    __stcs(reinterpret_cast<uint4*>(dst), v);
+  else
+    *reinterpret_cast<uint4*>(dst) = v;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Output treatment of one thread's 32 accumulator columns n0..n0+31 of row m
+// (group g). The caller has checked m < M and n0 < N; N is a multiple of 8.
+template <int EPI>
+__device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
+  if constexpr (EPI == kEpiGeluBf16) {
+    // H = GeLU(acc), bf16, row-major.
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n0 + 8 * j + 8 <= p.N) {
+        uint4 w;
+        w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
+        w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
+        w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
+        w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
+        store16(out + 8 * j, w, p.stream_out);
+      }
+    }
+  } else if constexpr (EPI == kEpiF32) {
+    float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (n0 + 4 * j + 4 <= p.N)
+        store16(out + 4 * j,
+                make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                           __float_as_uint(v[4 * j + 3])),
+                p.stream_out);
+    }
+  } else {
+    // Backward activation: acc = dH (row m = token t, column n = feature f).
+    // With P from aux_p: dP = dH * GeLU'(P) to out (bf16 [T][ldo]), and the
+    // transposes H^T = GeLU(P)^T to aux_ht and dP^T to aux_dpt (bf16 [F][ldt]).
+    // The 32 lanes of a warp hold 32 consecutive tokens, so each transposed
+    // store of one column is 64 contiguous bytes.
+    const float* P = static_cast<const float*>(p.aux_p[g]) + m * p.ldo + n0;
+    __nv_bfloat16* dP = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+    __nv_bfloat16* Ht = static_cast<__nv_bfloat16*>(p.aux_ht[g]) + int64_t(n0) * p.ldt + m;
+    __nv_bfloat16* dPt = static_cast<__nv_bfloat16*>(p.aux_dpt[g]) + int64_t(n0) * p.ldt + m;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n0 + 8 * j + 8 > p.N) continue;
+      const float4 p0 = *reinterpret_cast<const float4*>(P + 8 * j);
+      const float4 p1 = *reinterpret_cast<const float4*>(P + 8 * j + 4);
+      const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      float h[8], d[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float gv, dg;
+        gelu_and_grad_fast(pv[e], gv, dg);
+        h[e] = gv;
+        d[e] = v[8 * j + e] * dg;
+      }
+      uint4 w;
+      w.x = pack_bf16x2(d[0], d[1]);
+      w.y = pack_bf16x2(d[2], d[3]);
+      w.z = pack_bf16x2(d[4], d[5]);
+      w.w = pack_bf16x2(d[6], d[7]);
+      store16(dP + 8 * j, w, false);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t o = int64_t(8 * j + e) * p.ldt;
+        Ht[o] = __float2bfloat16_rn(h[e]);
+        dPt[o] = __float2bfloat16_rn(d[e]);
+      }
+    }
+  }
 }
 
 template <int BN, int EPI>
@@ -245,27 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         const int n0 = nb * BN + c;
         if (!row_ok || n0 >= p.N) continue;
-        if constexpr (EPI == kEpiGeluBf16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (n0 + 8 * j + 8 <= p.N) {
-              uint4 w;
-              w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
-              w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
-              w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
-              w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
-              *reinterpret_cast<uint4*>(out + 8 * j) = w;
-            }
-          }
-        } else {
-          float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (n0 + 4 * j + 4 <= p.N)
-              *reinterpret_cast<float4*>(out + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
+        epilogue_store<EPI>(p, g, m, n0, v);
       }
       if (++acc == 2) {
         acc = 0;
@@ -489,27 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         }
         const int n0 = nb * BN + c;
         if (!row_ok || n0 >= p.N) continue;
-        if constexpr (EPI == kEpiGeluBf16) {
-          __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (n0 + 8 * j + 8 <= p.N) {
-              uint4 w;
-              w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
-              w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
-              w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
-              w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
-              *reinterpret_cast<uint4*>(out + 8 * j) = w;
-            }
-          }
-        } else {
-          float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (n0 + 4 * j + 4 <= p.N)
-              *reinterpret_cast<float4*>(out + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          }
-        }
+        epilogue_store<EPI>(p, g, m, n0, v);
       }
       if (++acc == 2) {
         acc = 0;
@@ -658,11 +728,15 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.map_a[i] = *g.map_a[i];
     kp.map_b[i] = *g.map_b[i];
     kp.out[i] = g.out[i];
+    kp.aux_p[i] = g.aux_p[i];
+    kp.aux_ht[i] = g.aux_ht[i];
+    kp.aux_dpt[i] = g.aux_dpt[i];
   }
   const bool pair = use_pair_kernel();
   const int BN = pair ? 256 : tc_box_rows_b(g.N);
   const int TM = pair ? 256 : BM;
   kp.ldo = g.ldo;
+  kp.ldt = g.ldt;
   kp.M = g.M;
   kp.N = g.N;
   kp.groups = g.groups;
@@ -673,15 +747,23 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.tiles = kp.m_blocks * kp.n_blocks * (g.chain ? 1 : g.groups);
   kp.wait_ns = wait_ns;
   kp.inject = g.inject;
-  kp.group_m = env_int("TPMLP_GROUP_M", 0);
+  kp.group_m = env_int("TPMLP_GROUP_M", g.group_m);
+  kp.shared = g.shared;
+  kp.stream_out = env_int("TPMLP_STREAM_OUT", g.stream_out);
   if (kp.tiles == 0) return cudaSuccess;
-  if (pair) {
-    if (env_int("TPMLP_PAIR_STAGES", 6) == 7)
-      return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16, 7>(kp, s) : launch_pair_impl<kEpiF32, 7>(kp, s);
-    return g.epi == kEpiGeluBf16 ? launch_pair_impl<kEpiGeluBf16, 6>(kp, s) : launch_pair_impl<kEpiF32, 6>(kp, s);
+  switch (g.epi) {
+    case kEpiGeluBf16:
+      return pair ? launch_pair_impl<kEpiGeluBf16, 6>(kp, s)
+                  : (BN == 256 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiGeluBf16>(kp, s));
+    case kEpiF32:
+      return pair ? launch_pair_impl<kEpiF32, 6>(kp, s)
+                  : (BN == 256 ? launch_impl<256, kEpiF32>(kp, s) : launch_impl<128, kEpiF32>(kp, s));
+    case kEpiBwdAct:
+      return pair ? launch_pair_impl<kEpiBwdAct, 6>(kp, s)
+                  : (BN == 256 ? launch_impl<256, kEpiBwdAct>(kp, s) : launch_impl<128, kEpiBwdAct>(kp, s));
+    default:
+      return cudaErrorInvalidValue;
   }
-  if (BN == 256) return g.epi == kEpiGeluBf16 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<256, kEpiF32>(kp, s);
-  return g.epi == kEpiGeluBf16 ? launch_impl<128, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiF32>(kp, s);
 }
 
 int num_sms() {

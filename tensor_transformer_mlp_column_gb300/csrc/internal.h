@@ -23,7 +23,10 @@ enum WaitSite : int {
 enum TcEpilogue : int {
   kEpiGeluBf16 = 0,  // out bf16 = GeLU(acc)
   kEpiF32 = 1,       // out fp32 = acc
+  kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), aux_ht = GeLU(P)^T, aux_dpt = out^T (P from aux_p)
 };
+
+enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
 
 // One grouped GEMM on the tensor cores: for every group g,
 //   out[g][m, n] = sum_k Aop_g[m, k] * Bop_g[n, k]        (chain == 0)
@@ -35,12 +38,19 @@ struct TcGemm {
   const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
   const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
+  const void* aux_p[kMaxGroups];         // kEpiBwdAct only: P (fp32, row stride ldo)
+  void* aux_ht[kMaxGroups];              // kEpiBwdAct only: H^T (bf16, row stride ldt)
+  void* aux_dpt[kMaxGroups];             // kEpiBwdAct only: dP^T (bf16, row stride ldt)
   int64_t ldo;
+  int64_t ldt;
   int M, N, K;
   int groups;
   int chain;
   int epi;     // TcEpilogue
   int inject;  // test hook, 0 = off
+  int shared;      // TcShared: an operand read by every group (tile order exploits it)
+  int group_m;     // tile rows per band of the tile order (see decode_tile); 0 or 1 = columns fastest
+  int stream_out;  // 1: evict-first epilogue stores
 };
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
@@ -90,12 +100,6 @@ cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_t
 cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int64_t ldi, void* out, int64_t ldo,
                                  cudaStream_t s);
 
-// Backward elementwise step of the bf16 path, for n shards at once:
-//   from P [n][T][Fs] and dH [n][T][Fs] (fp32) write H^T [n][Fs][ldt] (bf16),
-//   dP [n][T][Fs] (bf16) and dP^T [n][Fs][ldt] (bf16), where
-//   H = GeLU(P), dP = dH * GeLU'(P).
-cudaError_t launch_bwd_act_bf16(const float* P, const float* dH, int n, int64_t T, int64_t Fs, int64_t ldt,
-                                void* Ht, void* dP, void* dPt, cudaStream_t s);
 // fp32 path: in place, P <- GeLU(P) and dH <- dH * GeLU'(P), count elements.
 cudaError_t launch_bwd_act_f32(float* P, float* dH, int64_t count, cudaStream_t s);
 
