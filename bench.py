@@ -289,6 +289,21 @@ def bench_tpmlp(args, rank, world, local_rank):
     return res
 
 
+def max_over_ranks(values, device):
+    """Element-wise MAX of `values` over all ranks of the process group: the
+    slowest replica sets the job's time."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world: int, flops_per_step_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job TFLOP/s: every rank's work divided by the slowest rank's time."""
+    return world * flops_per_step_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def bench_small_workloads(local_rank):
     """Forward time of the GPT-2-small and the sequence-sweep workloads (both
     modes), and the linear fit of forward time against seq for the sweep."""
@@ -443,9 +458,7 @@ def main():
     ms_step = res["total_ms"] / args.steps
     e2e_ms = res["e2e_ms"]
     if world > 1:
-        t = torch.tensor([ms_step, e2e_ms], device=torch.device("cuda", local_rank))
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step, e2e_ms = t.tolist()
+        ms_step, e2e_ms = max_over_ranks([ms_step, e2e_ms], torch.device("cuda", local_rank))
     if rank != 0:
         torch.distributed.destroy_process_group() if world > 1 else None
         return
@@ -481,7 +494,7 @@ def main():
                 "frac": round(ach / pk, 4), "traffic": None,
                 "peak_source": peaks["source"] + " (sustained bf16, kernel timed inside a long step)"}
     red_gbs = reduce_bytes / (avg["allreduce"] * 1e-3) / 1e9
-    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    value = job_throughput(world, step_flops, ms_step)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -497,7 +510,7 @@ def main():
         "kernels": kernel_report, "kernel_ms_sum": round(step_ms_sum, 4),
         "roofline": roof,
         "clocks": res["clocks"],
-        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_throughput(world, step_flops, e2e_ms), 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": res["launches"],
         "peaks": peaks,

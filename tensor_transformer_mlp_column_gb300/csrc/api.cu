@@ -135,6 +135,13 @@ int map_or_fail(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, in
   return TPMLP_OK;
 }
 
+int out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t pitch, const char* what) {
+  if (!make_output_map_f32(m, base, rows, cols, pitch))
+    return fail(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the output map of %s [%lld x %lld]", what,
+                static_cast<long long>(rows), static_cast<long long>(cols));
+  return TPMLP_OK;
+}
+
 // ----------------------------------------------------------- step launchers
 
 // H_i = GeLU(X A_i) for every shard.
@@ -175,7 +182,7 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
 int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int chain, cudaStream_t s) {
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
-    std::vector<CUtensorMap> mh(sh->n);
+    std::vector<CUtensorMap> mh(sh->n), mo(sh->n);
     TcGemm g{};
     g.groups = sh->n;
     for (int i = 0; i < sh->n; ++i) {
@@ -185,6 +192,8 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
       g.map_a[i] = &mh[i];
       g.map_b[i] = &sh->map_Bt[i];
       g.out[i] = chain ? out : static_cast<void*>(static_cast<float*>(out) + static_cast<size_t>(i) * T * D);
+      if ((rc = out_map(&mo[i], g.out[i], T, D, D, "Y_i"))) return rc;
+      g.map_out[i] = &mo[i];
     }
     g.ldo = D;
     g.M = static_cast<int>(T);
@@ -515,11 +524,14 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   const uint64_t wl = wait_limit_ns();
   TcGemm g{};
   g.groups = n;
-  // P_i = X A_i (recompute) and dH_i = dY B_i^T, fp32.
+  std::vector<CUtensorMap> mo(n);  // fp32 output maps of the current product (copied at each launch)
+  // P_i = X A_i (recompute), fp32.
   for (int i = 0; i < n; ++i) {
     g.map_a[i] = &mX;
     g.map_b[i] = &sh->map_At[i];
     g.out[i] = P + static_cast<size_t>(i) * T * Fs;
+    if ((rc = out_map(&mo[i], g.out[i], T, Fs, Fs, "P_i"))) return rc;
+    g.map_out[i] = &mo[i];
   }
   g.ldo = Fs;
   g.M = static_cast<int>(T);
@@ -549,6 +561,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
     g.map_a[i] = &mHt[i];
     g.map_b[i] = &mdYt;
     g.out[i] = dB[i];
+    if ((rc = out_map(&mo[i], g.out[i], Fs, D, D, "dB_i"))) return rc;
   }
   g.ldo = D;
   g.M = static_cast<int>(Fs);
@@ -563,6 +576,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
     g.map_a[i] = &mXt;
     g.map_b[i] = &mdPt[i];
     g.out[i] = dA[i];
+    if ((rc = out_map(&mo[i], g.out[i], D, Fs, Fs, "dA_i"))) return rc;
   }
   g.ldo = Fs;
   g.M = static_cast<int>(D);
@@ -575,6 +589,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
     g.map_a[i] = &mdP[i];
     g.map_b[i] = &sh->map_A[i];
     g.out[i] = dXp ? static_cast<void*>(dXp + static_cast<size_t>(i) * T * D) : dX;
+    if ((rc = out_map(&mo[i], g.out[i], T, D, D, "dX_i"))) return rc;
   }
   g.ldo = D;
   g.M = static_cast<int>(T);

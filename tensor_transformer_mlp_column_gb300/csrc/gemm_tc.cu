@@ -39,6 +39,7 @@ struct KParams {
   CUtensorMap map_a[kMaxGroups];
   CUtensorMap map_b[kMaxGroups];
   void* out[kMaxGroups];
+  CUtensorMap map_out[kMaxGroups];  // kEpiF32Tma: fp32 output per group, 32 x 32 boxes, 128-byte swizzle
   const void* aux_p[kMaxGroups];  // kEpiBwdAct: P per group (fp32, row pitch ldo)
   void* aux_ht[kMaxGroups];       // kEpiBwdAct: H^T per group (bf16, row pitch ldt)
   void* aux_dpt[kMaxGroups];      // kEpiBwdAct: dP^T per group (bf16, row pitch ldt)
@@ -394,7 +395,12 @@ struct PairCfg {
   static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 N rows
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
-  static constexpr size_t SMEM = 1024 + size_t(STAGES) * STAGE_BYTES + 256;
+  // kEpiF32Tma: two 32 x 32 fp32 staging blocks (4 KB each) per epilogue warp.
+  static constexpr uint32_t OUT_BLOCK = 32 * 32 * 4;
+  template <int EPI>
+  static constexpr uint32_t staging() { return EPI == kEpiF32Tma ? 4 * 2 * OUT_BLOCK : 0; }
+  template <int EPI>
+  static constexpr size_t smem() { return 1024 + size_t(STAGES) * STAGE_BYTES + staging<EPI>() + 256; }
 };
 
 template <int EPI, int STAGES>
@@ -405,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint8_t* s_out = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned staging of kEpiF32Tma
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_out + C::template staging<EPI>());
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
   uint64_t* acc_empty = acc_full + 2;
@@ -550,11 +557,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     }
   } else {
     // ---------------- epilogue (warps 2..5 of both CTAs)
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
+    const int quarter = warp & 3;  // rows quarter*32 .. +31 of this CTA's 128 (its TMEM lane quarter)
     const uint32_t acc_empty_even0 = map_to_cta(smem_addr(acc_empty), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
+    int blocks_out = 0;  // kEpiF32Tma: 32 x 32 blocks this warp has handed to TMA so far
     for (int tile = cluster; tile < p.tiles; tile += nclusters) {
       int g, mb, nb;
       decode_tile(p, tile, g, mb, nb);
@@ -564,7 +571,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         break;
       }
       tc_fence_after_sync();
-      const int64_t m = int64_t(mb) * 256 + int64_t(rank) * 128 + row;
+      const int64_t m_warp = int64_t(mb) * 256 + int64_t(rank) * 128 + quarter * 32;  // row of lane 0
+      const int64_t m = m_warp + lane;
       const bool row_ok = m < p.M;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 #pragma unroll 1
@@ -578,13 +586,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           if (lane == 0) mbar_arrive_cluster(acc_empty_even0 + 8u * static_cast<uint32_t>(acc));
         }
         const int n0 = nb * BN + c;
-        if (!row_ok || n0 >= p.N) continue;
-        epilogue_store<EPI>(p, g, m, n0, v);
+        if constexpr (EPI == kEpiF32Tma) {
+          // Stage the warp's 32 x 32 fp32 block in shared memory with the
+          // 128-byte swizzle (16-byte chunk j of row r at slot j ^ (r % 8),
+          // conflict-free for these row-per-lane writes), then one TMA store
+          // writes it as whole 128-byte lines, clipped to M x N.
+          if (n0 >= p.N || m_warp >= p.M) continue;  // warp-uniform
+          uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
+          if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.map_out[g], buf, n0, static_cast<int32_t>(m_warp));
+            bulk_commit_group();
+          }
+          ++blocks_out;
+        } else {
+          if (!row_ok || n0 >= p.N) continue;
+          epilogue_store<EPI>(p, g, m, n0, v);
+        }
       }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
       }
+    }
+    if constexpr (EPI == kEpiF32Tma) {
+      if (lane == 0) bulk_wait_group_all();  // every store has left shared memory and landed
+      __syncwarp();
     }
   }
 
@@ -600,8 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 template <int EPI, int STAGES>
 cudaError_t launch_pair_impl(const KParams& kp, cudaStream_t s) {
   using C = PairCfg<STAGES>;
+  constexpr size_t kSmem = C::template smem<EPI>();
   auto kern = tc_gemm_pair_kernel<EPI, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -610,16 +645,17 @@ cudaError_t launch_pair_impl(const KParams& kp, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // Persistent grid: as many CTA pairs as can be resident at once.
-  static int max_pairs[64][2] = {{0}};
+  // Persistent grid: as many CTA pairs as can be resident at once (per device
+  // and per instantiation, since the shared-memory size differs).
+  static int max_pairs[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  int& cached = max_pairs[dev][STAGES == 7 ? 1 : 0];
+  int& cached = max_pairs[dev];
   if (!cached) {
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
     int n = 0;
@@ -699,8 +735,10 @@ int tc_box_rows_b(int N) {
   return N <= 128 ? 128 : 256;
 }
 
-bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
-                      int box_rows) {
+// A 2-D row-major tensor [rows, cols] with a row pitch of pitch_bytes, boxes
+// of box_cols x box_rows elements, 128-byte swizzle.
+static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows, int64_t cols,
+                      int64_t pitch_bytes, int box_cols, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q;
@@ -712,13 +750,22 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_elems) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
+                      int box_rows) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, pitch_elems * 2, BK, box_rows);
+}
+
+bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rows, cols, pitch_elems * 4, 32, 32);
 }
 
 cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
@@ -731,8 +778,11 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.aux_p[i] = g.aux_p[i];
     kp.aux_ht[i] = g.aux_ht[i];
     kp.aux_dpt[i] = g.aux_dpt[i];
+    if (g.map_out[i]) kp.map_out[i] = *g.map_out[i];
   }
   const bool pair = use_pair_kernel();
+  // fp32 outputs with TMA maps leave the pair kernel through TMA stores.
+  const bool tma_out = pair && g.epi == kEpiF32 && g.map_out[0] != nullptr && env_int("TPMLP_TMA_STORE", 1) != 0;
   const int BN = pair ? 256 : tc_box_rows_b(g.N);
   const int TM = pair ? 256 : BM;
   kp.ldo = g.ldo;
@@ -756,6 +806,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
       return pair ? launch_pair_impl<kEpiGeluBf16, 6>(kp, s)
                   : (BN == 256 ? launch_impl<256, kEpiGeluBf16>(kp, s) : launch_impl<128, kEpiGeluBf16>(kp, s));
     case kEpiF32:
+      if (tma_out) return launch_pair_impl<kEpiF32Tma, 6>(kp, s);
       return pair ? launch_pair_impl<kEpiF32, 6>(kp, s)
                   : (BN == 256 ? launch_impl<256, kEpiF32>(kp, s) : launch_impl<128, kEpiF32>(kp, s));
     case kEpiBwdAct:

@@ -24,6 +24,7 @@ enum TcEpilogue : int {
   kEpiGeluBf16 = 0,  // out bf16 = GeLU(acc)
   kEpiF32 = 1,       // out fp32 = acc
   kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), aux_ht = GeLU(P)^T, aux_dpt = out^T (P from aux_p)
+  kEpiF32Tma = 3,    // out fp32 = acc through TMA stores (chosen by the launcher when map_out is given)
 };
 
 enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
@@ -38,6 +39,7 @@ struct TcGemm {
   const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
   const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
+  const CUtensorMap* map_out[kMaxGroups];  // optional fp32 output maps (make_output_map_f32) for TMA stores
   const void* aux_p[kMaxGroups];         // kEpiBwdAct only: P (fp32, row stride ldo)
   void* aux_ht[kMaxGroups];              // kEpiBwdAct only: H^T (bf16, row stride ldt)
   void* aux_dpt[kMaxGroups];             // kEpiBwdAct only: dP^T (bf16, row stride ldt)
@@ -58,6 +60,10 @@ struct TcGemm {
 // 128-byte swizzling. Returns false if the driver rejects it.
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
                       int box_rows);
+
+// Encodes a TMA map for an fp32 output matrix [rows, cols] (row pitch
+// pitch_elems) written in 32 x 32 boxes with 128-byte swizzling.
+bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
 
 // Box heights of the two operands used by the tensor-core kernel.
 constexpr int kTcBoxRowsA = 128;
