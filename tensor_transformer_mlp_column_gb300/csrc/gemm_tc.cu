@@ -398,7 +398,9 @@ struct PairCfg {
   // kEpiF32Tma: two 32 x 32 fp32 staging blocks (4 KB each) per epilogue warp.
   static constexpr uint32_t OUT_BLOCK = 32 * 32 * 4;
   template <int EPI>
-  static constexpr uint32_t staging() { return EPI == kEpiF32Tma ? 4 * 2 * OUT_BLOCK : 0; }
+  static constexpr uint32_t staging() {
+    return EPI == kEpiF32Tma ? 4 * 2 * OUT_BLOCK : 0;
+  }
   template <int EPI>
   static constexpr size_t smem() { return 1024 + size_t(STAGES) * STAGE_BYTES + staging<EPI>() + 256; }
 };
@@ -597,8 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           __syncwarp();
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                           __float_as_uint(v[4 * j + 3]));
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -768,6 +771,7 @@ bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t col
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rows, cols, pitch_elems * 4, 32, 32);
 }
 
+
 cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   KParams kp;
   memset(&kp, 0, sizeof(kp));
@@ -780,9 +784,14 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.aux_dpt[i] = g.aux_dpt[i];
     if (g.map_out[i]) kp.map_out[i] = *g.map_out[i];
   }
-  const bool pair = use_pair_kernel();
-  // fp32 outputs with TMA maps leave the pair kernel through TMA stores.
-  const bool tma_out = pair && g.epi == kEpiF32 && g.map_out[0] != nullptr && env_int("TPMLP_TMA_STORE", 1) != 0;
+  // CTA pairs with 256 x 256 tiles, unless the product has too few of those
+  // tiles to occupy a quarter of the SMs: then single CTAs with 128-row tiles
+  // (and 128-column tiles, the operand boxes that pair mode encodes) spread it
+  // over four times as many SMs.
+  const int pair_tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256) * (g.chain ? 1 : g.groups);
+  const bool pair = use_pair_kernel() && pair_tiles >= num_sms() / 4;
+  // Outputs with TMA maps leave the pair kernel through TMA stores.
+  const bool tma_out = pair && g.map_out[0] != nullptr && env_int("TPMLP_TMA_STORE", 1) != 0;
   const int BN = pair ? 256 : tc_box_rows_b(g.N);
   const int TM = pair ? 256 : BM;
   kp.ldo = g.ldo;

@@ -64,7 +64,6 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 // Encodes a TMA map for an fp32 output matrix [rows, cols] (row pitch
 // pitch_elems) written in 32 x 32 boxes with 128-byte swizzling.
 bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
-
 // Box heights of the two operands used by the tensor-core kernel.
 constexpr int kTcBoxRowsA = 128;
 int tc_box_rows_b(int N);
