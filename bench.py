@@ -31,6 +31,38 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+
+# DRAM bytes (read + write) per launch of each kernel of the step on the large
+# workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum,
+# one pass; command and figures in profiles/traffic_large_forward.md). Valid
+# only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
+# source_hash() of those sources, and a different hash reports null.
+TRAFFIC_SOURCE_HASH = "1b1679d8f59aad88"
+TRAFFIC_BYTES = {
+    "gemm1_gelu(faithful)": 1_810_996_224,
+    "gemm2_partials": 2_955_575_296,
+    "allreduce": 2_404_559_872,
+    "gemm1_gelu(fused)": 1_808_030_464,
+    "gemm2_fused_sum": 2_969_479_680,
+}
+
+
+def source_hash() -> str:
+    import hashlib
+
+    d = os.path.join(ROOT, "tensor_transformer_mlp_column_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_of(kernel: str):
+    if source_hash() != TRAFFIC_SOURCE_HASH:
+        return None
+    return TRAFFIC_BYTES.get(kernel)
 METRIC = "TP-MLP fwd TFLOP/s on 1 GB300 (% BF16 peak); partial-sum reduce GB/s (% HBM)"
 
 
@@ -482,16 +514,22 @@ def main():
                                 "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4)}
     step_ms_sum = sum(avg.values())
     dominant = max(avg, key=lambda k: avg[k])
+    default_workload = args.workload == "large" and not args.T and not args.N
+    traffic = traffic_of(dominant) if default_workload else None
     if dominant == "allreduce":
         ach = reduce_bytes / (avg[dominant] * 1e-3) / 1e9
         roof = {"kernel": dominant, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": None,
-                "peak_source": peaks["source"]}
+                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes": reduce_bytes, "peak_source": peaks["source"]}
     else:
         ach = flops_of[dominant] / (avg[dominant] * 1e-3) / 1e12
         pk = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
-                "frac": round(ach / pk, 4), "traffic": None,
+                "frac": round(ach / pk, 4), "traffic": traffic,
+                "algorithmic_flops": flops_of[dominant],
+                # operands read once and results written once
+                "algorithmic_bytes": (2.0 * (T * D + D * F + T * F) if dominant.startswith("gemm1") else
+                                      2.0 * (T * F + F * D) + 4.0 * T * D * (N if dominant == "gemm2_partials" else 1)),
                 "peak_source": peaks["source"] + " (sustained bf16, kernel timed inside a long step)"}
     red_gbs = reduce_bytes / (avg["allreduce"] * 1e-3) / 1e9
     value = job_throughput(world, step_flops, ms_step)
