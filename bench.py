@@ -283,34 +283,61 @@ def bench_tpmlp(args, rank, world, local_rank):
             per_kernel[name].append(evs[i].elapsed_time(evs[i + 1]))
     avg = {k: sum(v) / len(v) for k, v in per_kernel.items()}
 
-    # ---- end to end through the public API, host buffers, copies inside the timed region
+    # ---- end to end through the public API, host buffers, copies inside the timed region.
+    # Every step uploads its input X from pinned host memory, runs tpmlp_forward in
+    # both modes and downloads both results. The copies run on their own streams
+    # with double-buffered device tensors, so step k+1's upload and step k's
+    # downloads overlap the compute of the neighbouring steps.
+    del H, Yp, Y1, Y2
     Xh = inp["X"].pin_memory()
-    Yh1 = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    Yh2 = torch.empty((T, D), dtype=torch.float32).pin_memory()
-    Xd = torch.empty_like(X)
+    Yh1 = [torch.empty((T, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    Yh2 = [torch.empty((T, D), dtype=torch.float32).pin_memory() for _ in range(2)]
+    Xd = [torch.empty_like(X) for _ in range(2)]
+    Yd1 = [torch.empty((T, D), dtype=torch.float32, device=dev) for _ in range(2)]
+    Yd2 = [torch.empty((T, D), dtype=torch.float32, device=dev) for _ in range(2)]
     ws_f = torch.empty(tp.tpmlp_workspace_bytes(T, sh, "faithful"), dtype=torch.uint8, device=dev)
     ws_u = torch.empty(tp.tpmlp_workspace_bytes(T, sh, "fused"), dtype=torch.uint8, device=dev)
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready, in_free, y1_ready, y2_ready, out_free = ([ev(), ev()] for _ in range(5))
 
-    def e2e_step():
-        Xd.copy_(Xh, non_blocking=True)
-        tp.tpmlp_forward(Xd, sh, "faithful", Y1, ws_f)
-        Yh1.copy_(Y1, non_blocking=True)
-        tp.tpmlp_forward(Xd, sh, "fused", Y2, ws_u)
-        Yh2.copy_(Y2, non_blocking=True)
+    def e2e_step(k):
+        b = k % 2
+        with torch.cuda.stream(s_in):
+            if k >= 2:
+                s_in.wait_event(in_free[b])  # step k-2 has finished reading Xd[b]
+            Xd[b].copy_(Xh, non_blocking=True)
+            in_ready[b].record(s_in)
+        stream.wait_event(in_ready[b])
+        if k >= 2:
+            stream.wait_event(out_free[b])  # step k-2's results have been downloaded
+        tp.tpmlp_forward(Xd[b], sh, "faithful", Yd1[b], ws_f, stream)
+        y1_ready[b].record(stream)
+        tp.tpmlp_forward(Xd[b], sh, "fused", Yd2[b], ws_u, stream)
+        y2_ready[b].record(stream)
+        in_free[b].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(y1_ready[b])
+            Yh1[b].copy_(Yd1[b], non_blocking=True)
+            s_out.wait_event(y2_ready[b])
+            Yh2[b].copy_(Yd2[b], non_blocking=True)
+            out_free[b].record(s_out)
 
-    for _ in range(max(1, min(args.warmup, 3))):
-        e2e_step()
+    for k in range(max(2, min(args.warmup, 3))):
+        e2e_step(k)
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e2e_steps = max(2, min(args.steps, 20))
+    e0.record(s_in)  # before the first upload
+    for k in range(e2e_steps):
+        e2e_step(k)
+    e1.record(s_out)  # after the last download
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     tp.tpmlp_check_status(stream)
+    Yh1, Yh2 = Yh1[0], Yh2[0]
 
     res = {
         "total_ms": total_ms, "avg": avg, "clocks": clk, "e2e_ms": e2e_ms,
@@ -334,6 +361,37 @@ def max_over_ranks(values, device):
 def job_throughput(world: int, flops_per_step_per_rank: float, ms_per_step: float) -> float:
     """Whole-job TFLOP/s: every rank's work divided by the slowest rank's time."""
     return world * flops_per_step_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
+def bench_gelu(local_rank, peaks):
+    """tpmlp_gelu on 1 GiB of input (bf16 and fp32): 2 * n * sizeof(elt) bytes per call."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for dt, name in ((torch.bfloat16, "bf16"), (torch.float32, "f32")):
+        n = (1 << 30) // torch.tensor([], dtype=dt).element_size()
+        x = torch.randn(n, device=dev, dtype=torch.float32).to(dt)
+        y = torch.empty_like(x)
+        for _ in range(3):
+            tp.tpmlp_gelu(x, y)
+        reps = 20
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(reps):
+            tp.tpmlp_gelu(x, y)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        gbs = 2.0 * n * x.element_size() / (ms * 1e-3) / 1e9
+        out[name] = {"elements": n, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+        del x, y
+    return out
 
 
 def bench_small_workloads(local_rank):
@@ -561,6 +619,7 @@ def main():
     if not args.no_backward and world == 1 and not args.T and not args.N:
         line["backward"] = bench_backward(args, local_rank, peaks)
         line["other_workloads"] = bench_small_workloads(local_rank)
+        line["gelu"] = bench_gelu(local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))
