@@ -177,6 +177,17 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
                    void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
                    size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* Test hook for the time limits inside the tensor-core product: runs the
+ * H_i = GeLU(X A_i) product of tpmlp_hidden (bf16 shards only) with stage
+ * fill number `fill` (1-based, counted by each CTA's producer) never issued,
+ * and a wait limit of limit_ms (1..10000). Every CTA that reaches that fill
+ * gives up after the limit, drains its copies and MMAs, frees its tensor
+ * memory and records TPMLP_ERR_TIMEOUT, which the next tpmlp_check_status()
+ * returns; the other CTAs finish normally. H is left partly written.
+ * TPMLP_ERR_UNSUPPORTED for fp32 shards. */
+int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* shards, void* H, int fill,
+                                      int limit_ms, tpmlp_stream_t stream);
+
 /* tpmlp_forward without any allocation: the same Y, but the scratch lives in
  * a fixed 64 MiB array of device memory that the library reserves on every
  * GPU where its device code is loaded and keeps until the process exits. (The

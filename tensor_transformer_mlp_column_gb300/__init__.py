@@ -59,6 +59,7 @@ SIGNATURES = {
     "tpmlp_backward": (_I, [_P, _P, _I64, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
     "tpmlp_selftest_wait_timeout": (_I, [_I, _P]),
     "tpmlp_forward_noalloc": (_I, [_P, _I64, _P, _P, _I, _P]),
+    "tpmlp_selftest_gemm_withheld_fill": (_I, [_P, _I64, _P, _P, _I, _I, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -280,6 +281,13 @@ def tpmlp_forward_noalloc(X: torch.Tensor, shards: Shards, Y: torch.Tensor, mode
     _check(lib().tpmlp_forward_noalloc(_dev(X, "X"), X.shape[0], shards.handle, _dev(Y, "Y"), _mode(mode),
                                        _stream(stream)), "tpmlp_forward_noalloc")
     return Y
+
+
+def tpmlp_selftest_gemm_withheld_fill(X: torch.Tensor, shards: Shards, H: torch.Tensor, fill: int, limit_ms: int,
+                                      stream=None) -> None:
+    """Runs the GeLU(X A_i) product with stage fill `fill` withheld (test hook)."""
+    _check(lib().tpmlp_selftest_gemm_withheld_fill(_dev(X, "X"), X.shape[0], shards.handle, _dev(H, "H"), fill,
+                                                   limit_ms, _stream(stream)), "tpmlp_selftest_gemm_withheld_fill")
 
 
 def tpmlp_selftest_wait_timeout(limit_ms: int, stream=None) -> None:

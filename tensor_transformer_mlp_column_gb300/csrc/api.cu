@@ -144,8 +144,10 @@ int out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t pitc
 
 // ----------------------------------------------------------- step launchers
 
-// H_i = GeLU(X A_i) for every shard.
-int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaStream_t s) {
+// H_i = GeLU(X A_i) for every shard. `inject` and `wait_ns` are the test
+// hooks of tpmlp_selftest_gemm_withheld_fill (0 = off / the default limit).
+int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaStream_t s, int inject = 0,
+               uint64_t wait_ns = 0) {
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     CUtensorMap mx;
@@ -166,7 +168,8 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
     g.shared = kSharedA;  // X feeds every shard
     g.group_m = 8;        // bands of 8 M blocks: best measured at the large workload
     g.stream_out = 1;
-    TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
+    g.inject = inject;
+    TRY_CUDA(launch_tc_gemm(g, wait_ns ? wait_ns : wait_limit_ns(), s));
     return TPMLP_OK;
   }
   for (int i = 0; i < sh->n; ++i) {
@@ -601,6 +604,19 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
   return TPMLP_OK;
+}
+
+int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* sh, void* H, int fill,
+                                      int limit_ms, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (!X || !H) return fail(TPMLP_ERR_ARG, "X and H must not be NULL");
+  if (!aligned16(X) || !aligned16(H)) return fail(TPMLP_ERR_ALIGN, "X and H must be 16-byte aligned");
+  if (fill < 1) return fail(TPMLP_ERR_ARG, "fill = %d must be >= 1", fill);
+  if (limit_ms < 1 || limit_ms > 10000) return fail(TPMLP_ERR_ARG, "limit_ms = %d outside 1..10000", limit_ms);
+  if (sh->dt != TPMLP_BF16) return fail(TPMLP_ERR_UNSUPPORTED, "the tensor-core product needs bf16 shards");
+  if ((rc = check_handle_device(sh))) return rc;
+  return run_hidden(X, T, sh, H, stream, fill, static_cast<uint64_t>(limit_ms) * 1000000ull);
 }
 
 int tpmlp_selftest_wait_timeout(int limit_ms, tpmlp_stream_t stream) {

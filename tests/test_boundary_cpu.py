@@ -112,6 +112,7 @@ def test_gelu_and_allreduce_argument_errors(tp):
     assert l.tpmlp_allreduce(FAKE, 2, 0, FAKE, None) == tp.TPMLP_OK
     assert l.tpmlp_allreduce(FAKE, 2, 8, FAKE + 8, None) == tp.TPMLP_ERR_ALIGN
     assert l.tpmlp_selftest_wait_timeout(0, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_selftest_gemm_withheld_fill(FAKE, 16, None, FAKE, 1, 10, None) == tp.TPMLP_ERR_ARG
 
 
 def test_calls_without_a_gpu_report_cuda_or_device_errors(tp):
