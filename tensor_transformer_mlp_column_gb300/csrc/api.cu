@@ -151,7 +151,7 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     CUtensorMap mx;
-    int rc = map_or_fail(&mx, X, T, D, D, kTcBoxRowsA, "X");
+    int rc = map_or_fail(&mx, X, T, D, D, tc_box_rows_a(), "X");
     if (rc) return rc;
     TcGemm g{};
     g.groups = sh->n;
@@ -166,7 +166,7 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
     g.K = static_cast<int>(D);
     g.epi = kEpiGeluBf16;
     g.shared = kSharedA;  // X feeds every shard
-    g.group_m = 8;        // bands of 8 M blocks: best measured at the large workload
+    g.group_m = 16;       // bands of 16 M blocks: fewest DRAM re-reads of the shards' A_i^T measured
     g.stream_out = 1;
     g.inject = inject;
     TRY_CUDA(launch_tc_gemm(g, wait_ns ? wait_ns : wait_limit_ns(), s));
@@ -190,7 +190,7 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
     g.groups = sh->n;
     for (int i = 0; i < sh->n; ++i) {
       int rc = map_or_fail(&mh[i], at<uint16_t>(const_cast<void*>(H), 0) + static_cast<size_t>(i) * T * Fs, T, Fs,
-                           Fs, kTcBoxRowsA, "H_i");
+                           Fs, tc_box_rows_a(), "H_i");
       if (rc) return rc;
       g.map_a[i] = &mh[i];
       g.map_b[i] = &sh->map_Bt[i];
@@ -512,17 +512,17 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   TRY_CUDA(launch_transpose_u16(dY, T, D, D, dYt, Tp, s));  // dY^T [D, Tp]
 
   CUtensorMap mX, mdY, mXt, mdYt;
-  if ((rc = map_or_fail(&mX, X, T, D, D, kTcBoxRowsA, "X"))) return rc;
-  if ((rc = map_or_fail(&mdY, dY, T, D, D, kTcBoxRowsA, "dY"))) return rc;
-  if ((rc = map_or_fail(&mXt, Xt, D, T, Tp, kTcBoxRowsA, "X^T"))) return rc;
+  if ((rc = map_or_fail(&mX, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
+  if ((rc = map_or_fail(&mdY, dY, T, D, D, tc_box_rows_a(), "dY"))) return rc;
+  if ((rc = map_or_fail(&mXt, Xt, D, T, Tp, tc_box_rows_a(), "X^T"))) return rc;
   if ((rc = map_or_fail(&mdYt, dYt, D, T, Tp, tc_box_rows_b(static_cast<int>(D)), "dY^T"))) return rc;
   std::vector<CUtensorMap> mHt(n), mdPt(n), mdP(n);
   for (int i = 0; i < n; ++i) {
-    if ((rc = map_or_fail(&mHt[i], Ht + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp, kTcBoxRowsA, "H_i^T"))) return rc;
+    if ((rc = map_or_fail(&mHt[i], Ht + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp, tc_box_rows_a(), "H_i^T"))) return rc;
     if ((rc = map_or_fail(&mdPt[i], dPt + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp,
                           tc_box_rows_b(static_cast<int>(Fs)), "dP_i^T")))
       return rc;
-    if ((rc = map_or_fail(&mdP[i], dP + static_cast<size_t>(i) * T * Fs, T, Fs, Fs, kTcBoxRowsA, "dP_i"))) return rc;
+    if ((rc = map_or_fail(&mdP[i], dP + static_cast<size_t>(i) * T * Fs, T, Fs, Fs, tc_box_rows_a(), "dP_i"))) return rc;
   }
   const uint64_t wl = wait_limit_ns();
   TcGemm g{};
@@ -542,7 +542,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.K = static_cast<int>(D);
   g.epi = kEpiF32;
   g.shared = kSharedA;  // X (then dY) feeds every shard
-  g.group_m = 8;
+  g.group_m = 16;
   g.stream_out = 0;     // P and dH are read back right away by the activation step
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dH_i = dY B_i^T with the activation step in its epilogue: dP_i = dH_i *
@@ -571,7 +571,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.N = static_cast<int>(D);
   g.K = static_cast<int>(T);
   g.shared = kSharedB;  // dY^T feeds every shard
-  g.group_m = 8;
+  g.group_m = 16;
   g.stream_out = 1;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dA_i = X^T dP_i: [D, Fs], K = T.
@@ -585,7 +585,7 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.M = static_cast<int>(D);
   g.N = static_cast<int>(Fs);
   g.shared = kSharedA;  // X^T feeds every shard
-  g.group_m = 8;
+  g.group_m = 16;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dX = sum_i dP_i A_i^T: [T, D], K = Fs.
   for (int i = 0; i < n; ++i) {

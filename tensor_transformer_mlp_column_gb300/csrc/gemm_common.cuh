@@ -1,0 +1,174 @@
+// gemm_common.cuh — what the tensor-core GEMM kernels share: the launch
+// parameter block, the tile order, and the epilogue output treatments.
+#pragma once
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace tpmlp {
+
+constexpr int BM = 128;  // rows of a tile per CTA
+constexpr int BK = 64;   // K per pipeline stage: one 128-byte swizzle row of bf16
+constexpr int kThreads = 192;  // warp 0 TMA producer, warp 1 MMA issuer, warps 2..5 epilogue
+
+struct KParams {
+  CUtensorMap map_a[kMaxGroups];
+  CUtensorMap map_b[kMaxGroups];
+  void* out[kMaxGroups];
+  CUtensorMap map_out[kMaxGroups];  // kEpiF32Tma: fp32 output per group, 32 x 32 boxes, 128-byte swizzle
+  const void* aux_p[kMaxGroups];    // kEpiBwdAct: P per group (fp32, row pitch ldo)
+  void* aux_ht[kMaxGroups];         // kEpiBwdAct: H^T per group (bf16, row pitch ldt)
+  void* aux_dpt[kMaxGroups];        // kEpiBwdAct: dP^T per group (bf16, row pitch ldt)
+  int64_t ldo, ldt;
+  int M, N;
+  int groups;
+  int chain;
+  int m_blocks, n_blocks, k_blocks;  // tile-grid units of the kernel that runs (see decode_tile)
+  int tiles;
+  uint64_t wait_ns;
+  int* status;     // device status word (bounded waits record their site here)
+  int inject;      // test hook: > 0 withholds that fill (1-based) in every CTA
+  int a_box;       // rows of the M x K operand's TMA box (128, or 64 when quads split it)
+  int group_m;     // tile order: bands of group_m tile rows, rows fastest inside a band (1 = columns fastest)
+  int shared;      // kSharedNone / kSharedA / kSharedB: an operand that every group reads
+  int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
+};
+
+// Maps a tile index to (group, M block, N block). The tiles form a grid of
+// `rows` x `cols`, walked in bands of group_m rows with rows fastest inside a
+// band, so the tiles in flight together cover about group_m rows x
+// (tiles in flight / group_m) columns and each operand panel is fetched from
+// DRAM about once per band instead of once per tile.
+//   shared A (every group reads the same M x K operand): rows = M blocks,
+//     cols = the groups' N blocks side by side;
+//   shared B (every group reads the same N x K operand): rows = the groups'
+//     M blocks stacked, cols = N blocks;
+//   otherwise each group's grid in turn (chain mode: the one output grid).
+// "Blocks" are the kernel's tile units (for the CTA-quad kernel an N block is
+// a pair of 256-column blocks).
+__device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
+  int rows_total, cols, base = 0;
+  if (p.chain || p.shared == kSharedNone) {
+    const int per_group = p.m_blocks * p.n_blocks;
+    g = p.chain ? 0 : tile / per_group;
+    base = g * per_group;
+    rows_total = p.m_blocks;
+    cols = p.n_blocks;
+  } else if (p.shared == kSharedA) {
+    rows_total = p.m_blocks;
+    cols = p.groups * p.n_blocks;
+  } else {
+    rows_total = p.groups * p.m_blocks;
+    cols = p.n_blocks;
+  }
+  const int t = tile - base;
+  const int gm = p.group_m > 0 ? p.group_m : 1;
+  const int span = gm * cols;
+  const int first = (t / span) * gm;
+  const int band = min(rows_total - first, gm);
+  const int q = t % span;
+  const int row = first + q % band;
+  const int col = q / band;
+  if (p.chain || p.shared == kSharedNone) {
+    mb = row;
+    nb = col;
+  } else if (p.shared == kSharedA) {
+    mb = row;
+    g = col / p.n_blocks;
+    nb = col % p.n_blocks;
+  } else {
+    g = row / p.m_blocks;
+    mb = row % p.m_blocks;
+    nb = col;
+  }
+}
+
+// 16-byte global stores; `stream` marks them evict-first so results that are
+// not read again soon do not push the operands out of L2.
+__device__ __forceinline__ void store16(void* dst, uint4 v, bool stream) {
+  if (stream)
+    __stcs(reinterpret_cast<uint4*>(dst), v);
+  else
+    *reinterpret_cast<uint4*>(dst) = v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Output treatment of one thread's 32 accumulator columns n0..n0+31 of row m
+// (group g). The caller has checked m < M and n0 < N; N is a multiple of 8.
+template <int EPI>
+__device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
+  if constexpr (EPI == kEpiGeluBf16) {
+    // H = GeLU(acc), bf16, row-major.
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n0 + 8 * j + 8 <= p.N) {
+        uint4 w;
+        w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
+        w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
+        w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
+        w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
+        store16(out + 8 * j, w, p.stream_out);
+      }
+    }
+  } else if constexpr (EPI == kEpiF32) {
+    float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (n0 + 4 * j + 4 <= p.N)
+        store16(out + 4 * j,
+                make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                           __float_as_uint(v[4 * j + 3])),
+                p.stream_out);
+    }
+  } else {
+    // Backward activation: acc = dH (row m = token t, column n = feature f).
+    // With P from aux_p: dP = dH * GeLU'(P) to out (bf16 [T][ldo]), and the
+    // transposes H^T = GeLU(P)^T to aux_ht and dP^T to aux_dpt (bf16 [F][ldt]).
+    // The 32 lanes of a warp hold 32 consecutive tokens, so each transposed
+    // store of one column is 64 contiguous bytes.
+    const float* P = static_cast<const float*>(p.aux_p[g]) + m * p.ldo + n0;
+    __nv_bfloat16* dP = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+    __nv_bfloat16* Ht = static_cast<__nv_bfloat16*>(p.aux_ht[g]) + int64_t(n0) * p.ldt + m;
+    __nv_bfloat16* dPt = static_cast<__nv_bfloat16*>(p.aux_dpt[g]) + int64_t(n0) * p.ldt + m;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n0 + 8 * j + 8 > p.N) continue;
+      const float4 p0 = *reinterpret_cast<const float4*>(P + 8 * j);
+      const float4 p1 = *reinterpret_cast<const float4*>(P + 8 * j + 4);
+      const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      float h[8], d[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float gv, dg;
+        gelu_and_grad_fast(pv[e], gv, dg);
+        h[e] = gv;
+        d[e] = v[8 * j + e] * dg;
+      }
+      uint4 w;
+      w.x = pack_bf16x2(d[0], d[1]);
+      w.y = pack_bf16x2(d[2], d[3]);
+      w.z = pack_bf16x2(d[4], d[5]);
+      w.w = pack_bf16x2(d[6], d[7]);
+      store16(dP + 8 * j, w, false);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int64_t o = int64_t(8 * j + e) * p.ldt;
+        Ht[o] = __float2bfloat16_rn(h[e]);
+        dPt[o] = __float2bfloat16_rn(d[e]);
+      }
+    }
+  }
+}
+
+// Launches the CTA-pair kernel (quad = 0) or the CTA-quad kernel (quad = 1,
+// two pairs sharing the M x K operand through TMA multicast) with epilogue
+// `epi`; kp's tile units must match (256-row M blocks; 256-column N blocks,
+// or pairs of them for the quad kernel).
+cudaError_t launch_pair(const KParams& kp, int epi, int quad, cudaStream_t s);
+
+}  // namespace tpmlp

@@ -1,0 +1,357 @@
+// gemm_pair.cu — tcgen05 cta_group::2 GEMM: a CTA pair (cluster of 2 CTAs on
+// two SMs) computes one 256 x 256 tile; optionally two pairs form a quad
+// (cluster of 4) that computes two 256 x 256 tiles side by side in N and
+// shares the M x K operand through TMA multicast.
+//
+// Per k-block each CTA brings in its 128 rows of the M x K operand and its
+// 128 of the 256 rows of the N x K operand (the pair MMA reads both CTAs'
+// shared memory). In a quad, the two CTAs at the same position of the two
+// pairs need the same 128 M x K rows: each loads 64 of them once and
+// multicasts them to both, so a CTA fetches 24 KB per k-block instead of 32 KB
+// and L2 serves 25 % fewer bytes per MMA.
+//   every CTA, warp 0 lane 0 : TMA producer; the pair's bytes are counted on
+//                              the full barrier of the pair's even CTA, which
+//                              its producer arms with both CTAs' bytes
+//   even CTA, warp 1 lane 0  : MMA issuer (M=256, N=256, K=16 per
+//                              instruction) into one of two TMEM accumulators;
+//                              commits free each stage in every CTA that shares
+//                              it and publish each accumulator in the pair
+//   every CTA, warps 2..5    : epilogue of the CTA's own 128 rows; release the
+//                              accumulator on the pair's even CTA
+// Every wait is bounded; on a timeout the CTA raises the abort flag of every
+// CTA of its cluster, all roles leave their loops, copies in flight and MMAs
+// are drained, and both CTAs of each pair free their TMEM.
+#include "gemm_common.cuh"
+
+namespace tpmlp {
+
+namespace {
+
+template <int STAGES_>
+struct PairCfg {
+  static constexpr int STAGES = STAGES_;
+  static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
+  static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 N rows
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
+  // kEpiF32Tma: two 32 x 32 fp32 staging blocks (4 KB each) per epilogue warp.
+  static constexpr uint32_t OUT_BLOCK = 32 * 32 * 4;
+  template <int EPI>
+  static constexpr uint32_t staging() {
+    return EPI == kEpiF32Tma ? 4 * 2 * OUT_BLOCK : 0;
+  }
+  template <int EPI>
+  static constexpr size_t smem() {
+    return 1024 + size_t(STAGES) * STAGE_BYTES + staging<EPI>() + 256;
+  }
+};
+
+template <int EPI, int STAGES, bool QUAD>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ KParams p) {
+  using C = PairCfg<STAGES>;
+  constexpr int BN = 256;
+  constexpr uint32_t kCtas = QUAD ? 4 : 2;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint8_t* s_out = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned staging of kEpiF32Tma
+  uint64_t* full = reinterpret_cast<uint64_t*>(s_out + C::template staging<EPI>());
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const uint32_t pos = rank & 1u;   // position in the pair: 0 = even CTA, issues the pair's MMAs
+  const uint32_t pq = rank >> 1;    // which pair of the quad (always 0 for a lone pair)
+  const uint32_t lead = rank & ~1u; // the pair's even CTA
+  const int cluster = static_cast<int>(cluster_id_x());
+  const int nclusters = static_cast<int>(cluster_count_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full + s, 1);                    // even CTA: its producer's arrive (+ the pair's bytes)
+      mbar_init(empty + s, QUAD ? 2u : 1u);      // one commit from each pair whose MMAs read the stage
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + b, 1);   // one commit per tile
+      mbar_init(acc_empty + b, 8);  // even CTA: one arrival per epilogue warp of the pair
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int g = 0; g < p.groups; ++g) {
+      tma_prefetch_desc(&p.map_a[g]);
+      tma_prefetch_desc(&p.map_b[g]);
+    }
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+  tc_fence_before_sync();
+  cluster_sync_all();  // barriers of every CTA initialised, TMEM allocated
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const WaitGuard guard{abort_flag, p.wait_ns, p.status};
+  const uint32_t abort_addr = smem_addr(const_cast<int*>(abort_flag));
+  auto raise_abort_in_cluster = [&]() {
+    for (uint32_t r = 0; r < kCtas; ++r)
+      if (r != rank) st_cluster_u32(map_to_cta(abort_addr, r), 1u);
+  };
+  const int kb_per_tile = p.chain ? p.groups * p.k_blocks : p.k_blocks;
+  bool aborted = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (every CTA)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, parity_bits = 0;
+      int fill = 0;
+      for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        int g, mb, nb;
+        decode_tile(p, tile, g, mb, nb);
+        const int m0 = mb * 256 + static_cast<int>(pos) * 128;
+        const int nb256 = QUAD ? 2 * nb + static_cast<int>(pq) : nb;
+        const int n0 = nb256 * BN + static_cast<int>(pos) * 128;
+        int gg = g, kk = 0;  // group and K block of the next fill (chain mode walks the groups in order)
+        for (int kb = 0; kb < kb_per_tile; ++kb, ++kk) {
+          if (kk == p.k_blocks) {
+            kk = 0;
+            ++gg;
+          }
+          if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
+            aborted = true;
+            break;
+          }
+          const uint32_t full_lead = map_to_cta(smem_addr(full + stage), lead);
+          ++fill;
+          if (fill != p.inject) {
+            if (pos == 0) {
+              mbar_arrive_expect_tx(full + stage, 2 * C::STAGE_BYTES);
+              armed |= 1u << stage;
+              parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+            }
+            if constexpr (QUAD) {
+              // 64 of this position's 128 M x K rows, to this CTA and its twin in the other pair.
+              const uint16_t mask = static_cast<uint16_t>((1u << pos) | (1u << (2 + pos)));
+              tma_load_2d_pair_multicast(sA + stage * C::A_BYTES + pq * (C::A_BYTES / 2), &p.map_a[gg], kk * BK,
+                                         m0 + static_cast<int>(pq) * 64, full_lead, mask);
+            } else {
+              tma_load_2d_pair(sA + stage * C::A_BYTES, &p.map_a[gg], kk * BK, m0, full_lead);
+            }
+            tma_load_2d_pair(sB + stage * C::B_BYTES, &p.map_b[gg], kk * BK, n0, full_lead);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (aborted) {
+        raise_abort_in_cluster();
+        if (pos == 0) {
+          for (int s = 0; s < C::STAGES; ++s)
+            if (armed >> s & 1u) wait_drain(full + s, (parity_bits >> s) & 1u, p.wait_ns);
+        } else {
+          // This CTA's copies are counted on the even CTA's barriers; give any
+          // copy still in flight time to land before shared memory is released.
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && pos == 0) {
+      // ---------------- MMA issuer (even CTA of each pair)
+      constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
+      constexpr uint16_t kStageMask = QUAD ? 0xF : 0x3;  // CTAs whose shared memory holds this pair's stages
+      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        if (!wait_bounded(acc_empty + acc, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < kb_per_tile; ++kb) {
+          if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES);
+          const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+                             (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_multicast(empty + stage, kStageMask);  // frees the stage once these MMAs have read it
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (aborted) break;
+        tc_commit_pair_multicast(acc_full + acc, pair_mask);  // accumulator complete in both CTAs of the pair
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (aborted) {
+        raise_abort_in_cluster();
+        tc_commit_pair_multicast(drain, static_cast<uint16_t>(1u << rank));
+        wait_drain(drain, 0, p.wait_ns);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5 of every CTA)
+    const int quarter = warp & 3;  // rows quarter*32 .. +31 of this CTA's 128 (its TMEM lane quarter)
+    const uint32_t acc_empty_lead = map_to_cta(smem_addr(acc_empty), lead);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int blocks_out = 0;  // kEpiF32Tma: 32 x 32 blocks this warp has handed to TMA so far
+    for (int tile = cluster; tile < p.tiles; tile += nclusters) {
+      int g, mb, nb;
+      decode_tile(p, tile, g, mb, nb);
+      bool ok = wait_bounded(acc_full + acc, acc_phase, guard, kSiteEpilogue);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) raise_abort_in_cluster();
+        break;
+      }
+      tc_fence_after_sync();
+      const int nb256 = QUAD ? 2 * nb + static_cast<int>(pq) : nb;
+      const int64_t m_warp = int64_t(mb) * 256 + int64_t(pos) * 128 + quarter * 32;  // row of lane 0
+      const int64_t m = m_warp + lane;
+      const bool row_ok = m < p.M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        float v[32];
+        __syncwarp();
+        tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
+        if (c + 32 == BN) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
+        }
+        const int n0 = nb256 * BN + c;
+        if constexpr (EPI == kEpiF32Tma) {
+          // Stage the warp's 32 x 32 fp32 block in shared memory with the
+          // 128-byte swizzle (16-byte chunk j of row r at slot j ^ (r % 8),
+          // conflict-free for these row-per-lane writes), then one TMA store
+          // writes it as whole 128-byte lines, clipped to M x N.
+          if (n0 >= p.N || m_warp >= p.M) continue;  // warp-uniform
+          uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
+          if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_uint4(__float_as_uint(v[4 * j]), __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                           __float_as_uint(v[4 * j + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.map_out[g], buf, n0, static_cast<int32_t>(m_warp));
+            bulk_commit_group();
+          }
+          ++blocks_out;
+        } else {
+          if (!row_ok || n0 >= p.N) continue;
+          epilogue_store<EPI>(p, g, m, n0, v);
+        }
+      }
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if constexpr (EPI == kEpiF32Tma) {
+      if (lane == 0) bulk_wait_group_all();  // every store has left shared memory and landed
+      __syncwarp();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncwarp();
+  cluster_sync_all();  // every CTA done: no MMA, copy or remote arrival still targets any of them
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int EPI, int STAGES, bool QUAD>
+cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
+  using C = PairCfg<STAGES>;
+  constexpr size_t kSmem = C::template smem<EPI>();
+  constexpr unsigned kCtas = QUAD ? 4 : 2;
+  auto kern = tc_gemm_pair_kernel<EPI, STAGES, QUAD>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Persistent grid: as many clusters as can be resident at once (per device
+  // and per instantiation, since the shared-memory size differs).
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  int& cached = max_clusters[dev];
+  if (!cached) {
+    cfg.gridDim = dim3(kCtas * (num_sms() / kCtas), 1, 1);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    cached = n > 0 ? n : 1;
+  }
+  const int clusters = kp.tiles < cached ? kp.tiles : cached;
+  cfg.gridDim = dim3(kCtas * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, kp);
+}
+
+template <bool QUAD>
+cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
+  switch (epi) {
+    case kEpiGeluBf16:
+      return launch_impl<kEpiGeluBf16, 6, QUAD>(kp, s);
+    case kEpiF32:
+      return launch_impl<kEpiF32, 6, QUAD>(kp, s);
+    case kEpiBwdAct:
+      return launch_impl<kEpiBwdAct, 6, QUAD>(kp, s);
+    case kEpiF32Tma:
+      return launch_impl<kEpiF32Tma, 6, QUAD>(kp, s);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_pair(const KParams& kp, int epi, int quad, cudaStream_t s) {
+  return quad ? launch_epi<true>(kp, epi, s) : launch_epi<false>(kp, epi, s);
+}
+
+}  // namespace tpmlp

@@ -65,8 +65,8 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
 // pitch_elems) written in 32 x 32 boxes with 128-byte swizzling.
 bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
 // Box heights of the two operands used by the tensor-core kernel.
-constexpr int kTcBoxRowsA = 128;
-int tc_box_rows_b(int N);
+int tc_box_rows_a();       // M x K operand (rows of the output)
+int tc_box_rows_b(int N);  // N x K operand of a product with N output columns
 
 cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s);
 
