@@ -463,25 +463,35 @@ def bench_backward(args, local_rank, peaks):
     dX = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
     dA = [torch.empty((w.D, w.Fs), dtype=torch.float32, device=dev) for _ in range(w.N)]
     dB = [torch.empty((w.Fs, w.D), dtype=torch.float32, device=dev) for _ in range(w.N)]
-    for mode in ("faithful", "fused"):
-        ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, mode, True), dtype=torch.uint8, device=dev)
+    # Pre-activations saved by a training-mode forward, for the saved-P backward.
+    _, P = tp.tpmlp_forward_save(X, sh, "fused")
+    for mode, saved in (("faithful", False), ("fused", False), ("faithful", True), ("fused", True)):
+        ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, mode, 2 if saved else 1), dtype=torch.uint8, device=dev)
+
+        def run():
+            tp.tpmlp_backward(X, dY, sh, mode, dX, dA, dB, ws, P=P if saved else None)
+
         for _ in range(3):
-            tp.tpmlp_backward(X, dY, sh, mode, dX, dA, dB, ws)
+            run()
         tp.tpmlp_check_status(stream)
         reps = max(3, min(args.steps // 10, 10))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         e0.record(stream)
         for _ in range(reps):
-            tp.tpmlp_backward(X, dY, sh, mode, dX, dA, dB, ws)
+            run()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         tp.tpmlp_check_status(stream)
         ms = e0.elapsed_time(e1) / reps
         alg = 8.0 * w.T * w.D * w.F / (ms * 1e-3) / 1e12
-        out[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
-                     "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1),
-                     "frac_bf16_incl_recompute": round(alg * 10 / 8 / peaks["bf16_tflops_sustained"], 4)}
+        if saved:  # no recompute: all 8*T*D*F FLOP are algorithmic
+            out[f"saved_P_{mode}"] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
+                                      "frac_bf16": round(alg / peaks["bf16_tflops_sustained"], 4)}
+        else:
+            out[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
+                         "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1),
+                         "frac_bf16_incl_recompute": round(alg * 10 / 8 / peaks["bf16_tflops_sustained"], 4)}
         del ws
     sh.free()
     return out

@@ -120,10 +120,11 @@ int tpmlp_shard_get_transposed(const tpmlp_shards* shards, int i, const void** A
 /* Releases everything the handle owns (synchronises the device first). NULL is a no-op. */
 void tpmlp_shards_free(tpmlp_shards* shards);
 
-/* Bytes of workspace that tpmlp_forward (backward = 0) or tpmlp_backward
- * (backward = 1) needs for T tokens, these shards and this mode; 0 on bad
- * arguments. The workspace holds the shards' H_i (and, in FAITHFUL mode, the
- * partials), so it grows with T * F and, for FAITHFUL, with n * T * D. */
+/* Bytes of workspace that tpmlp_forward / tpmlp_forward_save (backward = 0),
+ * tpmlp_backward (backward = 1) or tpmlp_backward_saved (backward = 2) needs
+ * for T tokens, these shards and this mode; 0 on bad arguments. The workspace
+ * holds the shards' H_i (and, in FAITHFUL mode, the partials), so it grows
+ * with T * F and, for FAITHFUL, with n * T * D. */
 size_t tpmlp_workspace_bytes(int64_t T, const tpmlp_shards* shards, tpmlp_mode mode, int backward);
 
 /* tp_mlp(X, shards): Y = sum_i GeLU(X A_i) B_i ([P4] "What to implement",
@@ -208,6 +209,24 @@ int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shar
  * array needs to start at zero, and it keeps the last call's contents. */
 int tpmlp_forward_noalloc(const void* X, int64_t T, const tpmlp_shards* shards, void* Y, tpmlp_mode mode,
                           tpmlp_stream_t stream);
+
+/* Training-mode forward: the same Y as tpmlp_forward, and in addition the
+ * shards' pre-activations P_i = X A_i (fp32), which tpmlp_backward_saved
+ * uses instead of recomputing them. ai-hpc.org "LLM Lab Notes 06" §4 notes
+ * that the backward costs about the sum of the forward passes; keeping P
+ * removes the recompute (2*T*D*F of the backward's 10*T*D*F FLOP) at the
+ * price of T*F*4 bytes.
+ *   P     device [n][T][F/n] fp32, written (shard i's block at P + i*T*(F/n)).
+ *   other arguments as for tpmlp_forward (same workspace size). */
+int tpmlp_forward_save(const void* X, int64_t T, const tpmlp_shards* shards, void* Y, void* P, tpmlp_mode mode,
+                       void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* tpmlp_backward with the P written by tpmlp_forward_save for the same X and
+ * shards: the same dX, dA_i, dB_i without recomputing P (P is only read).
+ *   workspace  at least tpmlp_workspace_bytes(T, shards, mode, 2) bytes. */
+int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T, const tpmlp_shards* shards,
+                         void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
+                         size_t workspace_bytes, tpmlp_stream_t stream);
 
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit

@@ -60,6 +60,8 @@ SIGNATURES = {
     "tpmlp_selftest_wait_timeout": (_I, [_I, _P]),
     "tpmlp_forward_noalloc": (_I, [_P, _I64, _P, _P, _I, _P]),
     "tpmlp_selftest_gemm_withheld_fill": (_I, [_P, _I64, _P, _P, _I, _I, _P]),
+    "tpmlp_forward_save": (_I, [_P, _I64, _P, _P, _P, _I, _P, _SZ, _P]),
+    "tpmlp_backward_saved": (_I, [_P, _P, _P, _I64, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -198,7 +200,8 @@ def tpmlp_shard(A: torch.Tensor, B: torch.Tensor, n: int, stream=None) -> Shards
     return Shards(h.value, D, F, n, A.dtype)
 
 
-def tpmlp_workspace_bytes(T: int, shards: Shards, mode="faithful", backward: bool = False) -> int:
+def tpmlp_workspace_bytes(T: int, shards: Shards, mode="faithful", backward: int = 0) -> int:
+    """backward: 0 = forward, 1 = tpmlp_backward, 2 = tpmlp_backward_saved."""
     return int(lib().tpmlp_workspace_bytes(T, shards.handle, _mode(mode), int(backward)))
 
 
@@ -257,8 +260,11 @@ def tpmlp_fused_sum(H: torch.Tensor, shards: Shards, Y: Optional[torch.Tensor] =
 def tpmlp_backward(X: torch.Tensor, dY: torch.Tensor, shards: Shards, mode="faithful",
                    dX: Optional[torch.Tensor] = None, dA: Optional[Sequence[torch.Tensor]] = None,
                    dB: Optional[Sequence[torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
-                   stream=None):
-    """Gradients of sum(Y * dY): (dX [T, D], [dA_i [D, F/n]], [dB_i [F/n, D]]), all fp32."""
+                   stream=None, P: Optional[torch.Tensor] = None):
+    """Gradients of sum(Y * dY): (dX [T, D], [dA_i [D, F/n]], [dB_i [F/n, D]]), all fp32.
+
+    With P (from tpmlp_forward_save) this is tpmlp_backward_saved, which skips
+    recomputing the pre-activations."""
     T, D, Fs, n = X.shape[0], shards.D, shards.Fs, shards.n
     dev = X.device
     dX = torch.empty((T, D), dtype=torch.float32, device=dev) if dX is None else dX
@@ -266,12 +272,37 @@ def tpmlp_backward(X: torch.Tensor, dY: torch.Tensor, shards: Shards, mode="fait
     dB = [torch.empty((Fs, D), dtype=torch.float32, device=dev) for _ in range(n)] if dB is None else list(dB)
     pa = (ctypes.c_void_p * n)(*[_dev(t, "dA_i") for t in dA])
     pb = (ctypes.c_void_p * n)(*[_dev(t, "dB_i") for t in dB])
-    nb = tpmlp_workspace_bytes(T, shards, mode, True)
+    nb = tpmlp_workspace_bytes(T, shards, mode, 2 if P is not None else 1)
     ws = _workspace(nb, workspace)
-    _check(lib().tpmlp_backward(_dev(X, "X"), _dev(dY, "dY"), T, shards.handle, _dev(dX, "dX"), pa, pb,
-                                _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
-           "tpmlp_backward")
+    if P is None:
+        _check(lib().tpmlp_backward(_dev(X, "X"), _dev(dY, "dY"), T, shards.handle, _dev(dX, "dX"), pa, pb,
+                                    _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+               "tpmlp_backward")
+    else:
+        _check(lib().tpmlp_backward_saved(_dev(X, "X"), _dev(dY, "dY"), _dev(P, "P"), T, shards.handle,
+                                          _dev(dX, "dX"), pa, pb, _mode(mode), ws.data_ptr(),
+                                          ws.numel() * ws.element_size(), _stream(stream)),
+               "tpmlp_backward_saved")
     return dX, dA, dB
+
+
+def tpmlp_backward_saved(X: torch.Tensor, dY: torch.Tensor, P: torch.Tensor, shards: Shards, mode="faithful", **kw):
+    """tpmlp_backward with the pre-activations P saved by tpmlp_forward_save."""
+    return tpmlp_backward(X, dY, shards, mode, P=P, **kw)
+
+
+def tpmlp_forward_save(X: torch.Tensor, shards: Shards, mode="faithful", Y: Optional[torch.Tensor] = None,
+                       P: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Training-mode forward: (Y [T, D] fp32, P [n, T, F/n] fp32 pre-activations)."""
+    T = X.shape[0]
+    Y = torch.empty((T, shards.D), dtype=torch.float32, device=X.device) if Y is None else Y
+    P = torch.empty((shards.n, T, shards.Fs), dtype=torch.float32, device=X.device) if P is None else P
+    nb = tpmlp_workspace_bytes(T, shards, mode, 0)
+    ws = _workspace(nb, workspace)
+    _check(lib().tpmlp_forward_save(_dev(X, "X"), T, shards.handle, _dev(Y, "Y"), _dev(P, "P"), _mode(mode),
+                                    ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpmlp_forward_save")
+    return Y, P
 
 
 def tpmlp_forward_noalloc(X: torch.Tensor, shards: Shards, Y: torch.Tensor, mode="faithful", stream=None) -> torch.Tensor:

@@ -107,8 +107,11 @@ WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int ba
     w.H = take(n * t * Fs * es);
     if (mode == TPMLP_FAITHFUL) w.Yp = take(n * t * D * 4);
   } else {
-    w.P = take(n * t * Fs * 4);
-    if (sh->dt == TPMLP_F32) w.dH = take(n * t * Fs * 4);  // bf16 applies the activation in the dH epilogue
+    if (backward == 1) w.P = take(n * t * Fs * 4);  // backward == 2: the caller's saved P
+    if (sh->dt == TPMLP_F32) {  // bf16 applies the activation in the dH epilogue instead
+      w.H = take(n * t * Fs * 4);
+      w.dH = take(n * t * Fs * 4);
+    }
     if (sh->dt == TPMLP_BF16) {
       w.Xt = take(D * tp * 2);
       w.dYt = take(D * tp * 2);
@@ -144,10 +147,11 @@ int out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t pitc
 
 // ----------------------------------------------------------- step launchers
 
-// H_i = GeLU(X A_i) for every shard. `inject` and `wait_ns` are the test
-// hooks of tpmlp_selftest_gemm_withheld_fill (0 = off / the default limit).
+// H_i = GeLU(X A_i) for every shard, and with P_out also P_i = X A_i (fp32,
+// [n][T][Fs]). `inject` and `wait_ns` are the test hooks of
+// tpmlp_selftest_gemm_withheld_fill (0 = off / the default limit).
 int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaStream_t s, int inject = 0,
-               uint64_t wait_ns = 0) {
+               uint64_t wait_ns = 0, void* P_out = nullptr) {
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     CUtensorMap mx;
@@ -159,12 +163,13 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
       g.map_a[i] = &mx;
       g.map_b[i] = &sh->map_At[i];
       g.out[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
+      if (P_out) g.out2[i] = static_cast<float*>(P_out) + static_cast<size_t>(i) * T * Fs;
     }
     g.ldo = Fs;
     g.M = static_cast<int>(T);
     g.N = static_cast<int>(Fs);
     g.K = static_cast<int>(D);
-    g.epi = kEpiGeluBf16;
+    g.epi = P_out ? kEpiGeluSaveP : kEpiGeluBf16;
     g.shared = kSharedA;  // X feeds every shard
     g.group_m = 16;       // bands of 16 M blocks: fewest DRAM re-reads of the shards' A_i^T measured
     g.stream_out = 1;
@@ -173,11 +178,12 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
     return TPMLP_OK;
   }
   for (int i = 0; i < sh->n; ++i) {
-    SimtGemm g{static_cast<const float*>(X), D, 1, static_cast<const float*>(sh->desc[i].A), Fs, 1,
-               static_cast<float*>(H) + static_cast<size_t>(i) * T * Fs, Fs, static_cast<int>(T),
-               static_cast<int>(Fs), static_cast<int>(D), kSimtGelu};
+    float* Ci = static_cast<float*>(P_out ? P_out : H) + static_cast<size_t>(i) * T * Fs;
+    SimtGemm g{static_cast<const float*>(X), D, 1, static_cast<const float*>(sh->desc[i].A), Fs, 1, Ci, Fs,
+               static_cast<int>(T), static_cast<int>(Fs), static_cast<int>(D), P_out ? kSimtStore : kSimtGelu};
     TRY_CUDA(launch_simt_gemm(g, s));
   }
+  if (P_out) TRY_CUDA(launch_gelu(P_out, H, static_cast<int64_t>(sh->n) * T * Fs, 0, s));  // H = GeLU(P)
   return TPMLP_OK;
 }
 
@@ -216,6 +222,30 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
                static_cast<int>(Fs), (chain && i > 0) ? kSimtAccumulate : kSimtStore};
     TRY_CUDA(launch_simt_gemm(g, s));
   }
+  return TPMLP_OK;
+}
+
+int check_common(const tpmlp_shards* sh, int64_t T);
+
+// tpmlp_forward, and with P also tpmlp_forward_save.
+int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void* P, tpmlp_mode mode, void* ws,
+                 size_t ws_bytes, cudaStream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if (!X || !Y || !ws) return fail(TPMLP_ERR_ARG, "X, Y and workspace must not be NULL");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "X, Y and workspace must be 16-byte aligned");
+  const WsPlan w = plan_workspace(T, sh, mode, 0);
+  if (ws_bytes < w.total)
+    return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  void* H = at<char>(ws, w.H);
+  if ((rc = run_hidden(X, T, sh, H, stream, 0, 0, P))) return rc;
+  if (mode == TPMLP_FUSED) return run_second(H, T, sh, Y, 1, stream);
+  float* Yp = at<float>(ws, w.Yp);
+  if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
+  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
   return TPMLP_OK;
 }
 
@@ -383,7 +413,7 @@ void tpmlp_shards_free(tpmlp_shards* sh) {
 }
 
 size_t tpmlp_workspace_bytes(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
-  if (!sh || T < 1 || (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED)) return 0;
+  if (!sh || T < 1 || (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) || backward < 0 || backward > 2) return 0;
   return plan_workspace(T, sh, mode, backward).total;
 }
 
@@ -428,27 +458,38 @@ int tpmlp_fused_sum(const void* H, int64_t T, const tpmlp_shards* sh, void* Y, t
 
 int tpmlp_forward(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, tpmlp_mode mode, void* ws,
                   size_t ws_bytes, tpmlp_stream_t stream) {
-  int rc = check_common(sh, T);
-  if (rc) return rc;
-  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
-  if (!X || !Y || !ws) return fail(TPMLP_ERR_ARG, "X, Y and workspace must not be NULL");
-  if (!aligned16(X) || !aligned16(Y) || !aligned16(ws))
-    return fail(TPMLP_ERR_ALIGN, "X, Y and workspace must be 16-byte aligned");
-  const WsPlan w = plan_workspace(T, sh, mode, 0);
-  if (ws_bytes < w.total)
-    return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
-  if ((rc = check_handle_device(sh))) return rc;
-  void* H = at<char>(ws, w.H);
-  if ((rc = run_hidden(X, T, sh, H, stream))) return rc;
-  if (mode == TPMLP_FUSED) return run_second(H, T, sh, Y, 1, stream);
-  float* Yp = at<float>(ws, w.Yp);
-  if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
-  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
-  return TPMLP_OK;
+  return forward_impl(X, T, sh, Y, nullptr, mode, ws, ws_bytes, stream);
 }
+
+int tpmlp_forward_save(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void* P, tpmlp_mode mode, void* ws,
+                       size_t ws_bytes, tpmlp_stream_t stream) {
+  if (!P) return fail(TPMLP_ERR_ARG, "P must not be NULL");
+  if (!aligned16(P)) return fail(TPMLP_ERR_ALIGN, "P must be 16-byte aligned");
+  return forward_impl(X, T, sh, Y, P, mode, ws, ws_bytes, stream);
+}
+
+static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
+                         void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
 
 int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards* sh, void* dX, void* const* dA,
                    void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
+  return backward_impl(X, dY, nullptr, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream);
+}
+
+int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T, const tpmlp_shards* sh, void* dX,
+                         void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
+                         tpmlp_stream_t stream) {
+  if (!P) return fail(TPMLP_ERR_ARG, "P must not be NULL");
+  if (!aligned16(P)) return fail(TPMLP_ERR_ALIGN, "P must be 16-byte aligned");
+  return backward_impl(X, dY, P, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream);
+}
+
+// tpmlp_backward (P_saved == NULL: P_i = X A_i is recomputed into the
+// workspace) and tpmlp_backward_saved (P_saved is the forward's P, only read).
+static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
+                         void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
   int rc = check_common(sh, T);
   if (rc) return rc;
   if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
@@ -459,13 +500,14 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
     if (!dA[i] || !dB[i]) return fail(TPMLP_ERR_ARG, "dA[%d] or dB[%d] is NULL", i, i);
     if (!aligned16(dA[i]) || !aligned16(dB[i])) return fail(TPMLP_ERR_ALIGN, "dA[%d], dB[%d] must be 16-byte aligned", i, i);
   }
-  const WsPlan w = plan_workspace(T, sh, mode, 1);
+  const WsPlan w = plan_workspace(T, sh, mode, P_saved ? 2 : 1);
   if (ws_bytes < w.total)
     return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
   if ((rc = check_handle_device(sh))) return rc;
   const int n = sh->n;
   const int64_t D = sh->D, Fs = sh->Fs;
-  float* P = at<float>(ws, w.P);
+  // P_i = X A_i: the caller's (only read) or recomputed here into the workspace.
+  float* P = P_saved ? const_cast<float*>(static_cast<const float*>(P_saved)) : at<float>(ws, w.P);
   float* dH = at<float>(ws, w.dH);
   float* dXp = mode == TPMLP_FAITHFUL ? at<float>(ws, w.dXp) : nullptr;
   cudaStream_t s = stream;
@@ -473,21 +515,22 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   if (sh->dt == TPMLP_F32) {
     const float* x = static_cast<const float*>(X);
     const float* dy = static_cast<const float*>(dY);
+    float* H = at<float>(ws, w.H);
     for (int i = 0; i < n; ++i) {
       const float* Ai = static_cast<const float*>(sh->desc[i].A);
       const float* Bi = static_cast<const float*>(sh->desc[i].B);
       float* Pi = P + static_cast<size_t>(i) * T * Fs;
       float* dHi = dH + static_cast<size_t>(i) * T * Fs;
       const int t = static_cast<int>(T), d = static_cast<int>(D), fs = static_cast<int>(Fs);
-      // P_i = X A_i ; dH_i = dY B_i^T
-      TRY_CUDA(launch_simt_gemm(SimtGemm{x, D, 1, Ai, Fs, 1, Pi, Fs, t, fs, d, kSimtStore}, s));
+      // P_i = X A_i (unless saved) ; dH_i = dY B_i^T
+      if (!P_saved) TRY_CUDA(launch_simt_gemm(SimtGemm{x, D, 1, Ai, Fs, 1, Pi, Fs, t, fs, d, kSimtStore}, s));
       TRY_CUDA(launch_simt_gemm(SimtGemm{dy, D, 1, Bi, 1, D, dHi, Fs, t, fs, d, kSimtStore}, s));
     }
-    // P <- H = GeLU(P), dH <- dP = dH * GeLU'(P)
-    TRY_CUDA(launch_bwd_act_f32(P, dH, static_cast<int64_t>(n) * T * Fs, s));
+    // H = GeLU(P), dH <- dP = dH * GeLU'(P)
+    TRY_CUDA(launch_bwd_act_f32(P, H, dH, static_cast<int64_t>(n) * T * Fs, s));
     for (int i = 0; i < n; ++i) {
       const float* Ai = static_cast<const float*>(sh->desc[i].A);
-      const float* Hi = P + static_cast<size_t>(i) * T * Fs;
+      const float* Hi = H + static_cast<size_t>(i) * T * Fs;
       const float* dPi = dH + static_cast<size_t>(i) * T * Fs;
       const int t = static_cast<int>(T), d = static_cast<int>(D), fs = static_cast<int>(Fs);
       // dB_i = H_i^T dY ; dA_i = X^T dP_i ; dX_i = dP_i A_i^T
@@ -543,8 +586,8 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
   g.epi = kEpiF32;
   g.shared = kSharedA;  // X (then dY) feeds every shard
   g.group_m = 16;
-  g.stream_out = 0;     // P and dH are read back right away by the activation step
-  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  g.stream_out = 0;     // P is read back right away by the dH product's epilogue
+  if (!P_saved) TRY_CUDA(launch_tc_gemm(g, wl, s));
   // dH_i = dY B_i^T with the activation step in its epilogue: dP_i = dH_i *
   // GeLU'(P_i) and the transposes H_i^T = GeLU(P_i)^T and dP_i^T, all bf16.
   for (int i = 0; i < n; ++i) {

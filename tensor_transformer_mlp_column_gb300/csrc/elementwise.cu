@@ -154,14 +154,15 @@ __global__ void __launch_bounds__(256) transpose_u16_kernel(const uint16_t* __re
 
 // ------------------------------------------------------------------ backward activation (fp32 path)
 
-// In place: P <- GeLU(P), dH <- dH * GeLU'(P). (The bf16 path applies this
-// step in the epilogue of its dH product instead.)
-__global__ void bwd_act_f32_kernel(float* __restrict__ P, float* __restrict__ dH, int64_t count) {
+// H <- GeLU(P) and, in place, dH <- dH * GeLU'(P); P is only read. (The bf16
+// path applies this step in the epilogue of its dH product instead.)
+__global__ void bwd_act_f32_kernel(const float* __restrict__ P, float* __restrict__ H, float* __restrict__ dH,
+                                   int64_t count) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
     float g, dg;
     gelu_and_grad_fast(P[j], g, dg);
-    P[j] = g;
+    H[j] = g;
     dH[j] = dH[j] * dg;
   }
 }
@@ -216,9 +217,9 @@ cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_act_f32(float* P, float* dH, int64_t count, cudaStream_t s) {
+cudaError_t launch_bwd_act_f32(const float* P, float* H, float* dH, int64_t count, cudaStream_t s) {
   if (count <= 0) return cudaSuccess;
-  bwd_act_f32_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(P, dH, count);
+  bwd_act_f32_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(P, H, dH, count);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ struct KParams {
   CUtensorMap map_a[kMaxGroups];
   CUtensorMap map_b[kMaxGroups];
   void* out[kMaxGroups];
+  void* out2[kMaxGroups];           // kEpiGeluSaveP: fp32 pre-activation per group (row pitch ldo)
   CUtensorMap map_out[kMaxGroups];  // kEpiF32Tma: fp32 output per group, 32 x 32 boxes, 128-byte swizzle
   const void* aux_p[kMaxGroups];    // kEpiBwdAct: P per group (fp32, row pitch ldo)
   void* aux_ht[kMaxGroups];         // kEpiBwdAct: H^T per group (bf16, row pitch ldt)
@@ -101,8 +102,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // (group g). The caller has checked m < M and n0 < N; N is a multiple of 8.
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
-  if constexpr (EPI == kEpiGeluBf16) {
-    // H = GeLU(acc), bf16, row-major.
+  if constexpr (EPI == kEpiGeluBf16 || EPI == kEpiGeluSaveP) {
+    // H = GeLU(acc), bf16, row-major (and, saving P, acc itself in fp32).
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -113,6 +114,13 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
         w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
         w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
         store16(out + 8 * j, w, p.stream_out);
+        if constexpr (EPI == kEpiGeluSaveP) {
+          float* P = static_cast<float*>(p.out2[g]) + m * p.ldo + n0 + 8 * j;
+          store16(P, make_uint4(__float_as_uint(v[8 * j]), __float_as_uint(v[8 * j + 1]), __float_as_uint(v[8 * j + 2]),
+                                __float_as_uint(v[8 * j + 3])), false);
+          store16(P + 4, make_uint4(__float_as_uint(v[8 * j + 4]), __float_as_uint(v[8 * j + 5]),
+                                    __float_as_uint(v[8 * j + 6]), __float_as_uint(v[8 * j + 7])), false);
+        }
       }
     }
   } else if constexpr (EPI == kEpiF32) {

@@ -239,6 +239,8 @@ cudaError_t launch_single_epi(const KParams& kp, int epi, cudaStream_t s) {
       return launch_single<BN, kEpiF32>(kp, s);
     case kEpiBwdAct:
       return launch_single<BN, kEpiBwdAct>(kp, s);
+    case kEpiGeluSaveP:
+      return launch_single<BN, kEpiGeluSaveP>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }
@@ -359,6 +361,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.map_a[i] = *g.map_a[i];
     kp.map_b[i] = *g.map_b[i];
     kp.out[i] = g.out[i];
+    kp.out2[i] = g.out2[i];
     kp.aux_p[i] = g.aux_p[i];
     kp.aux_ht[i] = g.aux_ht[i];
     kp.aux_dpt[i] = g.aux_dpt[i];

@@ -25,6 +25,7 @@ enum TcEpilogue : int {
   kEpiF32 = 1,       // out fp32 = acc
   kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), aux_ht = GeLU(P)^T, aux_dpt = out^T (P from aux_p)
   kEpiF32Tma = 3,    // out fp32 = acc through TMA stores (chosen by the launcher when map_out is given)
+  kEpiGeluSaveP = 4, // out bf16 = GeLU(acc) and out2 fp32 = acc (the pre-activation), same row stride
 };
 
 enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
@@ -39,6 +40,7 @@ struct TcGemm {
   const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
   const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
+  void* out2[kMaxGroups];                // kEpiGeluSaveP only: fp32 pre-activation, row stride ldo
   const CUtensorMap* map_out[kMaxGroups];  // optional fp32 output maps (make_output_map_f32) for TMA stores
   const void* aux_p[kMaxGroups];         // kEpiBwdAct only: P (fp32, row stride ldo)
   void* aux_ht[kMaxGroups];              // kEpiBwdAct only: H^T (bf16, row stride ldt)
@@ -105,8 +107,8 @@ cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_t
 cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int64_t ldi, void* out, int64_t ldo,
                                  cudaStream_t s);
 
-// fp32 path: in place, P <- GeLU(P) and dH <- dH * GeLU'(P), count elements.
-cudaError_t launch_bwd_act_f32(float* P, float* dH, int64_t count, cudaStream_t s);
+// fp32 path: H <- GeLU(P) and, in place, dH <- dH * GeLU'(P); count elements.
+cudaError_t launch_bwd_act_f32(const float* P, float* H, float* dH, int64_t count, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 

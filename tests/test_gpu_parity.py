@@ -315,3 +315,38 @@ def test_bounded_wait_reports_timeout_and_context_survives(tp):
     tp.tpmlp_check_status()  # cleared
     x = torch.randn(1000, device="cuda")
     np.testing.assert_allclose(f64(tp.tpmlp_gelu(x)), oracle.gelu(f64(x)), rtol=2e-6, atol=1e-7)
+
+
+# ----------------------------------------------------------------- saved pre-activations (training mode)
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", SMALL[:3] + [("pair_tiles", 1000, 512, 4096, 4)], ids=lambda c: c[0])
+def test_forward_save_and_backward_saved(tp, case, dtype):
+    w = small_workload(*case, dtype)
+    inp = make_inputs(w, seed=51, with_dy=True)
+    ref = {k: f64(v) for k, v in inp.items()}
+    shards_ref = oracle.shard_mlp(ref["A"], ref["B"], w.N)
+    dX_ref, dA_ref, dB_ref = oracle.tp_mlp_backward(ref["X"], ref["dY"], shards_ref)
+    d = on_gpu(inp)
+    sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
+    for mode in ("faithful", "fused"):
+        Y, P = tp.tpmlp_forward_save(d["X"], sh, mode)
+        # the same output as the inference forward, bit for bit
+        assert torch.equal(Y, tp.tpmlp_forward(d["X"], sh, mode))
+        # P_i = X A_i: exact bf16/fp32 products summed in fp32
+        for i, (A_i, _) in enumerate(shards_ref):
+            P_ref = ref["X"] @ A_i
+            assert np.max(np.abs(f64(P[i]) - P_ref)) <= 1e-5 * np.max(np.abs(P_ref)), f"P_{i}"
+        P_before = P.clone()
+        g_re = tp.tpmlp_backward(d["X"], d["dY"], sh, mode)
+        g_sv = tp.tpmlp_backward_saved(d["X"], d["dY"], P, sh, mode)
+        assert torch.equal(P, P_before)  # the saved P is only read
+        # the same kernels on the same P: identical gradients
+        assert torch.equal(g_re[0], g_sv[0])
+        for i in range(w.N):
+            assert torch.equal(g_re[1][i], g_sv[1][i]) and torch.equal(g_re[2][i], g_sv[2][i])
+        check(f64(g_sv[0]), dX_ref, dtype, f"dX {mode}")
+        for i in range(w.N):
+            check(f64(g_sv[1][i]), dA_ref[i], dtype, f"dA_{i} {mode}")
+            check(f64(g_sv[2][i]), dB_ref[i], dtype, f"dB_{i} {mode}")
+    tp.tpmlp_check_status()
