@@ -17,4 +17,11 @@ from .tpmlp_oracle import (  # noqa: F401
     tp_mlp_backward_dx_rows,
     grad_A_cols,
     grad_B_rows,
+    LN_EPS,
+    layer_norm,
+    block_mlp,
+    block_mlp_rows,
+    layer_norm_backward,
+    block_mlp_backward,
+    block_mlp_backward_dx_rows,
 )

@@ -181,3 +181,76 @@ def grad_B_rows(X, dY, A_i, rows):
     """Rows `rows` of dB_i = H_i^T dY: row j needs column j of H_i = GeLU(X A_i)."""
     H = gelu(_f64(X) @ _f64(A_i)[:, rows])
     return H.T @ _f64(dY)
+
+
+# ---------------------------------------------------------------------------
+# The FFN half of a tensor-parallel transformer block (ai-hpc.org "LLM Lab
+# Notes 06", §2 steps 5-7): normalise the block input, run the column/row
+# split MLP, and add the residual. The block there calls
+# F.layer_norm(x, (hidden,)) with no weight, bias or eps, so the normalisation
+# has no affine parameters and PyTorch's default eps.
+# ---------------------------------------------------------------------------
+
+LN_EPS = 1e-5
+
+
+def layer_norm(x, eps: float = LN_EPS):
+    """Row-wise (x - mean) / sqrt(var + eps), var the biased variance of the row."""
+    x = _f64(x)
+    mu = x.mean(axis=-1, keepdims=True)
+    var = ((x - mu) ** 2).mean(axis=-1, keepdims=True)
+    return (x - mu) / np.sqrt(var + eps)
+
+
+def block_mlp(x, shards, eps: float = LN_EPS):
+    """out = x + sum_i GeLU(LN(x) A_i) B_i: the residual is added to the
+    all-reduced sum (ai-hpc.org §2: local_out = AllReduce(mid @ w2); out = x + local_out)."""
+    return _f64(x) + tp_mlp(layer_norm(x, eps), shards)
+
+
+def block_mlp_rows(x, shards, rows, eps: float = LN_EPS):
+    """Rows `rows` of block_mlp: every step is row-wise in x."""
+    return block_mlp(_f64(x)[rows], shards, eps)
+
+
+def layer_norm_backward(x, g, eps: float = LN_EPS):
+    """The gradient of sum(layer_norm(x) * g) with respect to x, row by row.
+
+    The backward of the block (ai-hpc.org "LLM Lab Notes 06", §2 step 8) passes
+    through the normalisation. For one row with y = (x - mu) r,
+    r = (var + eps)^(-1/2), differentiating mu and var gives the Jacobian
+        dy_j/dx_k = r (delta_jk - 1/D - y_j y_k / D),
+    which is symmetric; the gradient is that matrix applied to g, built here
+    for each row as written.
+    """
+    x = _f64(x)
+    g = _f64(g)
+    D = x.shape[-1]
+    y = layer_norm(x, eps)
+    mu = x.mean(axis=-1, keepdims=True)
+    r = 1.0 / np.sqrt(((x - mu) ** 2).mean(axis=-1, keepdims=True) + eps)
+    out = np.empty_like(x)
+    eye = np.eye(D)
+    for t in range(x.shape[0]):
+        J = r[t, 0] * (eye - 1.0 / D - np.outer(y[t], y[t]) / D)
+        out[t] = J @ g[t]
+    return out
+
+
+def block_mlp_backward(x, dout, shards, eps: float = LN_EPS):
+    """Gradients of L = sum(block_mlp(x) * dout): (dx, [dA_i], [dB_i]).
+
+    The residual passes dout to x unchanged; the MLP sees the normalised input
+    and the same upstream gradient, and its input gradient goes back through
+    the normalisation.
+    """
+    x = _f64(x)
+    dout = _f64(dout)
+    dxn, dA, dB = tp_mlp_backward(layer_norm(x, eps), dout, shards)
+    return dout + layer_norm_backward(x, dxn, eps), dA, dB
+
+
+def block_mlp_backward_dx_rows(x, dout, shards, rows, eps: float = LN_EPS):
+    """Rows `rows` of block_mlp_backward's dx: each row needs only its own x and dout rows."""
+    dx, _, _ = block_mlp_backward(_f64(x)[rows], _f64(dout)[rows], shards, eps)
+    return dx

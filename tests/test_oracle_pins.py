@@ -302,3 +302,106 @@ def test_gradient_pins_catch_a_wrong_gelu_grad():
     h = 1e-5
     fd = (oracle.gelu(x + h) - oracle.gelu(x - h)) / (2 * h)
     assert np.max(np.abs(bad(x) - fd)) > 1e-2
+
+
+# ---------------------------------------------------------------- block tail: layer norm + residual
+
+def test_layer_norm_against_torch_library_routine():
+    import torch
+
+    rng = np.random.default_rng(21)
+    x = rng.normal(size=(7, 33)) * 3 + 1.5
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (33,), eps=1e-5).numpy()
+    np.testing.assert_allclose(oracle.layer_norm(x), ref, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_norm_closed_forms():
+    rng = np.random.default_rng(22)
+    x = rng.normal(size=(5, 64)) * 2 - 3
+    y = oracle.layer_norm(x)
+    var = x.var(axis=1)
+    np.testing.assert_allclose(y.mean(axis=1), 0, atol=1e-13)
+    np.testing.assert_allclose(y.var(axis=1), var / (var + oracle.LN_EPS), rtol=1e-12)
+    # without eps the map is invariant to a per-row positive scale and shift
+    np.testing.assert_allclose(oracle.layer_norm(4.0 * x + 7.0, eps=0.0), oracle.layer_norm(x, eps=0.0), atol=1e-12)
+    # a constant row normalises to zero
+    assert np.all(oracle.layer_norm(np.full((2, 8), 3.25)) == 0.0)
+    # two elements (a, b): (a - m) / sqrt(((a - b) / 2)^2 + eps)
+    a, b = 1.0, 2.0
+    h = (b - a) / 2
+    np.testing.assert_allclose(oracle.layer_norm([[a, b]]), [[-h / math.sqrt(h * h + 1e-5), h / math.sqrt(h * h + 1e-5)]])
+
+
+def test_block_mlp_residual_and_composition():
+    rng = np.random.default_rng(23)
+    T, D, F = 6, 8, 24
+    x, A, B = rng.normal(size=(T, D)), rng.normal(size=(D, F)), rng.normal(size=(F, D))
+    # with B = 0 the MLP contributes nothing and the block is the identity
+    assert np.array_equal(oracle.block_mlp(x, oracle.shard_mlp(A, np.zeros((F, D)), 3)), x)
+    # otherwise it is x + the unsplit MLP of the normalised input, for every divisor
+    ref = x + oracle.mlp(oracle.layer_norm(x), A, B)
+    for n in [1, 2, 3, 4, 6]:
+        np.testing.assert_allclose(oracle.block_mlp(x, oracle.shard_mlp(A, B, n)), ref, rtol=1e-13, atol=1e-13)
+    rows = [0, 4]
+    np.testing.assert_allclose(oracle.block_mlp_rows(x, oracle.shard_mlp(A, B, 2), rows), ref[rows], rtol=1e-13)
+
+
+def test_layer_norm_backward_against_autograd_and_differences():
+    import torch
+
+    rng = np.random.default_rng(24)
+    x, g = rng.normal(size=(4, 12)) * 2 + 0.5, rng.normal(size=(4, 12))
+    xt = torch.from_numpy(x).requires_grad_(True)
+    (torch.nn.functional.layer_norm(xt, (12,), eps=1e-5) * torch.from_numpy(g)).sum().backward()
+    np.testing.assert_allclose(oracle.layer_norm_backward(x, g), xt.grad.numpy(), rtol=1e-11, atol=1e-12)
+    # central differences of sum(LN(x) * g)
+    h = 1e-6
+    fd = np.zeros_like(x)
+    for t in range(x.shape[0]):
+        for k in range(x.shape[1]):
+            e = np.zeros_like(x)
+            e[t, k] = h
+            fd[t, k] = ((oracle.layer_norm(x + e) - oracle.layer_norm(x - e)) * g).sum() / (2 * h)
+    np.testing.assert_allclose(oracle.layer_norm_backward(x, g), fd, rtol=1e-6, atol=1e-7)
+    # the gradient is orthogonal to the constant direction and to y (shift and, without eps, scale invariance)
+    dx = oracle.layer_norm_backward(x, g, eps=0.0)
+    np.testing.assert_allclose(dx.sum(axis=1), 0, atol=1e-11)
+    np.testing.assert_allclose((dx * x).sum(axis=1), 0, atol=1e-10)
+
+
+def test_block_backward_against_autograd():
+    import torch
+
+    rng = np.random.default_rng(25)
+    T, D, F, n = 5, 8, 24, 3
+    x, dout = rng.normal(size=(T, D)), rng.normal(size=(T, D))
+    A, B = rng.normal(size=(D, F)) * 0.5, rng.normal(size=(F, D)) * 0.5
+    xt = torch.from_numpy(x).requires_grad_(True)
+    At = torch.from_numpy(A).requires_grad_(True)
+    Bt = torch.from_numpy(B).requires_grad_(True)
+    xn = torch.nn.functional.layer_norm(xt, (D,), eps=1e-5)
+    out = xt + torch.nn.functional.gelu(xn @ At, approximate="tanh") @ Bt
+    np.testing.assert_allclose(out.detach().numpy(), oracle.block_mlp(x, oracle.shard_mlp(A, B, n)), rtol=1e-12)
+    (out * torch.from_numpy(dout)).sum().backward()
+    dx, dA, dB = oracle.block_mlp_backward(x, dout, oracle.shard_mlp(A, B, n))
+    np.testing.assert_allclose(dx, xt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(np.concatenate(dA, axis=1), At.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(np.concatenate(dB, axis=0), Bt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    rows = [1, 3]
+    np.testing.assert_allclose(oracle.block_mlp_backward_dx_rows(x, dout, oracle.shard_mlp(A, B, n), rows), dx[rows],
+                               rtol=1e-12, atol=1e-13)
+
+
+def test_block_pins_catch_planted_mistakes():
+    rng = np.random.default_rng(26)
+    x, g = rng.normal(size=(3, 10)) + 1.0, rng.normal(size=(3, 10))
+    ref = oracle.layer_norm_backward(x, g)
+    y = oracle.layer_norm(x)
+    r = 1.0 / np.sqrt(x.var(axis=1, keepdims=True) + 1e-5)
+    # dropping the mean-of-g term, or the y-projection term, changes the gradient
+    no_mean = r * (g - y * (g * y).mean(axis=1, keepdims=True))
+    no_proj = r * (g - g.mean(axis=1, keepdims=True))
+    assert np.max(np.abs(no_mean - ref)) > 1e-2 and np.max(np.abs(no_proj - ref)) > 1e-2
+    # the unbiased variance gives a different normalisation
+    bad = (x - x.mean(axis=1, keepdims=True)) / np.sqrt(x.var(axis=1, ddof=1, keepdims=True) + 1e-5)
+    assert np.max(np.abs(bad - y)) > 1e-2
