@@ -497,6 +497,81 @@ def bench_backward(args, local_rank, peaks):
     return out
 
 
+def _time_ms(fn, dev, stream, reps: int, warm: int = 3) -> float:
+    import torch
+
+    for _ in range(warm):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for _ in range(reps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+def bench_block(args, local_rank, peaks):
+    """The block's FFN half, out = x + sum_i GeLU(LN(x) A_i) B_i: forward on
+    the large workload (T=16384, D=4096, F=16384, N=8) against the plain MLP
+    forward, the layer norm alone (2 * T * D * 2 bytes), and the block's
+    backward on the fwd+bwd workload (T=8192, D=8192, F=32768, N=8)."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import WORKLOADS, make_block_inputs
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, min(args.steps // 10, 10))
+    out = {}
+    w = WORKLOADS["large"]
+    inp = make_block_inputs(w, seed=0)
+    x = inp["x"].to(dev)
+    sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+    del inp
+    y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    xn = torch.empty_like(x)
+    fwd = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16"}
+    ms = _time_ms(lambda: tp.tpmlp_layer_norm(x, 1e-5, xn), dev, stream, 20)
+    gbs = 2.0 * w.T * w.D * 2 / (ms * 1e-3) / 1e9
+    fwd["layer_norm"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_block_workspace_bytes(w.T, sh, mode, 0), dtype=torch.uint8, device=dev)
+        ms_b = _time_ms(lambda: tp.tpmlp_block_forward(x, sh, mode, 1e-5, y, None, ws), dev, stream, reps)
+        ms_m = _time_ms(lambda: tp.tpmlp_forward(xn, sh, mode, y, ws), dev, stream, reps)
+        tf = w.fwd_flops() / (ms_b * 1e-3) / 1e12
+        fwd[mode] = {"ms": round(ms_b, 4), "TFLOP/s": round(tf, 1), "mlp_forward_ms": round(ms_m, 4),
+                     "overhead_ms": round(ms_b - ms_m, 4)}
+        del ws
+    tp.tpmlp_check_status(stream)
+    sh.free()
+    del x, y, xn
+    out["forward"] = fwd
+    if args.no_backward:
+        return out
+    w = WORKLOADS["fwd_bwd"]
+    inp = make_block_inputs(w, seed=0, with_dout=True)
+    x, dout = inp["x"].to(dev), inp["dout"].to(dev)
+    sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+    del inp
+    dx = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    dA = [torch.empty((w.D, w.Fs), dtype=torch.float32, device=dev) for _ in range(w.N)]
+    dB = [torch.empty((w.Fs, w.D), dtype=torch.float32, device=dev) for _ in range(w.N)]
+    bwd = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16"}
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_block_workspace_bytes(w.T, sh, mode, 1), dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: tp.tpmlp_block_backward(x, dout, sh, mode, 1e-5, dx, dA, dB, ws), dev, stream, reps)
+        alg = 8.0 * w.T * w.D * w.F / (ms * 1e-3) / 1e12
+        bwd[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1), "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1)}
+        del ws
+    tp.tpmlp_check_status(stream)
+    sh.free()
+    out["backward"] = bwd
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,6 +705,7 @@ def main():
         line["backward"] = bench_backward(args, local_rank, peaks)
         line["other_workloads"] = bench_small_workloads(local_rank)
         line["gelu"] = bench_gelu(local_rank, peaks)
+        line["block"] = bench_block(args, local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

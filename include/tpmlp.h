@@ -228,6 +228,56 @@ int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
                          size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * The FFN half of a transformer block ([P1] §2 steps 5-7 and 8):
+ *
+ *     out = x + sum_i GeLU(LN(x) A_i) B_i,
+ *
+ * LN the row-wise layer norm (x - mean) / sqrt(var + eps) with the biased
+ * variance and no scale or shift ([P1] calls it with the hidden size only).
+ * The residual x is added to the finished shard sum ([P1] §2: the all-reduced
+ * output, then the residual). In bf16 mode LN(x) is rounded to bf16 when it
+ * becomes the first product's operand, like every other operand.
+ * ---------------------------------------------------------------------- */
+
+/* y = LN(x) row by row. x, y device [T, D] of type dt (may be the same
+ * buffer); T >= 0, 1 <= D <= 25536 (TPMLP_ERR_SHAPE above); eps > 0 and
+ * finite. Statistics in fp32, two-pass (mean, then mean squared deviation). */
+int tpmlp_layer_norm(const void* x, int64_t T, int64_t D, tpmlp_dtype dt, float eps, void* y, tpmlp_stream_t stream);
+
+/* Workspace bytes tpmlp_block_forward (backward = 0) or tpmlp_block_backward
+ * (backward = 1) needs; 0 on bad arguments. */
+size_t tpmlp_block_workspace_bytes(int64_t T, const tpmlp_shards* shards, tpmlp_mode mode, int backward);
+
+/* out = x + sum_i GeLU(LN(x) A_i) B_i.
+ *   x    device [T, D] of the handle's dtype: the block input and residual.
+ *   eps  the layer norm's eps (PyTorch's default is 1e-5).
+ *   out  device [T, D] fp32, written; must not overlap x.
+ *   xn   device [T, D] of the handle's dtype that receives LN(x) as it entered
+ *        the first product, or NULL (then it lives in the workspace).
+ *   mode FAITHFUL: shard partials, then one pass that sums them in shard
+ *        order and adds x (out = x + (((Y_0 + Y_1) + ...))); FUSED: on-chip
+ *        shard-ordered accumulation with x added in the product's epilogue.
+ *   workspace  at least tpmlp_block_workspace_bytes(T, shards, mode, 0). */
+int tpmlp_block_forward(const void* x, int64_t T, const tpmlp_shards* shards, float eps, void* out, void* xn,
+                        tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Backward of tpmlp_block_forward for the upstream gradient dout: the
+ * gradients of L = sum(out * dout) ([P1] §2 step 8). The residual passes dout
+ * to x; the MLP's backward (as in tpmlp_backward, with X = LN(x) recomputed
+ * and dY = dout) gives dA_i, dB_i and the gradient g of LN(x), which goes back
+ * through the norm:
+ *   dx = dout + r (g - mean(g) - y mean(g * y)),  y = LN(x), r = 1/sqrt(var + eps),
+ * with g the shard-ordered sum of the partials in FAITHFUL mode (summed in the
+ * same pass) and the on-chip sum in FUSED mode.
+ *   x, dout  device [T, D] of the handle's dtype.
+ *   dx       device [T, D] fp32.
+ *   dA, dB   as for tpmlp_backward.
+ *   workspace  at least tpmlp_block_workspace_bytes(T, shards, mode, 1). */
+int tpmlp_block_backward(const void* x, const void* dout, int64_t T, const tpmlp_shards* shards, float eps, void* dx,
+                         void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
+                         size_t workspace_bytes, tpmlp_stream_t stream);
+
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit
  * of limit_ms milliseconds (1..10000). The block then stops and records

@@ -62,6 +62,11 @@ SIGNATURES = {
     "tpmlp_selftest_gemm_withheld_fill": (_I, [_P, _I64, _P, _P, _I, _I, _P]),
     "tpmlp_forward_save": (_I, [_P, _I64, _P, _P, _P, _I, _P, _SZ, _P]),
     "tpmlp_backward_saved": (_I, [_P, _P, _P, _I64, _P, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
+    "tpmlp_layer_norm": (_I, [_P, _I64, _I64, _I, ctypes.c_float, _P, _P]),
+    "tpmlp_block_workspace_bytes": (_SZ, [_I64, _P, _I, _I]),
+    "tpmlp_block_forward": (_I, [_P, _I64, _P, ctypes.c_float, _P, _P, _I, _P, _SZ, _P]),
+    "tpmlp_block_backward": (_I, [_P, _P, _I64, _P, ctypes.c_float, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P,
+                                  _SZ, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -312,6 +317,51 @@ def tpmlp_forward_noalloc(X: torch.Tensor, shards: Shards, Y: torch.Tensor, mode
     _check(lib().tpmlp_forward_noalloc(_dev(X, "X"), X.shape[0], shards.handle, _dev(Y, "Y"), _mode(mode),
                                        _stream(stream)), "tpmlp_forward_noalloc")
     return Y
+
+
+def tpmlp_layer_norm(x: torch.Tensor, eps: float = 1e-5, y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = (x - mean) / sqrt(var + eps) per row of x [T, D] (no scale or shift), same dtype as x."""
+    y = torch.empty_like(x) if y is None else y
+    T, D = x.shape
+    _check(lib().tpmlp_layer_norm(_dev(x, "x") if T else 0, T, D, _dt(x), float(eps), _dev(y, "y") if T else 0,
+                                  _stream(stream)), "tpmlp_layer_norm")
+    return y
+
+
+def tpmlp_block_workspace_bytes(T: int, shards: Shards, mode="faithful", backward: int = 0) -> int:
+    return int(lib().tpmlp_block_workspace_bytes(T, shards.handle, _mode(mode), int(backward)))
+
+
+def tpmlp_block_forward(x: torch.Tensor, shards: Shards, mode="faithful", eps: float = 1e-5,
+                        out: Optional[torch.Tensor] = None, xn: Optional[torch.Tensor] = None,
+                        workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out = x + sum_i GeLU(LN(x) A_i) B_i, fp32 [T, D]. With xn, LN(x) is also written there."""
+    T = x.shape[0]
+    out = torch.empty((T, shards.D), dtype=torch.float32, device=x.device) if out is None else out
+    ws = _workspace(tpmlp_block_workspace_bytes(T, shards, mode, 0), workspace)
+    _check(lib().tpmlp_block_forward(_dev(x, "x"), T, shards.handle, float(eps), _dev(out, "out"),
+                                     _dev(xn, "xn") if xn is not None else None, _mode(mode), ws.data_ptr(),
+                                     ws.numel() * ws.element_size(), _stream(stream)), "tpmlp_block_forward")
+    return out
+
+
+def tpmlp_block_backward(x: torch.Tensor, dout: torch.Tensor, shards: Shards, mode="faithful", eps: float = 1e-5,
+                         dx: Optional[torch.Tensor] = None, dA: Optional[Sequence[torch.Tensor]] = None,
+                         dB: Optional[Sequence[torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                         stream=None):
+    """Gradients of sum(out * dout) for tpmlp_block_forward: (dx [T, D], [dA_i], [dB_i]), all fp32."""
+    T, D, Fs, n = x.shape[0], shards.D, shards.Fs, shards.n
+    dev = x.device
+    dx = torch.empty((T, D), dtype=torch.float32, device=dev) if dx is None else dx
+    dA = [torch.empty((D, Fs), dtype=torch.float32, device=dev) for _ in range(n)] if dA is None else list(dA)
+    dB = [torch.empty((Fs, D), dtype=torch.float32, device=dev) for _ in range(n)] if dB is None else list(dB)
+    pa = (ctypes.c_void_p * n)(*[_dev(t, "dA_i") for t in dA])
+    pb = (ctypes.c_void_p * n)(*[_dev(t, "dB_i") for t in dB])
+    ws = _workspace(tpmlp_block_workspace_bytes(T, shards, mode, 1), workspace)
+    _check(lib().tpmlp_block_backward(_dev(x, "x"), _dev(dout, "dout"), T, shards.handle, float(eps), _dev(dx, "dx"),
+                                      pa, pb, _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                      _stream(stream)), "tpmlp_block_backward")
+    return dx, dA, dB
 
 
 def tpmlp_selftest_gemm_withheld_fill(X: torch.Tensor, shards: Shards, H: torch.Tensor, fill: int, limit_ms: int,

@@ -187,8 +187,10 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
   return TPMLP_OK;
 }
 
-// Y_i = H_i B_i into Yp (chain = 0), or Y = sum_i H_i B_i into Y (chain = 1).
-int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int chain, cudaStream_t s) {
+// Y_i = H_i B_i into Yp (chain = 0), or Y = sum_i H_i B_i into Y (chain = 1);
+// with chain = 1 and a residual R [T][D] of the path's type, Y = R + that sum.
+int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int chain, cudaStream_t s,
+               const void* resid = nullptr) {
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     std::vector<CUtensorMap> mh(sh->n), mo(sh->n);
@@ -212,6 +214,7 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
     g.epi = kEpiF32;
     g.group_m = 8;
     g.stream_out = 1;
+    g.resid = chain ? resid : nullptr;
     TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
     return TPMLP_OK;
   }
@@ -222,10 +225,49 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
                static_cast<int>(Fs), (chain && i > 0) ? kSimtAccumulate : kSimtStore};
     TRY_CUDA(launch_simt_gemm(g, s));
   }
+  if (chain && resid)
+    TRY_CUDA(launch_add_residual_f32(static_cast<float*>(out), static_cast<const float*>(resid), T * D, s));
   return TPMLP_OK;
 }
 
 int check_common(const tpmlp_shards* sh, int64_t T);
+
+// The block's backward tail: the input gradient of the MLP (its shard
+// partials, or their sum) goes back through the layer norm of x and picks up
+// the residual's dout: dx = dout + LN'(x)^T g.
+struct LnTail {
+  const void* x;
+  const void* dout;
+  float eps;
+  float* dx;
+};
+
+// Workspace of the block calls: LN(x), in FUSED backward the summed MLP input
+// gradient, then the MLP call's own workspace.
+struct BlockPlan {
+  size_t xn = 0, dxn = 0, inner = 0, total = 0;
+  WsPlan w;
+};
+
+BlockPlan plan_block(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  BlockPlan b;
+  const size_t td = static_cast<size_t>(T) * sh->D;
+  b.xn = 0;
+  size_t off = round_up(td * esize(sh->dt), 256);
+  if (backward && mode == TPMLP_FUSED) {
+    b.dxn = off;
+    off = round_up(off + td * 4, 256);
+  }
+  b.inner = off;
+  b.w = plan_workspace(T, sh, mode, backward ? 1 : 0);
+  b.total = off + b.w.total;
+  return b;
+}
+
+int check_eps(float eps) {
+  if (!(eps > 0.f) || !(eps < 1e30f)) return fail(TPMLP_ERR_ARG, "eps = %g must be positive and finite", double(eps));
+  return TPMLP_OK;
+}
 
 // tpmlp_forward, and with P also tpmlp_forward_save.
 int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void* P, tpmlp_mode mode, void* ws,
@@ -246,6 +288,20 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
   float* Yp = at<float>(ws, w.Yp);
   if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
   TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
+  return TPMLP_OK;
+}
+
+// The last step of the backward: dX = the shard-ordered sum of the partials
+// (FAITHFUL; FUSED already accumulated dX), or with a tail the block's dx.
+int finish_dx(const float* dXp, int n, int64_t T, const tpmlp_shards* sh, void* dX, const LnTail* tail,
+              cudaStream_t s) {
+  if (tail) {
+    const float* G = dXp ? dXp : static_cast<const float*>(dX);
+    TRY_CUDA(launch_layer_norm_bwd(G, dXp ? n : 1, tail->x, tail->dout, T, static_cast<int>(sh->D), tail->eps,
+                                   sh->dt == TPMLP_BF16, tail->dx, s));
+    return TPMLP_OK;
+  }
+  if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * sh->D, static_cast<float*>(dX), s));
   return TPMLP_OK;
 }
 
@@ -470,11 +526,11 @@ int tpmlp_forward_save(const void* X, int64_t T, const tpmlp_shards* sh, void* Y
 
 static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
-                         cudaStream_t stream);
+                         cudaStream_t stream, const LnTail* tail);
 
 int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards* sh, void* dX, void* const* dA,
                    void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
-  return backward_impl(X, dY, nullptr, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream);
+  return backward_impl(X, dY, nullptr, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream, nullptr);
 }
 
 int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T, const tpmlp_shards* sh, void* dX,
@@ -482,14 +538,18 @@ int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T
                          tpmlp_stream_t stream) {
   if (!P) return fail(TPMLP_ERR_ARG, "P must not be NULL");
   if (!aligned16(P)) return fail(TPMLP_ERR_ALIGN, "P must be 16-byte aligned");
-  return backward_impl(X, dY, P, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream);
+  return backward_impl(X, dY, P, T, sh, dX, dA, dB, mode, ws, ws_bytes, stream, nullptr);
 }
 
 // tpmlp_backward (P_saved == NULL: P_i = X A_i is recomputed into the
 // workspace) and tpmlp_backward_saved (P_saved is the forward's P, only read).
+// With a tail (tpmlp_block_backward), X is the normalised block input, and
+// the input gradient is finished by the tail kernel instead of the reduce:
+// from the partials in FAITHFUL mode, from dX (then a scratch buffer) in
+// FUSED mode.
 static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, const LnTail* tail) {
   int rc = check_common(sh, T);
   if (rc) return rc;
   if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
@@ -540,8 +600,7 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
       const int epi = (!dXp && i > 0) ? kSimtAccumulate : kSimtStore;
       TRY_CUDA(launch_simt_gemm(SimtGemm{dPi, Fs, 1, Ai, 1, Fs, C, D, t, d, fs, epi}, s));
     }
-    if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
-    return TPMLP_OK;
+    return finish_dx(dXp, n, T, sh, dX, tail, s);
   }
 
   // bf16: tensor-core products on K-major operands.
@@ -645,8 +704,80 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
   g.shared = kSharedNone;
   g.group_m = 8;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
-  if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * D, static_cast<float*>(dX), s));
+  return finish_dx(dXp, n, T, sh, dX, tail, s);
+}
+
+int tpmlp_layer_norm(const void* x, int64_t T, int64_t D, tpmlp_dtype dt, float eps, void* y, tpmlp_stream_t stream) {
+  if (T < 0 || D < 1) return fail(TPMLP_ERR_ARG, "T = %lld must be >= 0 and D = %lld >= 1",
+                                  static_cast<long long>(T), static_cast<long long>(D));
+  if (D > static_cast<int64_t>(layer_norm_max_d()))
+    return fail(TPMLP_ERR_SHAPE, "D = %lld exceeds the largest supported row of %zu", static_cast<long long>(D),
+                layer_norm_max_d());
+  if (dt != TPMLP_F32 && dt != TPMLP_BF16) return fail(TPMLP_ERR_ARG, "unknown dtype %d", int(dt));
+  int rc = check_eps(eps);
+  if (rc) return rc;
+  if (T == 0) return TPMLP_OK;
+  if (!x || !y) return fail(TPMLP_ERR_ARG, "x and y must not be NULL");
+  if (!aligned16(x) || !aligned16(y)) return fail(TPMLP_ERR_ALIGN, "x and y must be 16-byte aligned");
+  if ((rc = check_device(nullptr))) return rc;
+  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(D), eps, dt == TPMLP_BF16, y, stream));
   return TPMLP_OK;
+}
+
+size_t tpmlp_block_workspace_bytes(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  if (!sh || T < 1 || (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) || backward < 0 || backward > 1) return 0;
+  return plan_block(T, sh, mode, backward).total;
+}
+
+int tpmlp_block_forward(const void* x, int64_t T, const tpmlp_shards* sh, float eps, void* out, void* xn,
+                        tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if ((rc = check_eps(eps))) return rc;
+  if (!x || !out || !ws) return fail(TPMLP_ERR_ARG, "x, out and workspace must not be NULL");
+  if (!aligned16(x) || !aligned16(out) || !aligned16(ws) || (xn && !aligned16(xn)))
+    return fail(TPMLP_ERR_ALIGN, "x, out, xn and workspace must be 16-byte aligned");
+  if (sh->D > static_cast<int64_t>(layer_norm_max_d()))
+    return fail(TPMLP_ERR_SHAPE, "D = %lld exceeds the largest supported row of %zu",
+                static_cast<long long>(sh->D), layer_norm_max_d());
+  const BlockPlan b = plan_block(T, sh, mode, 0);
+  if (ws_bytes < b.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, b.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  const bool bf16 = sh->dt == TPMLP_BF16;
+  void* xnb = xn ? xn : at<char>(ws, b.xn);
+  void* inner = at<char>(ws, b.inner);
+  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(sh->D), eps, bf16, xnb, stream));
+  void* H = at<char>(inner, b.w.H);
+  if ((rc = run_hidden(xnb, T, sh, H, stream))) return rc;
+  if (mode == TPMLP_FUSED) return run_second(H, T, sh, out, 1, stream, x);
+  float* Yp = at<float>(inner, b.w.Yp);
+  if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
+  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(out), stream, x, bf16 ? 2 : 1));
+  return TPMLP_OK;
+}
+
+int tpmlp_block_backward(const void* x, const void* dout, int64_t T, const tpmlp_shards* sh, float eps, void* dx,
+                         void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
+                         tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if ((rc = check_eps(eps))) return rc;
+  if (!x || !dout || !dx || !ws) return fail(TPMLP_ERR_ARG, "x, dout, dx and workspace must not be NULL");
+  if (!aligned16(x) || !aligned16(dout) || !aligned16(dx) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "x, dout, dx and workspace must be 16-byte aligned");
+  if (sh->D > static_cast<int64_t>(layer_norm_max_d()))
+    return fail(TPMLP_ERR_SHAPE, "D = %lld exceeds the largest supported row of %zu",
+                static_cast<long long>(sh->D), layer_norm_max_d());
+  const BlockPlan b = plan_block(T, sh, mode, 1);
+  if (ws_bytes < b.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, b.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  void* xn = at<char>(ws, b.xn);
+  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(sh->D), eps, sh->dt == TPMLP_BF16, xn, stream));
+  const LnTail tail{x, dout, eps, static_cast<float*>(dx)};
+  void* dxn = mode == TPMLP_FUSED ? at<char>(ws, b.dxn) : dx;  // FAITHFUL: the partials feed the tail directly
+  return backward_impl(xn, dout, nullptr, T, sh, dxn, dA, dB, mode, at<char>(ws, b.inner), b.w.total, stream, &tail);
 }
 
 int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* sh, void* H, int fill,

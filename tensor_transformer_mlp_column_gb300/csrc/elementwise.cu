@@ -52,12 +52,27 @@ __global__ void gelu_bf16_kernel(const __nv_bfloat16* __restrict__ x, __nv_bfloa
 
 // ------------------------------------------------------------------ all-reduce
 
-// Y[j] = ((Yp[0][j] + Yp[1][j]) + Yp[2][j]) + ... in fp32, shard order fixed.
-// Each thread owns float4 columns of the [n][count] block; the n loads of one
-// float4 are issued before the adds so n*16 bytes per thread are in flight.
-// Partials are read once (streaming loads), Y is written once.
+// Y[j] = ((Yp[0][j] + Yp[1][j]) + Yp[2][j]) + ... in fp32, shard order fixed,
+// and with a residual R (res_kind 1: fp32, 2: bf16) then Y[j] = R[j] + that
+// sum. Each thread owns float4 columns of the [n][count] block; the n loads of
+// one float4 are issued before the adds so n*16 bytes per thread are in
+// flight. Partials are read once (streaming loads), Y is written once.
+__device__ __forceinline__ float4 residual4(const void* res, int res_kind, int64_t i) {
+  if (res_kind == 1) return __ldcs(reinterpret_cast<const float4*>(res) + i);
+  const uint2 w = __ldcs(reinterpret_cast<const uint2*>(res) + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ float residual1(const void* res, int res_kind, int64_t j) {
+  if (res_kind == 1) return static_cast<const float*>(res)[j];
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(res)[j]);
+}
+
 template <int NMAX>
 __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __restrict__ Yp, int n, int64_t count,
+                                                               const void* __restrict__ res, int res_kind,
                                                                float* __restrict__ Y) {
   const int64_t n4 = count / 4;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -68,6 +83,8 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
 #pragma unroll
     for (int s = 0; s < NMAX; ++s)
       if (s < n) v[s] = __ldcs(P + s * shard_stride4 + i);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (res_kind) r = residual4(res, res_kind, i);
     float4 acc = v[0];
 #pragma unroll
     for (int s = 1; s < NMAX; ++s) {
@@ -78,23 +95,24 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
         acc.w += v[s].w;
       }
     }
+    if (res_kind) {
+      acc.x = r.x + acc.x;
+      acc.y = r.y + acc.y;
+      acc.z = r.z + acc.z;
+      acc.w = r.w + acc.w;
+    }
     __stcs(reinterpret_cast<float4*>(Y) + i, acc);
-  }
-  // Tail of count % 4 elements (never reached when count is a multiple of 4).
-  for (int64_t j = n4 * 4 + int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
-    float acc = Yp[j];
-    for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + j];
-    Y[j] = acc;
   }
 }
 
-// Any n: the same order, shards taken from memory one by one.
-__global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, float* __restrict__ Y) {
+// Any n and any count: the same order, shards taken from memory one by one.
+__global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, const void* __restrict__ res,
+                                     int res_kind, float* __restrict__ Y) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
     float acc = Yp[j];
     for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + j];
-    Y[j] = acc;
+    Y[j] = res_kind ? residual1(res, res_kind, j) + acc : acc;
   }
 }
 
@@ -180,19 +198,21 @@ cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStre
   return cudaGetLastError();
 }
 
-cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s) {
+cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s, const void* res,
+                             int res_kind) {
   if (count <= 0) return cudaSuccess;
+  if (!res) res_kind = 0;
   const int g = ew_grid(count, 4);
   if (count % 4 != 0)  // shard blocks would not be 16-byte aligned
-    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, Y);
+    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
   else if (n <= 4)
-    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
   else if (n <= 8)
-    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
   else if (n <= 16)
-    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, Y);
+    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
   else
-    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, Y);
+    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,7 @@ struct KParams {
   int group_m;     // tile order: bands of group_m tile rows, rows fastest inside a band (1 = columns fastest)
   int shared;      // kSharedNone / kSharedA / kSharedB: an operand that every group reads
   int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
+  const __nv_bfloat16* resid;  // kEpiF32 / kEpiF32Tma: residual [M][ldo] added to the accumulator, or null
 };
 
 // Maps a tile index to (group, M block, N block). The tiles form a grid of
@@ -100,6 +101,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Output treatment of one thread's 32 accumulator columns n0..n0+31 of row m
 // (group g). The caller has checked m < M and n0 < N; N is a multiple of 8.
+// The bf16 residual of output row m, columns n0..n0+31 (chunks of 8 past N
+// stay zero; N is a multiple of 8 on this path). Loaded before the
+// accumulator is read so that the load's latency overlaps tcgen05.ld.
+__device__ __forceinline__ void load_residual(const KParams& p, int64_t m, int n0, uint4 (&r)[4]) {
+  const __nv_bfloat16* src = p.resid + m * p.ldo + n0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    r[j] = (n0 + 8 * j + 8 <= p.N) ? __ldcs(reinterpret_cast<const uint4*>(src + 8 * j)) : make_uint4(0, 0, 0, 0);
+}
+
+// v[j] = residual[j] + v[j] (the residual added to the finished sum).
+__device__ __forceinline__ void add_residual(const uint4 (&r)[4], float (&v)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r[j]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      v[8 * j + 2 * e] = f.x + v[8 * j + 2 * e];
+      v[8 * j + 2 * e + 1] = f.y + v[8 * j + 2 * e + 1];
+    }
+  }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
   if constexpr (EPI == kEpiGeluBf16 || EPI == kEpiGeluSaveP) {

@@ -240,14 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
+        const int n0 = nb256 * BN + c;
+        uint4 res[4];
+        const bool with_res = (EPI == kEpiF32 || EPI == kEpiF32Tma) && p.resid != nullptr && row_ok && n0 < p.N;
+        if (with_res) load_residual(p, m, n0, res);
         __syncwarp();
         tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
+        if (with_res) add_residual(res, v);
         if (c + 32 == BN) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
         }
-        const int n0 = nb256 * BN + c;
         if constexpr (EPI == kEpiF32Tma) {
           // Stage the warp's 32 x 32 fp32 block in shared memory with the
           // 128-byte swizzle (16-byte chunk j of row r at slot j ^ (r % 8),

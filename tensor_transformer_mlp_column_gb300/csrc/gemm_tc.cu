@@ -195,13 +195,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         float v[32];
+        const int n0 = nb * BN + c;
+        uint4 res[4];
+        const bool with_res = EPI == kEpiF32 && p.resid != nullptr && row_ok && n0 < p.N;
+        if (with_res) load_residual(p, m, n0, res);
         __syncwarp();  // tcgen05.ld is warp-collective
         tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
+        if (with_res) add_residual(res, v);
         if (c + 32 == BN) {
           tc_fence_before_sync();
           mbar_arrive(acc_empty + acc);  // accumulator may be overwritten now
         }
-        const int n0 = nb * BN + c;
         if (!row_ok || n0 >= p.N) continue;
         epilogue_store<EPI>(p, g, m, n0, v);
       }
@@ -395,6 +399,8 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.group_m = env_int("TPMLP_GROUP_M", g.group_m);
   kp.shared = g.shared;
   kp.stream_out = env_int("TPMLP_STREAM_OUT", g.stream_out);
+  kp.resid = static_cast<const __nv_bfloat16*>(g.resid);
+  if (kp.resid && g.epi != kEpiF32) return cudaErrorInvalidValue;
   if (!kp.status) return cudaErrorInvalidSymbol;
   if (kp.tiles == 0) return cudaSuccess;
   if (pair) {

@@ -55,6 +55,7 @@ struct TcGemm {
   int shared;      // TcShared: an operand read by every group (tile order exploits it)
   int group_m;     // tile rows per band of the tile order (see decode_tile); 0 or 1 = columns fastest
   int stream_out;  // 1: evict-first epilogue stores
+  const void* resid;  // kEpiF32 (and its TMA-store form): bf16 residual [M][ldo] added to acc, or null
 };
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
@@ -88,7 +89,21 @@ struct SimtGemm {
 cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
 
 cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStream_t s);
-cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s);
+// Y = ((Yp[0] + Yp[1]) + ...) + Yp[n-1], and with a residual res (res_kind 1:
+// fp32, 2: bf16) Y = res + that sum.
+cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s,
+                             const void* res = nullptr, int res_kind = 0);
+
+// Row-wise layer norm without scale or shift: y = (x - mean) / sqrt(var + eps),
+// D <= layer_norm_max_d(); x and y [T][D] of the same type.
+size_t layer_norm_max_d();
+cudaError_t launch_layer_norm(const void* x, int64_t T, int D, float eps, int is_bf16, void* y, cudaStream_t s);
+// dx = dout + the layer norm's gradient for g = sum of the n partials G [n][T][D]
+// (fp32, summed in order); x and dout [T][D] of the path's type, dx fp32.
+cudaError_t launch_layer_norm_bwd(const float* G, int n, const void* x, const void* dout, int64_t T, int D, float eps,
+                                  int is_bf16, float* dx, cudaStream_t s);
+// out += res, fp32.
+cudaError_t launch_add_residual_f32(float* out, const float* res, int64_t count, cudaStream_t s);
 
 // Per-shard descriptor kept in device memory by the shards handle.
 struct ShardDesc {

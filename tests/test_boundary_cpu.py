@@ -125,3 +125,22 @@ def test_calls_without_a_gpu_report_cuda_or_device_errors(tp):
     rc = tp.lib().tpmlp_gelu(FAKE, FAKE, 8, 0, None)
     assert rc in (tp.TPMLP_ERR_CUDA, tp.TPMLP_ERR_DEVICE)
     assert tp.tpmlp_last_error()
+
+
+def test_block_call_argument_errors(tp):
+    l = tp.lib()
+    # layer norm: shape, eps, pointers, alignment (all checked before any CUDA call)
+    assert l.tpmlp_layer_norm(FAKE, 4, 0, 0, 1e-5, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_layer_norm(FAKE, -1, 8, 0, 1e-5, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_layer_norm(FAKE, 4, 25537, 0, 1e-5, FAKE, None) == tp.TPMLP_ERR_SHAPE
+    assert l.tpmlp_layer_norm(FAKE, 4, 8, 9, 1e-5, FAKE, None) == tp.TPMLP_ERR_ARG
+    for eps in (0.0, -1e-5, float("inf"), float("nan")):
+        assert l.tpmlp_layer_norm(FAKE, 4, 8, 0, eps, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_layer_norm(FAKE, 0, 8, 0, 1e-5, FAKE, None) == tp.TPMLP_OK  # no rows: nothing enqueued
+    assert l.tpmlp_layer_norm(None, 4, 8, 0, 1e-5, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_layer_norm(FAKE + 4, 4, 8, 0, 1e-5, FAKE, None) == tp.TPMLP_ERR_ALIGN
+    # the block calls need a handle
+    assert l.tpmlp_block_workspace_bytes(16, None, 0, 0) == 0
+    assert l.tpmlp_block_forward(FAKE, 4, None, 1e-5, FAKE, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_block_backward(FAKE, FAKE, 4, None, 1e-5, FAKE, None, None, 0, FAKE, 1 << 20,
+                                  None) == tp.TPMLP_ERR_ARG

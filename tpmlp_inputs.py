@@ -98,6 +98,25 @@ def make_inputs(w: Workload, seed: int = 0, with_dy: bool | None = None) -> dict
     return out
 
 
+def make_block_inputs(w: Workload, seed: int = 0, with_dout: bool | None = None) -> dict[str, torch.Tensor]:
+    """Inputs of the block's FFN half: the residual stream x [T, D] plus A, B (and dout [T, D]).
+
+    Each row of x is offset and scaled on its own (offset uniform in [-1, 1],
+    scale log-uniform in [0.5, 2]) so that the layer norm's centring and
+    scaling both matter; A, B and dout are drawn as in make_inputs.
+    """
+    inp = make_inputs(w, seed, with_dy=with_dout)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 4)
+    offset = torch.rand((w.T, 1), generator=g, dtype=torch.float32) * 2.0 - 1.0
+    scale = torch.exp((torch.rand((w.T, 1), generator=g, dtype=torch.float32) * 2.0 - 1.0) * math.log(2.0))
+    x = (inp.pop("X").to(torch.float32) * scale + offset).to(w.torch_dtype)
+    out = {"x": x, "A": inp["A"], "B": inp["B"]}
+    if "dY" in inp:
+        out["dout"] = inp["dY"]
+    return out
+
+
 def sample_indices(n: int, k: int, seed: int) -> list[int]:
     """k distinct sorted indices in [0, n), always including the first and last."""
     if k >= n:
