@@ -4,11 +4,18 @@
 // norm, fused with the shard-ordered sum of the input-gradient partials and
 // the residual's pass-through gradient.
 //
-// Both kernels give one CTA of 256 threads to one token row at a time
-// (persistent over rows). The row is staged in shared memory as fp32, so the
+// Both give one CTA to one token row at a time (persistent over rows): the
 // HBM traffic is one read of every input row and one write of every output
-// row; the statistics are exact two-pass fp32 (mean first, then the mean of
-// squared deviations), summed in a fixed order, so results are reproducible.
+// row. The statistics are two-pass fp32 (mean first, then the mean of squared
+// deviations), summed in a fixed order, so results are reproducible.
+//
+// Rows whose length is a multiple of 8 live in registers: each of THREADS
+// threads holds C chunks of 8 elements, sized so that THREADS * C * 8 covers
+// D. All loads of a row are issued before any of them is used, and the
+// forward kernel issues the next row's loads before it reduces the current
+// one, so each SM keeps 100+ KB of reads in flight (HBM needs about
+// bandwidth x latency / SMs = 7 TB/s x 1.5 us / 152 = 70 KB). Other lengths
+// use the shared-memory kernels (one row staged as fp32).
 #include "device.cuh"
 #include "internal.h"
 
@@ -24,15 +31,35 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Sum over the CTA; every thread gets the result. `red` holds 32 floats.
-__device__ __forceinline__ float block_sum(float v, float* red) {
+// Sum over a CTA of THREADS threads; every thread gets the result. `red`
+// holds 32 floats.
+template <int THREADS>
+__device__ __forceinline__ float block_sum_t(float v, float* red) {
   v = warp_sum(v);
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   __syncthreads();  // the previous call's readers are done with `red`
   if (l == 0) red[w] = v;
   __syncthreads();
-  return warp_sum(l < (kRowThreads >> 5) ? red[l] : 0.f);
+  return warp_sum(l < (THREADS >> 5) ? red[l] : 0.f);
 }
+
+// Two sums in one round of barriers; `red` holds 64 floats.
+template <int THREADS>
+__device__ __forceinline__ void block_sum2_t(float& a, float& b, float* red) {
+  a = warp_sum(a);
+  b = warp_sum(b);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) {
+    red[w] = a;
+    red[32 + w] = b;
+  }
+  __syncthreads();
+  a = warp_sum(l < (THREADS >> 5) ? red[l] : 0.f);
+  b = warp_sum(l < (THREADS >> 5) ? red[32 + l] : 0.f);
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) { return block_sum_t<kRowThreads>(v, red); }
 
 // 8 consecutive elements <-> 8 floats (16 bytes of bf16, 32 bytes of fp32).
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&f)[8]) {
@@ -199,6 +226,172 @@ __global__ void __launch_bounds__(kRowThreads) layer_norm_bwd_kernel(const float
   }
 }
 
+// ------------------------------------------------------------ rows in registers
+
+// 8 elements of E as loaded (16 bytes of bf16, 32 bytes of fp32).
+template <typename E>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 w;
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+};
+
+__device__ __forceinline__ void ld8(const __nv_bfloat16* p, Raw8<__nv_bfloat16>& r) {
+  r.w = __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void ld8(const float* p, Raw8<float>& r) {
+  r.a = __ldcs(reinterpret_cast<const float4*>(p));
+  r.b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+}
+__device__ __forceinline__ void zero8(Raw8<__nv_bfloat16>& r) { r.w = make_uint4(0, 0, 0, 0); }
+__device__ __forceinline__ void zero8(Raw8<float>& r) { r.a = r.b = make_float4(0.f, 0.f, 0.f, 0.f); }
+__device__ __forceinline__ void unpack8(const Raw8<__nv_bfloat16>& r, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r.w);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 t = __bfloat1622float2(h[j]);
+    f[2 * j] = t.x;
+    f[2 * j + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void unpack8(const Raw8<float>& r, float (&f)[8]) {
+  f[0] = r.a.x, f[1] = r.a.y, f[2] = r.a.z, f[3] = r.a.w, f[4] = r.b.x, f[5] = r.b.y, f[6] = r.b.z, f[7] = r.b.w;
+}
+
+// Chunk k of this thread is chunk threadIdx.x + k * THREADS of the row;
+// chunks past the row's nch load as zeros.
+template <typename E, int THREADS, int C>
+__device__ __forceinline__ void fetch_row(const E* __restrict__ row, int nch, Raw8<E> (&r)[C]) {
+#pragma unroll
+  for (int k = 0; k < C; ++k) {
+    const int c = threadIdx.x + k * THREADS;
+    if (c < nch)
+      ld8(row + 8 * c, r[k]);
+    else
+      zero8(r[k]);
+  }
+}
+
+// Layer norm of rows of D = 8 * nch elements held as C chunks per thread;
+// the next row's loads are issued before the current row is reduced.
+template <typename E, int THREADS, int C>
+__global__ void __launch_bounds__(THREADS) layer_norm_reg_kernel(const E* __restrict__ x, int64_t T, int D, float eps,
+                                                                 E* __restrict__ y) {
+  __shared__ float red[32];
+  const int nch = D >> 3;
+  Raw8<E> nxt[C];
+  int64_t t = blockIdx.x;
+  if (t < T) fetch_row<E, THREADS, C>(x + t * D, nch, nxt);
+  for (; t < T; t += gridDim.x) {
+    float v[C][8];
+#pragma unroll
+    for (int k = 0; k < C; ++k) unpack8(nxt[k], v[k]);
+    if (t + gridDim.x < T) fetch_row<E, THREADS, C>(x + (t + gridDim.x) * D, nch, nxt);
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < C; ++k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += v[k][j];  // zero-filled chunks add nothing
+    const float mean = block_sum_t<THREADS>(s, red) / static_cast<float>(D);
+    float q = 0.f;
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      if (static_cast<int>(threadIdx.x) + k * THREADS >= nch) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = v[k][j] - mean;
+        q += d * d;
+      }
+    }
+    const float r = 1.0f / sqrtf(block_sum_t<THREADS>(q, red) / static_cast<float>(D) + eps);
+    E* yr = y + t * D;
+#pragma unroll
+    for (int k = 0; k < C; ++k) {
+      const int c = threadIdx.x + k * THREADS;
+      if (c >= nch) continue;
+      float f[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = (v[k][j] - mean) * r;
+      store8(yr + 8 * c, f);
+    }
+  }
+}
+
+// The backward tail with one chunk per thread (D = 8 * nch <= 8 * THREADS):
+// x, dout and every partial of the thread's chunk are loaded before they are
+// combined (partials two at a time, added in shard order).
+template <typename E, int THREADS>
+__global__ void __launch_bounds__(THREADS) layer_norm_bwd_reg_kernel(const float* __restrict__ G, int n,
+                                                                     const E* __restrict__ x,
+                                                                     const E* __restrict__ dout, int64_t T, int D,
+                                                                     float eps, float* __restrict__ dx) {
+  __shared__ float red[64];
+  const int nch = D >> 3;
+  const int c = threadIdx.x;
+  const bool on = c < nch;
+  const int64_t gstride = T * D;
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const int64_t at = t * D + 8 * c;
+    Raw8<E> xr, dr;
+    float g[8], v[8];
+    if (on) {
+      ld8(x + at, xr);
+      ld8(dout + at, dr);
+      load8(G + at, g);
+      for (int k = 1; k < n; k += 2) {
+        float a[8], b[8];
+        load8(G + k * gstride + at, a);
+        if (k + 1 < n) load8(G + (k + 1) * gstride + at, b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] += a[j];
+        if (k + 1 < n) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] += b[j];
+        }
+      }
+      unpack8(xr, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = v[j] = 0.f;
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s += v[j];
+    const float mean = block_sum_t<THREADS>(s, red) / static_cast<float>(D);
+    float q = 0.f;
+    if (on) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = v[j] - mean;
+        q += d * d;
+      }
+    }
+    const float r = 1.0f / sqrtf(block_sum_t<THREADS>(q, red) / static_cast<float>(D) + eps);
+    float sg = 0.f, sgy = 0.f;
+    if (on) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] = (v[j] - mean) * r;  // y
+        sg += g[j];
+        sgy += g[j] * v[j];
+      }
+    }
+    block_sum2_t<THREADS>(sg, sgy, red);
+    const float mg = sg / static_cast<float>(D), mgy = sgy / static_cast<float>(D);
+    if (on) {
+      float d[8], f[8];
+      unpack8(dr, d);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = d[j] + r * (g[j] - mg - v[j] * mgy);
+      store8(dx + at, f);
+    }
+  }
+}
+
 // out[j] += res[j] (fp32), for the fp32 path's fused sum.
 __global__ void add_residual_f32_kernel(float* __restrict__ out, const float* __restrict__ res, int64_t count) {
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -206,9 +399,9 @@ __global__ void add_residual_f32_kernel(float* __restrict__ out, const float* __
 }
 
 template <typename K>
-int row_grid(K kern, size_t smem, int64_t T) {
+int row_grid(K kern, int threads, size_t smem, int64_t T) {
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRowThreads, smem) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int64_t cap = int64_t(num_sms()) * per_sm;
   return static_cast<int>(T < cap ? T : cap);
@@ -220,47 +413,106 @@ cudaError_t set_smem(K kern, size_t smem) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
+// Smallest power of two >= v, within [32, 1024].
+int pow2_threads(int v) {
+  int t = 32;
+  while (t < v && t < 1024) t <<= 1;
+  return t;
+}
+
+template <typename E, int THREADS, int C>
+cudaError_t ln_reg(const E* x, int64_t T, int D, float eps, E* y, cudaStream_t s) {
+  auto k = layer_norm_reg_kernel<E, THREADS, C>;
+  k<<<row_grid(k, THREADS, 0, T), THREADS, 0, s>>>(x, T, D, eps, y);
+  return cudaGetLastError();
+}
+
+// Forward: two chunks per thread where the row allows (so each thread has
+// four 16-byte loads in flight with the next row's), else one.
+template <typename E>
+cudaError_t ln_dispatch(const E* x, int64_t T, int D, float eps, E* y, cudaStream_t s) {
+  const int nch = D / 8;
+  const int threads = pow2_threads((nch + 1) / 2);
+  const int C = (nch + threads - 1) / threads;
+  if (D % 8 == 0 && C <= 2) {
+#define TPMLP_LN_CASE(TH)                                                        \
+  case TH:                                                                       \
+    return C == 1 ? ln_reg<E, TH, 1>(x, T, D, eps, y, s) : ln_reg<E, TH, 2>(x, T, D, eps, y, s);
+    switch (threads) {
+      TPMLP_LN_CASE(32)
+      TPMLP_LN_CASE(64)
+      TPMLP_LN_CASE(128)
+      TPMLP_LN_CASE(256)
+      TPMLP_LN_CASE(512)
+      TPMLP_LN_CASE(1024)
+      default:
+        break;
+    }
+#undef TPMLP_LN_CASE
+  }
+  const size_t smem = (32 + size_t(D)) * sizeof(float);
+  auto k = layer_norm_kernel<E>;
+  cudaError_t e = set_smem(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<row_grid(k, kRowThreads, smem, T), kRowThreads, smem, s>>>(x, T, D, eps, y);
+  return cudaGetLastError();
+}
+
+template <typename E, int THREADS>
+cudaError_t lnb_reg(const float* G, int n, const E* x, const E* dout, int64_t T, int D, float eps, float* dx,
+                    cudaStream_t s) {
+  auto k = layer_norm_bwd_reg_kernel<E, THREADS>;
+  k<<<row_grid(k, THREADS, 0, T), THREADS, 0, s>>>(G, n, x, dout, T, D, eps, dx);
+  return cudaGetLastError();
+}
+
+// Backward tail: one chunk per thread up to D = 8192, else the shared-memory kernel.
+template <typename E>
+cudaError_t lnb_dispatch(const float* G, int n, const E* x, const E* dout, int64_t T, int D, float eps, float* dx,
+                         cudaStream_t s) {
+  const int nch = D / 8;
+  if (D % 8 == 0 && nch <= 1024) {
+    switch (pow2_threads(nch)) {
+      case 32:
+        return lnb_reg<E, 32>(G, n, x, dout, T, D, eps, dx, s);
+      case 64:
+        return lnb_reg<E, 64>(G, n, x, dout, T, D, eps, dx, s);
+      case 128:
+        return lnb_reg<E, 128>(G, n, x, dout, T, D, eps, dx, s);
+      case 256:
+        return lnb_reg<E, 256>(G, n, x, dout, T, D, eps, dx, s);
+      case 512:
+        return lnb_reg<E, 512>(G, n, x, dout, T, D, eps, dx, s);
+      default:
+        return lnb_reg<E, 1024>(G, n, x, dout, T, D, eps, dx, s);
+    }
+  }
+  const size_t smem = (32 + 2 * size_t(D)) * sizeof(float);
+  auto k = layer_norm_bwd_kernel<E>;
+  cudaError_t e = set_smem(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<row_grid(k, kRowThreads, smem, T), kRowThreads, smem, s>>>(G, n, x, dout, T, D, eps, dx);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t layer_norm_max_d() { return (200 * 1024) / 8 - 64; }
 
 cudaError_t launch_layer_norm(const void* x, int64_t T, int D, float eps, int is_bf16, void* y, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const size_t smem = (32 + size_t(D)) * sizeof(float);
-  if (is_bf16) {
-    auto k = layer_norm_kernel<__nv_bfloat16>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    k<<<row_grid(k, smem, T), kRowThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(x), T, D, eps,
-                                                     static_cast<__nv_bfloat16*>(y));
-  } else {
-    auto k = layer_norm_kernel<float>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    k<<<row_grid(k, smem, T), kRowThreads, smem, s>>>(static_cast<const float*>(x), T, D, eps,
-                                                     static_cast<float*>(y));
-  }
-  return cudaGetLastError();
+  if (is_bf16)
+    return ln_dispatch(static_cast<const __nv_bfloat16*>(x), T, D, eps, static_cast<__nv_bfloat16*>(y), s);
+  return ln_dispatch(static_cast<const float*>(x), T, D, eps, static_cast<float*>(y), s);
 }
 
 cudaError_t launch_layer_norm_bwd(const float* G, int n, const void* x, const void* dout, int64_t T, int D, float eps,
                                   int is_bf16, float* dx, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const size_t smem = (32 + 2 * size_t(D)) * sizeof(float);
-  if (is_bf16) {
-    auto k = layer_norm_bwd_kernel<__nv_bfloat16>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    k<<<row_grid(k, smem, T), kRowThreads, smem, s>>>(G, n, static_cast<const __nv_bfloat16*>(x),
-                                                     static_cast<const __nv_bfloat16*>(dout), T, D, eps, dx);
-  } else {
-    auto k = layer_norm_bwd_kernel<float>;
-    cudaError_t e = set_smem(k, smem);
-    if (e != cudaSuccess) return e;
-    k<<<row_grid(k, smem, T), kRowThreads, smem, s>>>(G, n, static_cast<const float*>(x),
-                                                     static_cast<const float*>(dout), T, D, eps, dx);
-  }
-  return cudaGetLastError();
+  if (is_bf16)
+    return lnb_dispatch(G, n, static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(dout), T, D,
+                        eps, dx, s);
+  return lnb_dispatch(G, n, static_cast<const float*>(x), static_cast<const float*>(dout), T, D, eps, dx, s);
 }
 
 cudaError_t launch_add_residual_f32(float* out, const float* res, int64_t count, cudaStream_t s) {
