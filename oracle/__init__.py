@@ -24,4 +24,9 @@ from .tpmlp_oracle import (  # noqa: F401
     layer_norm_backward,
     block_mlp_backward,
     block_mlp_backward_dx_rows,
+    split_rows,
+    all_gather,
+    reduce_scatter,
+    tp_mlp_sp,
+    tp_mlp_sp_backward,
 )

@@ -254,3 +254,63 @@ def block_mlp_backward_dx_rows(x, dout, shards, rows, eps: float = LN_EPS):
     """Rows `rows` of block_mlp_backward's dx: each row needs only its own x and dout rows."""
     dx, _, _ = block_mlp_backward(_f64(x)[rows], _f64(dout)[rows], shards, eps)
     return dx
+
+
+# ---------------------------------------------------------------------------
+# Sequence-parallel form of the sum (duoan.github.io "Tensor Parallelism in
+# Megatron-LM", "Row split": the partials are summed by an all-reduce, or by
+# reduce-scatter / all-gather when the sequence is split). With n ranks and T
+# divisible by n, rank j holds token rows j*T/n .. (j+1)*T/n - 1 of X and of
+# the output; the all-gather assembles X from the slices in rank order, and
+# the reduce-scatter hands rank j the same rows of the shard-ordered sum.
+# ---------------------------------------------------------------------------
+
+def split_rows(M, n: int):
+    """Rank j's token slice: rows j*T/n .. (j+1)*T/n - 1 (T divisible by n)."""
+    M = _f64(M)
+    T = M.shape[0]
+    if n <= 0 or T % n != 0:
+        raise ValueError(f"T={T} is not divisible by n={n}")
+    Ts = T // n
+    return [M[j * Ts:(j + 1) * Ts] for j in range(n)]
+
+
+def all_gather(slices):
+    """The full [T, D] tensor from the n rank slices, in rank order."""
+    return np.concatenate([_f64(s) for s in slices], axis=0)
+
+
+def reduce_scatter(partials, n: int):
+    """Rank j's slice of ((P_0 + P_1) + ...) + P_{n-1}, summed slice by slice."""
+    parts = [split_rows(P, n) for P in partials]
+    out = []
+    for j in range(n):
+        acc = parts[0][j].copy()
+        for i in range(1, len(parts)):
+            acc = acc + parts[i][j]
+        out.append(acc)
+    return out
+
+
+def tp_mlp_sp(X_slices, shards):
+    """Sequence-parallel forward: all-gather X, every shard's partial, reduce-scatter."""
+    X = all_gather(X_slices)
+    partials = [shard_partial(X, A_i, B_i)[1] for (A_i, B_i) in shards]
+    return reduce_scatter(partials, len(X_slices))
+
+
+def tp_mlp_sp_backward(X_slices, dY_slices, shards):
+    """Sequence-parallel backward: all-gather X and dY, the shards' gradients,
+    and the dX partials reduce-scattered to the ranks: ([dX_j], [dA_i], [dB_i])."""
+    X = all_gather(X_slices)
+    dY = all_gather(dY_slices)
+    dA, dB, dX_parts = [], [], []
+    for A_i, B_i in shards:
+        A_i = _f64(A_i)
+        B_i = _f64(B_i)
+        P_i = X @ A_i
+        dP_i = (dY @ B_i.T) * gelu_grad(P_i)
+        dB.append(gelu(P_i).T @ dY)
+        dA.append(X.T @ dP_i)
+        dX_parts.append(dP_i @ A_i.T)
+    return reduce_scatter(dX_parts, len(X_slices)), dA, dB

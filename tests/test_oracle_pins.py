@@ -405,3 +405,63 @@ def test_block_pins_catch_planted_mistakes():
     # the unbiased variance gives a different normalisation
     bad = (x - x.mean(axis=1, keepdims=True)) / np.sqrt(x.var(axis=1, ddof=1, keepdims=True) + 1e-5)
     assert np.max(np.abs(bad - y)) > 1e-2
+
+
+# ---------------------------------------------------------------- sequence-parallel sum
+
+def test_reduce_scatter_brute_force_and_all_reduce_identity():
+    rng = np.random.default_rng(27)
+    n, T, D = 3, 6, 4
+    partials = [rng.normal(size=(T, D)) for _ in range(n)]
+    rs = oracle.reduce_scatter(partials, n)
+    # brute force with Python scalars: rank j, row r, column c
+    for j in range(n):
+        for r in range(T // n):
+            for c in range(D):
+                acc = partials[0][j * (T // n) + r][c]
+                for i in range(1, n):
+                    acc = acc + partials[i][j * (T // n) + r][c]
+                assert rs[j][r, c] == acc
+    # all-gather after reduce-scatter is the all-reduce, bit for bit in the same order
+    ar = partials[0] + partials[1] + partials[2]
+    assert np.array_equal(oracle.all_gather(rs), ar)
+    # and all-gather inverts the row split
+    X = rng.normal(size=(T, D))
+    assert np.array_equal(oracle.all_gather(oracle.split_rows(X, n)), X)
+    with pytest.raises(ValueError):
+        oracle.split_rows(np.zeros((7, 2)), 3)
+
+
+def test_sequence_parallel_forward_and_backward_equal_the_unsplit_ones():
+    rng = np.random.default_rng(28)
+    T, D, F = 8, 6, 12
+    X, dY = rng.normal(size=(T, D)), rng.normal(size=(T, D))
+    A, B = rng.normal(size=(D, F)) * 0.5, rng.normal(size=(F, D)) * 0.5
+    for n in (1, 2, 4):
+        shards = oracle.shard_mlp(A, B, n)
+        Y = oracle.tp_mlp(X, shards)
+        Ys = oracle.tp_mlp_sp(oracle.split_rows(X, n), shards)
+        assert len(Ys) == n and all(y.shape == (T // n, D) for y in Ys)
+        np.testing.assert_allclose(oracle.all_gather(Ys), oracle.mlp(X, A, B), rtol=1e-13, atol=1e-13)
+        for j, Yj in enumerate(Ys):  # rank j owns rows j*T/n.. of the all-reduced output
+            np.testing.assert_allclose(Yj, Y[j * (T // n):(j + 1) * (T // n)], rtol=1e-14, atol=1e-14)
+        dXs, dA, dB = oracle.tp_mlp_sp_backward(oracle.split_rows(X, n), oracle.split_rows(dY, n), shards)
+        dX_ref, dA_ref, dB_ref = oracle.tp_mlp_backward(X, dY, shards)
+        np.testing.assert_allclose(oracle.all_gather(dXs), dX_ref, rtol=1e-12, atol=1e-13)
+        for i in range(n):
+            np.testing.assert_allclose(dA[i], dA_ref[i], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(dB[i], dB_ref[i], rtol=1e-12, atol=1e-13)
+
+
+def test_sequence_parallel_pins_catch_planted_mistakes():
+    rng = np.random.default_rng(29)
+    n, T, D = 2, 4, 3
+    partials = [rng.normal(size=(T, D)) for _ in range(n)]
+    rs = oracle.reduce_scatter(partials, n)
+    # scattering by columns, or handing rank j the other rank's rows, is caught
+    by_cols = [sum(P[:, :2] for P in partials), sum(P[:, 2:] for P in partials)]
+    assert by_cols[0].shape != rs[0].shape or not np.allclose(by_cols[0], rs[0])
+    swapped = list(reversed(rs))
+    assert not np.allclose(oracle.all_gather(swapped), partials[0] + partials[1])
+    # a reduce-scatter that drops a partial
+    assert not np.allclose(oracle.split_rows(partials[0], n)[0], rs[0])
