@@ -572,6 +572,73 @@ def bench_block(args, local_rank, peaks):
     return out
 
 
+def bench_sp(args, local_rank, peaks):
+    """Sequence-parallel form: the forward with X in N rank slices and Y
+    reduce-scattered to them (large workload) against the plain forward, the
+    two simulated collectives alone, and the backward (fwd+bwd workload)."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import WORKLOADS, make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(3, min(args.steps // 10, 10))
+    w = WORKLOADS["large"]
+    inp = make_inputs(w, seed=0)
+    X = inp["X"].to(dev)
+    sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+    del inp
+    n, Ts = w.N, w.T // w.N
+    Xs = [c.clone() for c in torch.chunk(X, n, dim=0)]
+    Ys = [torch.empty((Ts, w.D), dtype=torch.float32, device=dev) for _ in range(n)]
+    Y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+    fwd = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16, {Ts} tokens per rank"}
+    Xg = torch.empty_like(X)
+    ms = _time_ms(lambda: tp.tpmlp_all_gather(Xs, Xg), dev, stream, 20)
+    gbs = 2.0 * w.T * w.D * 2 / (ms * 1e-3) / 1e9
+    fwd["all_gather"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    Yp = torch.randn((n, w.T, w.D), dtype=torch.float32, device=dev)
+    ms = _time_ms(lambda: tp.tpmlp_reduce_scatter(Yp, Ys), dev, stream, 20)
+    gbs = (n + 1.0) * w.T * w.D * 4 / (ms * 1e-3) / 1e9
+    fwd["reduce_scatter"] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm_gbs"], 4)}
+    del Yp
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_sp_workspace_bytes(w.T, sh, mode, 0), dtype=torch.uint8, device=dev)
+        ms_sp = _time_ms(lambda: tp.tpmlp_forward_sp(Xs, sh, mode, Ys, ws), dev, stream, reps)
+        ms_u = _time_ms(lambda: tp.tpmlp_forward(X, sh, mode, Y, ws), dev, stream, reps)
+        fwd[mode] = {"ms": round(ms_sp, 4), "TFLOP/s": round(w.fwd_flops() / (ms_sp * 1e-3) / 1e12, 1),
+                     "unsplit_forward_ms": round(ms_u, 4), "overhead_ms": round(ms_sp - ms_u, 4)}
+        del ws
+    tp.tpmlp_check_status(stream)
+    sh.free()
+    del X, Xs, Ys, Y, Xg
+    out = {"forward": fwd}
+    if args.no_backward:
+        return out
+    w = WORKLOADS["fwd_bwd"]
+    inp = make_inputs(w, seed=0)
+    n, Ts = w.N, w.T // w.N
+    Xs = [c.clone() for c in torch.chunk(inp["X"].to(dev), n, dim=0)]
+    dYs = [c.clone() for c in torch.chunk(inp["dY"].to(dev), n, dim=0)]
+    sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
+    del inp
+    dXs = [torch.empty((Ts, w.D), dtype=torch.float32, device=dev) for _ in range(n)]
+    dA = [torch.empty((w.D, w.Fs), dtype=torch.float32, device=dev) for _ in range(n)]
+    dB = [torch.empty((w.Fs, w.D), dtype=torch.float32, device=dev) for _ in range(n)]
+    bwd = {"workload": f"{w.name}: T={w.T} D={w.D} F={w.F} N={w.N} bf16, {Ts} tokens per rank"}
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_sp_workspace_bytes(w.T, sh, mode, 1), dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: tp.tpmlp_backward_sp(Xs, dYs, sh, mode, dXs, dA, dB, ws), dev, stream, reps)
+        alg = 8.0 * w.T * w.D * w.F / (ms * 1e-3) / 1e12
+        bwd[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1), "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1)}
+        del ws
+    tp.tpmlp_check_status(stream)
+    sh.free()
+    out["backward"] = bwd
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -706,6 +773,7 @@ def main():
         line["other_workloads"] = bench_small_workloads(local_rank)
         line["gelu"] = bench_gelu(local_rank, peaks)
         line["block"] = bench_block(args, local_rank, peaks)
+        line["sequence_parallel"] = bench_sp(args, local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

@@ -278,6 +278,53 @@ int tpmlp_block_backward(const void* x, const void* dout, int64_t T, const tpmlp
                          void* const* dA, void* const* dB, tpmlp_mode mode, void* workspace,
                          size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Sequence-parallel form ([P3] "Row split": the partials are summed by an
+ * all-reduce, or by reduce-scatter / all-gather when the sequence is split).
+ * The n ranks are the n shards; T must be divisible by n, and rank j holds
+ * token rows j*T/n .. (j+1)*T/n - 1 of X (and dY) and receives the same rows
+ * of the output (and of dX). Each call takes host arrays of n device
+ * pointers, one per rank slice, each 16-byte aligned. n <= TPMLP_MAX_SHARDS
+ * (TPMLP_ERR_UNSUPPORTED above), T % n != 0 gives TPMLP_ERR_DIVISIBILITY.
+ * ---------------------------------------------------------------------- */
+
+/* The simulated all-gather: out = slices[0] .. slices[n-1] back to back,
+ * slice_bytes (a multiple of 2) each. out device, n * slice_bytes bytes,
+ * overlapping no slice. */
+int tpmlp_all_gather(const void* const* slices, int n, int64_t slice_bytes, void* out, tpmlp_stream_t stream);
+
+/* The simulated reduce-scatter: the shard-ordered fp32 sum
+ * ((Yp_0 + Yp_1) + ...) + Yp_{n-1} of the partials Yp device [n][count]
+ * fp32, cut into n equal slices; slice j (count/n elements, count % n == 0)
+ * goes to Y_slices[j] (device fp32). Bit-identical to the matching part of
+ * tpmlp_allreduce. */
+int tpmlp_reduce_scatter(const void* Yp, int n, int64_t count, void* const* Y_slices, tpmlp_stream_t stream);
+
+/* Workspace bytes tpmlp_forward_sp (backward = 0) or tpmlp_backward_sp
+ * (backward = 1) needs; 0 on bad arguments (incl. T % n != 0). */
+size_t tpmlp_sp_workspace_bytes(int64_t T, const tpmlp_shards* shards, tpmlp_mode mode, int backward);
+
+/* Sequence-parallel forward: X = all-gather of the n slices, every shard's
+ * partial of GeLU(X A_i) B_i, and rank j's rows of the shard-ordered sum
+ * written to Y_slices[j].
+ *   X_slices  n device pointers, [T/n, D] of the handle's dtype.
+ *   Y_slices  n device pointers, [T/n, D] fp32.
+ *   mode      FAITHFUL: partials, then the reduce-scatter kernel; FUSED: the
+ *             on-chip shard-ordered sum, whose epilogue writes each output
+ *             row straight into its rank's slice.
+ *   workspace at least tpmlp_sp_workspace_bytes(T, shards, mode, 0). */
+int tpmlp_forward_sp(const void* const* X_slices, int64_t T, const tpmlp_shards* shards, void* const* Y_slices,
+                     tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Sequence-parallel backward: X and dY all-gathered from their slices, the
+ * gradients of tpmlp_backward, and dX reduce-scattered: rank j's rows of
+ * dX = sum_i dP_i A_i^T go to dX_slices[j] ([T/n, D] fp32). dA, dB as for
+ * tpmlp_backward (every rank's shard gradient is whole).
+ *   workspace at least tpmlp_sp_workspace_bytes(T, shards, mode, 1). */
+int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices, int64_t T,
+                      const tpmlp_shards* shards, void* const* dX_slices, void* const* dA, void* const* dB,
+                      tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit
  * of limit_ms milliseconds (1..10000). The block then stops and records

@@ -67,6 +67,12 @@ SIGNATURES = {
     "tpmlp_block_forward": (_I, [_P, _I64, _P, ctypes.c_float, _P, _P, _I, _P, _SZ, _P]),
     "tpmlp_block_backward": (_I, [_P, _P, _I64, _P, ctypes.c_float, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P,
                                   _SZ, _P]),
+    "tpmlp_all_gather": (_I, [ctypes.POINTER(_P), _I, _I64, _P, _P]),
+    "tpmlp_reduce_scatter": (_I, [_P, _I, _I64, ctypes.POINTER(_P), _P]),
+    "tpmlp_sp_workspace_bytes": (_SZ, [_I64, _P, _I, _I]),
+    "tpmlp_forward_sp": (_I, [ctypes.POINTER(_P), _I64, _P, ctypes.POINTER(_P), _I, _P, _SZ, _P]),
+    "tpmlp_backward_sp": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_P), _I64, _P, ctypes.POINTER(_P),
+                               ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -362,6 +368,76 @@ def tpmlp_block_backward(x: torch.Tensor, dout: torch.Tensor, shards: Shards, mo
                                       pa, pb, _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(),
                                       _stream(stream)), "tpmlp_block_backward")
     return dx, dA, dB
+
+
+def _ptrs(ts, name):
+    return (ctypes.c_void_p * len(ts))(*[_dev(t, name) for t in ts])
+
+
+def tpmlp_all_gather(slices: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The rank slices [T/n, ...] back to back: out [T, ...] (the simulated all-gather)."""
+    n = len(slices)
+    out = torch.empty((n * slices[0].shape[0],) + tuple(slices[0].shape[1:]), dtype=slices[0].dtype,
+                      device=slices[0].device) if out is None else out
+    nbytes = slices[0].numel() * slices[0].element_size()
+    _check(lib().tpmlp_all_gather(_ptrs(slices, "slice"), n, nbytes, _dev(out, "out"), _stream(stream)),
+           "tpmlp_all_gather")
+    return out
+
+
+def tpmlp_reduce_scatter(Yp: torch.Tensor, Y_slices: Optional[Sequence[torch.Tensor]] = None,
+                         stream=None) -> list:
+    """Rank j's rows of the shard-ordered sum of Yp [n, T, D] fp32: n tensors [T/n, D]."""
+    n, T = Yp.shape[0], Yp.shape[1]
+    rest = tuple(Yp.shape[2:])
+    if Y_slices is None:
+        Y_slices = [torch.empty((T // n,) + rest, dtype=torch.float32, device=Yp.device) for _ in range(n)]
+    count = Yp[0].numel()
+    _check(lib().tpmlp_reduce_scatter(_dev(Yp, "Yp"), n, count, _ptrs(Y_slices, "Y_slice"), _stream(stream)),
+           "tpmlp_reduce_scatter")
+    return list(Y_slices)
+
+
+def tpmlp_sp_workspace_bytes(T: int, shards: Shards, mode="faithful", backward: int = 0) -> int:
+    return int(lib().tpmlp_sp_workspace_bytes(T, shards.handle, _mode(mode), int(backward)))
+
+
+def tpmlp_forward_sp(X_slices: Sequence[torch.Tensor], shards: Shards, mode="faithful",
+                     Y_slices: Optional[Sequence[torch.Tensor]] = None, workspace: Optional[torch.Tensor] = None,
+                     stream=None) -> list:
+    """Sequence-parallel forward: rank j's rows of sum_i GeLU(X A_i) B_i, X the all-gather of X_slices."""
+    n = shards.n
+    Ts = X_slices[0].shape[0]
+    dev = X_slices[0].device
+    if Y_slices is None:
+        Y_slices = [torch.empty((Ts, shards.D), dtype=torch.float32, device=dev) for _ in range(n)]
+    T = Ts * len(X_slices)
+    ws = _workspace(tpmlp_sp_workspace_bytes(T, shards, mode, 0), workspace)
+    _check(lib().tpmlp_forward_sp(_ptrs(X_slices, "X_slice"), T, shards.handle, _ptrs(Y_slices, "Y_slice"),
+                                  _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpmlp_forward_sp")
+    return list(Y_slices)
+
+
+def tpmlp_backward_sp(X_slices: Sequence[torch.Tensor], dY_slices: Sequence[torch.Tensor], shards: Shards,
+                      mode="faithful", dX_slices: Optional[Sequence[torch.Tensor]] = None,
+                      dA: Optional[Sequence[torch.Tensor]] = None, dB: Optional[Sequence[torch.Tensor]] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
+    """Sequence-parallel backward: ([dX_j [T/n, D]], [dA_i], [dB_i]), all fp32."""
+    n, D, Fs = shards.n, shards.D, shards.Fs
+    Ts = X_slices[0].shape[0]
+    dev = X_slices[0].device
+    T = Ts * len(X_slices)
+    if dX_slices is None:
+        dX_slices = [torch.empty((Ts, D), dtype=torch.float32, device=dev) for _ in range(n)]
+    dA = [torch.empty((D, Fs), dtype=torch.float32, device=dev) for _ in range(n)] if dA is None else list(dA)
+    dB = [torch.empty((Fs, D), dtype=torch.float32, device=dev) for _ in range(n)] if dB is None else list(dB)
+    ws = _workspace(tpmlp_sp_workspace_bytes(T, shards, mode, 1), workspace)
+    _check(lib().tpmlp_backward_sp(_ptrs(X_slices, "X_slice"), _ptrs(dY_slices, "dY_slice"), T, shards.handle,
+                                   _ptrs(dX_slices, "dX_slice"), _ptrs(dA, "dA_i"), _ptrs(dB, "dB_i"), _mode(mode),
+                                   ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpmlp_backward_sp")
+    return list(dX_slices), dA, dB
 
 
 def tpmlp_selftest_gemm_withheld_fill(X: torch.Tensor, shards: Shards, H: torch.Tensor, fill: int, limit_ms: int,

@@ -189,8 +189,10 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
 
 // Y_i = H_i B_i into Yp (chain = 0), or Y = sum_i H_i B_i into Y (chain = 1);
 // with chain = 1 and a residual R [T][D] of the path's type, Y = R + that sum.
+// With slices (chain = 1 only), the output rows are cut into n rank slices of
+// T/n rows and slice j goes to slices->p[j] instead of `out`.
 int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int chain, cudaStream_t s,
-               const void* resid = nullptr) {
+               const void* resid = nullptr, const OutSlices* slices = nullptr) {
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     std::vector<CUtensorMap> mh(sh->n), mo(sh->n);
@@ -202,10 +204,17 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
       if (rc) return rc;
       g.map_a[i] = &mh[i];
       g.map_b[i] = &sh->map_Bt[i];
+      if (slices) {  // rank slices: one output (and output map) per slice of T/n rows
+        g.out[i] = slices->p[i];
+        if ((rc = out_map(&mo[i], g.out[i], T / sh->n, D, D, "Y slice"))) return rc;
+        g.map_out[i] = &mo[i];
+        continue;
+      }
       g.out[i] = chain ? out : static_cast<void*>(static_cast<float*>(out) + static_cast<size_t>(i) * T * D);
       if ((rc = out_map(&mo[i], g.out[i], T, D, D, "Y_i"))) return rc;
       g.map_out[i] = &mo[i];
     }
+    if (slices) g.slice_rows = T / sh->n;
     g.ldo = D;
     g.M = static_cast<int>(T);
     g.N = static_cast<int>(D);
@@ -218,12 +227,18 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
     TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
     return TPMLP_OK;
   }
-  for (int i = 0; i < sh->n; ++i) {
-    float* C = chain ? static_cast<float*>(out) : static_cast<float*>(out) + static_cast<size_t>(i) * T * D;
-    SimtGemm g{static_cast<const float*>(H) + static_cast<size_t>(i) * T * Fs, Fs, 1,
-               static_cast<const float*>(sh->desc[i].B), D, 1, C, D, static_cast<int>(T), static_cast<int>(D),
-               static_cast<int>(Fs), (chain && i > 0) ? kSimtAccumulate : kSimtStore};
-    TRY_CUDA(launch_simt_gemm(g, s));
+  // fp32: one product per shard (and, with rank slices, per slice of T/n rows).
+  const int nsl = slices ? sh->n : 1;
+  const int64_t rows = T / nsl;
+  for (int j = 0; j < nsl; ++j) {
+    for (int i = 0; i < sh->n; ++i) {
+      float* C = slices ? slices->p[j]
+                        : (chain ? static_cast<float*>(out) : static_cast<float*>(out) + static_cast<size_t>(i) * T * D);
+      SimtGemm g{static_cast<const float*>(H) + static_cast<size_t>(i) * T * Fs + static_cast<size_t>(j) * rows * Fs,
+                 Fs, 1, static_cast<const float*>(sh->desc[i].B), D, 1, C, D, static_cast<int>(rows),
+                 static_cast<int>(D), static_cast<int>(Fs), (chain && i > 0) ? kSimtAccumulate : kSimtStore};
+      TRY_CUDA(launch_simt_gemm(g, s));
+    }
   }
   if (chain && resid)
     TRY_CUDA(launch_add_residual_f32(static_cast<float*>(out), static_cast<const float*>(resid), T * D, s));
@@ -264,6 +279,37 @@ BlockPlan plan_block(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int bac
   return b;
 }
 
+// Workspace of the sequence-parallel calls: the all-gathered X (and dY), then
+// the MLP call's own workspace.
+struct SpPlan {
+  size_t x = 0, dy = 0, inner = 0, total = 0;
+  WsPlan w;
+};
+
+SpPlan plan_sp(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  SpPlan p;
+  const size_t bytes = static_cast<size_t>(T) * sh->D * esize(sh->dt);
+  size_t off = round_up(bytes, 256);
+  if (backward) {
+    p.dy = off;
+    off = round_up(off + bytes, 256);
+  }
+  p.inner = off;
+  p.w = plan_workspace(T, sh, mode, backward ? 1 : 0);
+  p.total = off + p.w.total;
+  return p;
+}
+
+// Checks a host array of n rank-slice pointers (non-NULL, 16-byte aligned).
+int check_slices(const void* const* p, int n, const char* what) {
+  if (!p) return fail(TPMLP_ERR_ARG, "%s must not be NULL", what);
+  for (int j = 0; j < n; ++j) {
+    if (!p[j]) return fail(TPMLP_ERR_ARG, "%s[%d] is NULL", what, j);
+    if (!aligned16(p[j])) return fail(TPMLP_ERR_ALIGN, "%s[%d] must be 16-byte aligned", what, j);
+  }
+  return TPMLP_OK;
+}
+
 int check_eps(float eps) {
   if (!(eps > 0.f) || !(eps < 1e30f)) return fail(TPMLP_ERR_ARG, "eps = %g must be positive and finite", double(eps));
   return TPMLP_OK;
@@ -294,7 +340,11 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
 // The last step of the backward: dX = the shard-ordered sum of the partials
 // (FAITHFUL; FUSED already accumulated dX), or with a tail the block's dx.
 int finish_dx(const float* dXp, int n, int64_t T, const tpmlp_shards* sh, void* dX, const LnTail* tail,
-              cudaStream_t s) {
+              const OutSlices* slices, cudaStream_t s) {
+  if (slices) {  // the rank slices were written by the product (fused) or come from the partials
+    if (dXp) TRY_CUDA(launch_reduce_scatter(dXp, n, T * sh->D, *slices, n, s));
+    return TPMLP_OK;
+  }
   if (tail) {
     const float* G = dXp ? dXp : static_cast<const float*>(dX);
     TRY_CUDA(launch_layer_norm_bwd(G, dXp ? n : 1, tail->x, tail->dout, T, static_cast<int>(sh->D), tail->eps,
@@ -526,7 +576,7 @@ int tpmlp_forward_save(const void* X, int64_t T, const tpmlp_shards* sh, void* Y
 
 static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
-                         cudaStream_t stream, const LnTail* tail);
+                         cudaStream_t stream, const LnTail* tail, const OutSlices* dx_slices = nullptr);
 
 int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards* sh, void* dX, void* const* dA,
                    void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
@@ -549,7 +599,7 @@ int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T
 // FUSED mode.
 static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
-                         cudaStream_t stream, const LnTail* tail) {
+                         cudaStream_t stream, const LnTail* tail, const OutSlices* dx_slices) {
   int rc = check_common(sh, T);
   if (rc) return rc;
   if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
@@ -596,11 +646,18 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
       // dB_i = H_i^T dY ; dA_i = X^T dP_i ; dX_i = dP_i A_i^T
       TRY_CUDA(launch_simt_gemm(SimtGemm{Hi, 1, Fs, dy, D, 1, static_cast<float*>(dB[i]), D, fs, d, t, kSimtStore}, s));
       TRY_CUDA(launch_simt_gemm(SimtGemm{x, 1, D, dPi, Fs, 1, static_cast<float*>(dA[i]), Fs, d, fs, t, kSimtStore}, s));
-      float* C = dXp ? dXp + static_cast<size_t>(i) * T * D : static_cast<float*>(dX);
       const int epi = (!dXp && i > 0) ? kSimtAccumulate : kSimtStore;
-      TRY_CUDA(launch_simt_gemm(SimtGemm{dPi, Fs, 1, Ai, 1, Fs, C, D, t, d, fs, epi}, s));
+      if (dXp || !dx_slices) {
+        float* C = dXp ? dXp + static_cast<size_t>(i) * T * D : static_cast<float*>(dX);
+        TRY_CUDA(launch_simt_gemm(SimtGemm{dPi, Fs, 1, Ai, 1, Fs, C, D, t, d, fs, epi}, s));
+      } else {  // fused, rank slices: each slice's rows of dX straight into its buffer
+        const int64_t rows = T / n;
+        for (int j = 0; j < n; ++j)
+          TRY_CUDA(launch_simt_gemm(SimtGemm{dPi + static_cast<size_t>(j) * rows * Fs, Fs, 1, Ai, 1, Fs,
+                                             dx_slices->p[j], D, static_cast<int>(rows), d, fs, epi}, s));
+      }
     }
-    return finish_dx(dXp, n, T, sh, dX, tail, s);
+    return finish_dx(dXp, n, T, sh, dX, tail, dx_slices, s);
   }
 
   // bf16: tensor-core products on K-major operands.
@@ -694,8 +751,14 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
     g.map_a[i] = &mdP[i];
     g.map_b[i] = &sh->map_A[i];
     g.out[i] = dXp ? static_cast<void*>(dXp + static_cast<size_t>(i) * T * D) : dX;
+    if (!dXp && dx_slices) {  // fused, rank slices: one output (and output map) per slice of T/n rows
+      g.out[i] = dx_slices->p[i];
+      if ((rc = out_map(&mo[i], g.out[i], T / n, D, D, "dX slice"))) return rc;
+      continue;
+    }
     if ((rc = out_map(&mo[i], g.out[i], T, D, D, "dX_i"))) return rc;
   }
+  if (!dXp && dx_slices) g.slice_rows = T / n;
   g.ldo = D;
   g.M = static_cast<int>(T);
   g.N = static_cast<int>(D);
@@ -704,7 +767,7 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
   g.shared = kSharedNone;
   g.group_m = 8;
   TRY_CUDA(launch_tc_gemm(g, wl, s));
-  return finish_dx(dXp, n, T, sh, dX, tail, s);
+  return finish_dx(dXp, n, T, sh, dX, tail, dx_slices, s);
 }
 
 int tpmlp_layer_norm(const void* x, int64_t T, int64_t D, tpmlp_dtype dt, float eps, void* y, tpmlp_stream_t stream) {
@@ -778,6 +841,114 @@ int tpmlp_block_backward(const void* x, const void* dout, int64_t T, const tpmlp
   const LnTail tail{x, dout, eps, static_cast<float*>(dx)};
   void* dxn = mode == TPMLP_FUSED ? at<char>(ws, b.dxn) : dx;  // FAITHFUL: the partials feed the tail directly
   return backward_impl(xn, dout, nullptr, T, sh, dxn, dA, dB, mode, at<char>(ws, b.inner), b.w.total, stream, &tail);
+}
+
+int tpmlp_all_gather(const void* const* slices, int n, int64_t slice_bytes, void* out, tpmlp_stream_t stream) {
+  if (n < 1 || n > TPMLP_MAX_SHARDS) return fail(TPMLP_ERR_ARG, "n = %d outside 1..%d", n, TPMLP_MAX_SHARDS);
+  if (slice_bytes < 0 || slice_bytes % 2 != 0)
+    return fail(TPMLP_ERR_ARG, "slice_bytes = %lld must be a non-negative multiple of 2",
+                static_cast<long long>(slice_bytes));
+  if (slice_bytes == 0) return TPMLP_OK;
+  int rc = check_slices(slices, n, "slices");
+  if (rc) return rc;
+  if (!out) return fail(TPMLP_ERR_ARG, "out must not be NULL");
+  if (!aligned16(out)) return fail(TPMLP_ERR_ALIGN, "out must be 16-byte aligned");
+  if ((rc = check_device(nullptr))) return rc;
+  InSlices in{};
+  for (int j = 0; j < n; ++j) in.p[j] = slices[j];
+  TRY_CUDA(launch_all_gather(in, n, slice_bytes, out, stream));
+  return TPMLP_OK;
+}
+
+int tpmlp_reduce_scatter(const void* Yp, int n, int64_t count, void* const* Y_slices, tpmlp_stream_t stream) {
+  if (n < 1 || n > TPMLP_MAX_SHARDS) return fail(TPMLP_ERR_ARG, "n = %d outside 1..%d", n, TPMLP_MAX_SHARDS);
+  if (count < 0) return fail(TPMLP_ERR_ARG, "count must be >= 0");
+  if (count % n != 0)
+    return fail(TPMLP_ERR_DIVISIBILITY, "count = %lld is not divisible by n = %d", static_cast<long long>(count), n);
+  if (count == 0) return TPMLP_OK;
+  if (!Yp) return fail(TPMLP_ERR_ARG, "Yp must not be NULL");
+  if (!aligned16(Yp)) return fail(TPMLP_ERR_ALIGN, "Yp must be 16-byte aligned");
+  int rc = check_slices(Y_slices, n, "Y_slices");
+  if (rc) return rc;
+  if ((rc = check_device(nullptr))) return rc;
+  OutSlices out{};
+  for (int j = 0; j < n; ++j) out.p[j] = static_cast<float*>(Y_slices[j]);
+  TRY_CUDA(launch_reduce_scatter(static_cast<const float*>(Yp), n, count, out, n, stream));
+  return TPMLP_OK;
+}
+
+size_t tpmlp_sp_workspace_bytes(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
+  if (!sh || T < 1 || T % sh->n != 0 || (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) || backward < 0 ||
+      backward > 1)
+    return 0;
+  return plan_sp(T, sh, mode, backward).total;
+}
+
+int tpmlp_forward_sp(const void* const* X_slices, int64_t T, const tpmlp_shards* sh, void* const* Y_slices,
+                     tpmlp_mode mode, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  const int n = sh->n;
+  if (n > TPMLP_MAX_SHARDS) return fail(TPMLP_ERR_UNSUPPORTED, "more than %d ranks", TPMLP_MAX_SHARDS);
+  if (T % n != 0)
+    return fail(TPMLP_ERR_DIVISIBILITY, "T = %lld is not divisible by n = %d", static_cast<long long>(T), n);
+  if ((rc = check_slices(X_slices, n, "X_slices"))) return rc;
+  if ((rc = check_slices(const_cast<const void* const*>(Y_slices), n, "Y_slices"))) return rc;
+  if (!ws) return fail(TPMLP_ERR_ARG, "workspace must not be NULL");
+  if (!aligned16(ws)) return fail(TPMLP_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const SpPlan p = plan_sp(T, sh, mode, 0);
+  if (ws_bytes < p.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, p.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  const int64_t Ts = T / n, D = sh->D;
+  InSlices in{};
+  OutSlices out{};
+  for (int j = 0; j < n; ++j) {
+    in.p[j] = X_slices[j];
+    out.p[j] = static_cast<float*>(Y_slices[j]);
+  }
+  void* X = at<char>(ws, p.x);
+  void* inner = at<char>(ws, p.inner);
+  TRY_CUDA(launch_all_gather(in, n, Ts * D * static_cast<int64_t>(esize(sh->dt)), X, stream));
+  void* H = at<char>(inner, p.w.H);
+  if ((rc = run_hidden(X, T, sh, H, stream))) return rc;
+  if (mode == TPMLP_FUSED) return run_second(H, T, sh, nullptr, 1, stream, nullptr, &out);
+  float* Yp = at<float>(inner, p.w.Yp);
+  if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
+  TRY_CUDA(launch_reduce_scatter(Yp, n, T * D, out, n, stream));
+  return TPMLP_OK;
+}
+
+int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices, int64_t T, const tpmlp_shards* sh,
+                      void* const* dX_slices, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws,
+                      size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  const int n = sh->n;
+  if (n > TPMLP_MAX_SHARDS) return fail(TPMLP_ERR_UNSUPPORTED, "more than %d ranks", TPMLP_MAX_SHARDS);
+  if (T % n != 0)
+    return fail(TPMLP_ERR_DIVISIBILITY, "T = %lld is not divisible by n = %d", static_cast<long long>(T), n);
+  if ((rc = check_slices(X_slices, n, "X_slices"))) return rc;
+  if ((rc = check_slices(dY_slices, n, "dY_slices"))) return rc;
+  if ((rc = check_slices(const_cast<const void* const*>(dX_slices), n, "dX_slices"))) return rc;
+  if (!ws) return fail(TPMLP_ERR_ARG, "workspace must not be NULL");
+  if (!aligned16(ws)) return fail(TPMLP_ERR_ALIGN, "workspace must be 16-byte aligned");
+  const SpPlan p = plan_sp(T, sh, mode, 1);
+  if (ws_bytes < p.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, p.total);
+  if ((rc = check_handle_device(sh))) return rc;
+  const int64_t slice_bytes = (T / n) * sh->D * static_cast<int64_t>(esize(sh->dt));
+  InSlices in{};
+  for (int j = 0; j < n; ++j) in.p[j] = X_slices[j];
+  TRY_CUDA(launch_all_gather(in, n, slice_bytes, at<char>(ws, p.x), stream));
+  for (int j = 0; j < n; ++j) in.p[j] = dY_slices[j];
+  TRY_CUDA(launch_all_gather(in, n, slice_bytes, at<char>(ws, p.dy), stream));
+  OutSlices out{};
+  for (int j = 0; j < n; ++j) out.p[j] = static_cast<float*>(dX_slices[j]);
+  // dX itself is never written: the partials are reduce-scattered (FAITHFUL) or
+  // the product writes the slices (FUSED); slice 0 stands in for the pointer.
+  return backward_impl(at<char>(ws, p.x), at<char>(ws, p.dy), nullptr, T, sh, dX_slices[0], dA, dB, mode,
+                       at<char>(ws, p.inner), p.w.total, stream, nullptr, &out);
 }
 
 int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* sh, void* H, int fill,

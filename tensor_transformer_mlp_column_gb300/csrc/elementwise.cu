@@ -70,13 +70,20 @@ __device__ __forceinline__ float residual1(const void* res, int res_kind, int64_
   return __bfloat162float(static_cast<const __nv_bfloat16*>(res)[j]);
 }
 
+// The output is cut into gridDim.y equal row slices (the ranks of a
+// reduce-scatter; one slice for the all-reduce): blocks with blockIdx.y = j
+// handle the `slice` elements j*slice .. (j+1)*slice - 1 and write them to
+// out.p[j].
 template <int NMAX>
 __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __restrict__ Yp, int n, int64_t count,
                                                                const void* __restrict__ res, int res_kind,
-                                                               float* __restrict__ Y) {
-  const int64_t n4 = count / 4;
+                                                               OutSlices out) {
+  const int64_t slice = count / gridDim.y;
+  const int64_t base4 = int64_t(blockIdx.y) * (slice / 4);
+  float* __restrict__ Y = out.p[blockIdx.y];
+  const int64_t n4 = slice / 4;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  const float4* P = reinterpret_cast<const float4*>(Yp);
+  const float4* P = reinterpret_cast<const float4*>(Yp) + base4;
   const int64_t shard_stride4 = count / 4;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
     float4 v[NMAX];
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
     for (int s = 0; s < NMAX; ++s)
       if (s < n) v[s] = __ldcs(P + s * shard_stride4 + i);
     float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (res_kind) r = residual4(res, res_kind, i);
+    if (res_kind) r = residual4(res, res_kind, base4 + i);
     float4 acc = v[0];
 #pragma unroll
     for (int s = 1; s < NMAX; ++s) {
@@ -105,15 +112,38 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
   }
 }
 
-// Any n and any count: the same order, shards taken from memory one by one.
+// Any n and any slice length: the same order, shards taken from memory one by one.
 __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, const void* __restrict__ res,
-                                     int res_kind, float* __restrict__ Y) {
+                                     int res_kind, OutSlices out) {
+  const int64_t slice = count / gridDim.y;
+  const int64_t base = int64_t(blockIdx.y) * slice;
+  float* __restrict__ Y = out.p[blockIdx.y];
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < count; j += stride) {
-    float acc = Yp[j];
-    for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + j];
-    Y[j] = res_kind ? residual1(res, res_kind, j) + acc : acc;
+  for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < slice; j += stride) {
+    float acc = Yp[base + j];
+    for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + base + j];
+    Y[j] = res_kind ? residual1(res, res_kind, base + j) + acc : acc;
   }
+}
+
+// ------------------------------------------------------------------ all-gather
+
+// out = the n input slices back to back (slice_bytes each), blockIdx.y = slice.
+// Each thread moves four words per pass, all four loads issued first.
+template <typename W>
+__global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__ out) {
+  const W* __restrict__ src = static_cast<const W*>(in.p[blockIdx.y]);
+  W* __restrict__ dst = out + int64_t(blockIdx.y) * words;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < words; i += 4 * stride) {
+    W w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = __ldcs(src + i + k * stride);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[i + k * stride] = w[k];
+  }
+  for (; i < words; i += stride) dst[i] = __ldcs(src + i);
 }
 
 // ------------------------------------------------------------------ shard copies
@@ -198,21 +228,54 @@ cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStre
   return cudaGetLastError();
 }
 
+cudaError_t launch_reduce_scatter(const float* Yp, int n, int64_t count, const OutSlices& out, int nslices,
+                                  cudaStream_t s, const void* res, int res_kind) {
+  if (count <= 0) return cudaSuccess;
+  if (nslices < 1 || nslices > kMaxGroups || count % nslices != 0) return cudaErrorInvalidValue;
+  if (!res) res_kind = 0;
+  const int64_t slice = count / nslices;
+  const unsigned gy = static_cast<unsigned>(nslices);
+  if (slice % 4 != 0) {  // slices would not be 16-byte aligned
+    dim3 g(static_cast<unsigned>((ew_grid(count, 1) + nslices - 1) / nslices), gy);
+    allreduce_any_kernel<<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
+    return cudaGetLastError();
+  }
+  dim3 g(static_cast<unsigned>((ew_grid(count, 4) + nslices - 1) / nslices), gy);
+  if (n <= 4)
+    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
+  else if (n <= 8)
+    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
+  else if (n <= 16)
+    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
+  else
+    allreduce_any_kernel<<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s, const void* res,
                              int res_kind) {
-  if (count <= 0) return cudaSuccess;
-  if (!res) res_kind = 0;
-  const int g = ew_grid(count, 4);
-  if (count % 4 != 0)  // shard blocks would not be 16-byte aligned
-    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
-  else if (n <= 4)
-    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
-  else if (n <= 8)
-    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
-  else if (n <= 16)
-    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
-  else
-    allreduce_any_kernel<<<ew_grid(count, 1), kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, Y);
+  OutSlices out{};
+  out.p[0] = Y;
+  return launch_reduce_scatter(Yp, n, count, out, 1, s, res, res_kind);
+}
+
+cudaError_t launch_all_gather(const InSlices& in, int nslices, int64_t slice_bytes, void* out, cudaStream_t s) {
+  if (slice_bytes <= 0) return cudaSuccess;
+  if (nslices < 1 || nslices > kMaxGroups) return cudaErrorInvalidValue;
+  const unsigned gy = static_cast<unsigned>(nslices);
+  auto gx = [&](int64_t words) {
+    return static_cast<unsigned>((ew_grid(words * nslices, 4) + nslices - 1) / nslices);
+  };
+  if (slice_bytes % 16 == 0) {
+    const int64_t w = slice_bytes / 16;
+    gather_slices_kernel<uint4><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint4*>(out));
+  } else if (slice_bytes % 4 == 0) {
+    const int64_t w = slice_bytes / 4;
+    gather_slices_kernel<uint32_t><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint32_t*>(out));
+  } else {
+    const int64_t w = slice_bytes / 2;
+    gather_slices_kernel<uint16_t><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint16_t*>(out));
+  }
   return cudaGetLastError();
 }
 

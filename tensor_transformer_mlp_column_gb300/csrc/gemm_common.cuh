@@ -34,6 +34,7 @@ struct KParams {
   int shared;      // kSharedNone / kSharedA / kSharedB: an operand that every group reads
   int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
   const __nv_bfloat16* resid;  // kEpiF32 / kEpiF32Tma: residual [M][ldo] added to the accumulator, or null
+  int64_t slice_rows;          // kEpiF32, chain: output row m goes to row m % slice_rows of out[m / slice_rows]
 };
 
 // Maps a tile index to (group, M block, N block). The tiles form a grid of
@@ -149,7 +150,10 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
       }
     }
   } else if constexpr (EPI == kEpiF32) {
-    float* out = static_cast<float*>(p.out[g]) + m * p.ldo + n0;
+    // With slice_rows, the rows are cut into rank slices, each its own buffer
+    // (the scattered output of a sequence-parallel sum; chain mode, g = 0).
+    float* out = p.slice_rows ? static_cast<float*>(p.out[m / p.slice_rows]) + (m % p.slice_rows) * p.ldo + n0
+                              : static_cast<float*>(p.out[g]) + m * p.ldo + n0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (n0 + 4 * j + 4 <= p.N)

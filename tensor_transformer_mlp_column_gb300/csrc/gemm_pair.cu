@@ -269,7 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&p.map_out[g], buf, n0, static_cast<int32_t>(m_warp));
+            // Rank slices (slice_rows % 32 == 0): the warp's 32 rows lie in one
+            // slice, whose own map takes the row within the slice.
+            const int map = p.slice_rows ? static_cast<int>(m_warp / p.slice_rows) : g;
+            const int64_t row = p.slice_rows ? m_warp % p.slice_rows : m_warp;
+            tma_store_2d(&p.map_out[map], buf, n0, static_cast<int32_t>(row));
             bulk_commit_group();
           }
           ++blocks_out;

@@ -401,11 +401,15 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.stream_out = env_int("TPMLP_STREAM_OUT", g.stream_out);
   kp.resid = static_cast<const __nv_bfloat16*>(g.resid);
   if (kp.resid && g.epi != kEpiF32) return cudaErrorInvalidValue;
+  kp.slice_rows = g.slice_rows;
+  if (g.slice_rows && (g.epi != kEpiF32 || !g.chain || g.resid)) return cudaErrorInvalidValue;
   if (!kp.status) return cudaErrorInvalidSymbol;
   if (kp.tiles == 0) return cudaSuccess;
   if (pair) {
     // Outputs with TMA maps leave the pair kernels through TMA stores.
-    const bool tma_out = g.epi == kEpiF32 && g.map_out[0] != nullptr && env_int("TPMLP_TMA_STORE", 1) != 0;
+    // (with rank slices only when no warp's 32 rows straddle two slices)
+    const bool tma_out = g.epi == kEpiF32 && g.map_out[0] != nullptr && g.slice_rows % 32 == 0 &&
+                         env_int("TPMLP_TMA_STORE", 1) != 0;
     return launch_pair(kp, tma_out ? kEpiF32Tma : g.epi, quad ? 1 : 0, s);
   }
   return BN == 256 ? launch_single_epi<256>(kp, g.epi, s) : launch_single_epi<128>(kp, g.epi, s);

@@ -56,6 +56,8 @@ struct TcGemm {
   int group_m;     // tile rows per band of the tile order (see decode_tile); 0 or 1 = columns fastest
   int stream_out;  // 1: evict-first epilogue stores
   const void* resid;  // kEpiF32 (and its TMA-store form): bf16 residual [M][ldo] added to acc, or null
+  int64_t slice_rows;  // chain == 1, kEpiF32: rows m go to out[m / slice_rows] (with output maps, one map per
+                       // slice of slice_rows rows); 0 = off
 };
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
@@ -89,10 +91,26 @@ struct SimtGemm {
 cudaError_t launch_simt_gemm(const SimtGemm& g, cudaStream_t s);
 
 cudaError_t launch_gelu(const void* x, void* y, int64_t n, int is_bf16, cudaStream_t s);
+// Pointer tables passed by value to the collective kernels (one per rank slice).
+struct OutSlices {
+  float* p[kMaxGroups];
+};
+struct InSlices {
+  const void* p[kMaxGroups];
+};
+
 // Y = ((Yp[0] + Yp[1]) + ...) + Yp[n-1], and with a residual res (res_kind 1:
 // fp32, 2: bf16) Y = res + that sum.
 cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s,
                              const void* res = nullptr, int res_kind = 0);
+// The same sum cut into nslices equal slices of count / nslices elements, slice
+// j written to out.p[j] (the simulated reduce-scatter; nslices = 1 is the
+// all-reduce).
+cudaError_t launch_reduce_scatter(const float* Yp, int n, int64_t count, const OutSlices& out, int nslices,
+                                  cudaStream_t s, const void* res = nullptr, int res_kind = 0);
+// out = in.p[0] .. in.p[nslices-1] back to back, slice_bytes each (a multiple
+// of 2; the simulated all-gather).
+cudaError_t launch_all_gather(const InSlices& in, int nslices, int64_t slice_bytes, void* out, cudaStream_t s);
 
 // Row-wise layer norm without scale or shift: y = (x - mean) / sqrt(var + eps),
 // D <= layer_norm_max_d(); x and y [T][D] of the same type.

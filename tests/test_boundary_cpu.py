@@ -144,3 +144,24 @@ def test_block_call_argument_errors(tp):
     assert l.tpmlp_block_forward(FAKE, 4, None, 1e-5, FAKE, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
     assert l.tpmlp_block_backward(FAKE, FAKE, 4, None, 1e-5, FAKE, None, None, 0, FAKE, 1 << 20,
                                   None) == tp.TPMLP_ERR_ARG
+
+
+def test_sequence_parallel_argument_errors(tp):
+    import ctypes
+
+    l = tp.lib()
+    P = ctypes.c_void_p
+    good = (P * 2)(FAKE, FAKE)
+    assert l.tpmlp_all_gather(good, 0, 32, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_all_gather(good, 17, 32, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_all_gather(good, 2, 31, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_all_gather(good, 2, 0, FAKE, None) == tp.TPMLP_OK  # nothing to copy
+    assert l.tpmlp_all_gather(None, 2, 32, FAKE, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_all_gather((P * 2)(FAKE, FAKE + 2), 2, 32, FAKE, None) == tp.TPMLP_ERR_ALIGN
+    assert l.tpmlp_all_gather(good, 2, 32, FAKE + 8, None) == tp.TPMLP_ERR_ALIGN
+    assert l.tpmlp_reduce_scatter(FAKE, 3, 16, (P * 3)(FAKE, FAKE, FAKE), None) == tp.TPMLP_ERR_DIVISIBILITY
+    assert l.tpmlp_reduce_scatter(FAKE, 2, 16, (P * 2)(FAKE, None), None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_reduce_scatter(FAKE, 2, 0, good, None) == tp.TPMLP_OK
+    assert l.tpmlp_sp_workspace_bytes(16, None, 0, 0) == 0
+    assert l.tpmlp_forward_sp(good, 16, None, good, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_backward_sp(good, good, 16, None, good, None, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
