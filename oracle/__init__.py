@@ -29,4 +29,11 @@ from .tpmlp_oracle import (  # noqa: F401
     reduce_scatter,
     tp_mlp_sp,
     tp_mlp_sp_backward,
+    softmax_rows,
+    attention_core,
+    mha,
+    shard_attention,
+    attn_shard_partial,
+    tp_attention,
+    tp_attention_rows,
 )

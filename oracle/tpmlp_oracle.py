@@ -314,3 +314,84 @@ def tp_mlp_sp_backward(X_slices, dY_slices, shards):
         dA.append(X.T @ dP_i)
         dX_parts.append(dP_i @ A_i.T)
     return reduce_scatter(dX_parts, len(X_slices)), dA, dB
+
+
+# ---------------------------------------------------------------------------
+# Head-split attention (duoan.github.io "Tensor Parallelism in Megatron-LM",
+# §4 "Attention: Split Heads"; ai-hpc.org "LLM Lab Notes 06" §2 steps 2-3):
+# with H heads of size d_h = D / H, rank i owns heads i*H/n .. (i+1)*H/n - 1,
+# i.e. columns i*D/n .. (i+1)*D/n - 1 of W^Q, W^K, W^V (column-parallel) and
+# the same rows of the output projection W^O (row-parallel). Per head and per
+# sequence of the batch, O = softmax(Q K^T / sqrt(d_h)) V with no mask; the
+# output projection's partials are summed like the MLP's.
+# X is [T, D] with T = batch * seq, sequence b occupying rows b*seq ..
+# (b+1)*seq - 1.
+# ---------------------------------------------------------------------------
+
+def softmax_rows(S):
+    """Row-wise softmax; the row maximum is subtracted first (the value is unchanged)."""
+    S = _f64(S)
+    E = np.exp(S - S.max(axis=-1, keepdims=True))
+    return E / E.sum(axis=-1, keepdims=True)
+
+
+def attention_core(Q, K, V, batch: int, heads: int):
+    """O [T, H*d_h]: for every sequence b and head h, softmax(Q_bh K_bh^T / sqrt(d_h)) V_bh."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    T, HD = Q.shape
+    if T % batch != 0 or HD % heads != 0:
+        raise ValueError("T must be divisible by batch and the width by heads")
+    s, dh = T // batch, HD // heads
+    O = np.empty_like(Q)
+    for b in range(batch):
+        r = slice(b * s, (b + 1) * s)
+        for h in range(heads):
+            c = slice(h * dh, (h + 1) * dh)
+            P = softmax_rows(Q[r, c] @ K[r, c].T / math.sqrt(dh))
+            O[r, c] = P @ V[r, c]
+    return O
+
+
+def mha(X, batch: int, Wq, Wk, Wv, Wo, heads: int):
+    """Unsplit multi-head attention: attention_core(X Wq, X Wk, X Wv) Wo."""
+    X = _f64(X)
+    return attention_core(X @ _f64(Wq), X @ _f64(Wk), X @ _f64(Wv), batch, heads) @ _f64(Wo)
+
+
+def shard_attention(Wq, Wk, Wv, Wo, heads: int, n: int):
+    """Rank i's (Wq_i, Wk_i, Wv_i, Wo_i): its heads' columns of Wq, Wk, Wv and rows of Wo."""
+    Wq, Wk, Wv, Wo = _f64(Wq), _f64(Wk), _f64(Wv), _f64(Wo)
+    D = Wq.shape[0]
+    if n <= 0 or heads % n != 0 or D % heads != 0:
+        raise ValueError(f"heads={heads} must be divisible by n={n} and D={D} by heads")
+    Dn = D // n
+    c = [slice(i * Dn, (i + 1) * Dn) for i in range(n)]
+    return [(Wq[:, c[i]], Wk[:, c[i]], Wv[:, c[i]], Wo[c[i], :]) for i in range(n)]
+
+
+def attn_shard_partial(X, batch: int, shard, local_heads: int):
+    """Rank i's work: O_i = attention over its local heads, and Y_i = O_i Wo_i. Returns (O_i, Y_i)."""
+    X = _f64(X)
+    Wq, Wk, Wv, Wo = shard
+    O = attention_core(X @ Wq, X @ Wk, X @ Wv, batch, local_heads)
+    return O, O @ Wo
+
+
+def tp_attention(X, batch: int, shards, heads: int, return_partials: bool = False):
+    """Every rank's partial, then the shard-ordered sum Y = ((Y_0 + Y_1) + ...) + Y_{n-1}."""
+    lh = heads // len(shards)
+    partials = [attn_shard_partial(X, batch, sh, lh) for sh in shards]
+    Y = partials[0][1].copy()
+    for _, Y_i in partials[1:]:
+        Y = Y + Y_i
+    if return_partials:
+        return Y, partials
+    return Y
+
+
+def tp_attention_rows(X, batch: int, shards, heads: int, seqs):
+    """The rows of tp_attention belonging to sequences `seqs` (each sequence attends only to itself)."""
+    X = _f64(X)
+    s = X.shape[0] // batch
+    rows = np.concatenate([np.arange(b * s, (b + 1) * s) for b in seqs])
+    return tp_attention(X[rows], len(seqs), shards, heads)

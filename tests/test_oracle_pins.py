@@ -465,3 +465,85 @@ def test_sequence_parallel_pins_catch_planted_mistakes():
     assert not np.allclose(oracle.all_gather(swapped), partials[0] + partials[1])
     # a reduce-scatter that drops a partial
     assert not np.allclose(oracle.split_rows(partials[0], n)[0], rs[0])
+
+
+# ---------------------------------------------------------------- head-split attention
+
+def test_attention_core_against_torch_sdpa():
+    import torch
+
+    rng = np.random.default_rng(30)
+    batch, s, heads, dh = 2, 5, 3, 4
+    Q, K, V = (rng.normal(size=(batch * s, heads * dh)) for _ in range(3))
+    O = oracle.attention_core(Q, K, V, batch, heads)
+
+    def bhsd(M):  # [T, H*dh] -> [batch, heads, s, dh]
+        return torch.from_numpy(M).reshape(batch, s, heads, dh).permute(0, 2, 1, 3)
+
+    ref = torch.nn.functional.scaled_dot_product_attention(bhsd(Q), bhsd(K), bhsd(V))
+    ref = ref.permute(0, 2, 1, 3).reshape(batch * s, heads * dh).numpy()
+    np.testing.assert_allclose(O, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_attention_closed_forms():
+    rng = np.random.default_rng(31)
+    s, dh = 6, 4
+    Q, V = rng.normal(size=(s, dh)), rng.normal(size=(s, dh))
+    # identical keys: uniform weights, every output row is the mean of V
+    K = np.tile(rng.normal(size=(1, dh)), (s, 1))
+    np.testing.assert_allclose(oracle.attention_core(Q, K, V, 1, 1), np.tile(V.mean(axis=0), (s, 1)), rtol=1e-13)
+    # identical values: the output is that row whatever the weights
+    Vc = np.tile(V[:1], (s, 1))
+    np.testing.assert_allclose(oracle.attention_core(Q, rng.normal(size=(s, dh)), Vc, 1, 1), Vc, rtol=1e-13)
+    # a one-token sequence attends only to itself
+    np.testing.assert_allclose(oracle.attention_core(Q[:1], Q[1:2], V[:1], 1, 1), V[:1], rtol=1e-14)
+    # softmax rows sum to one and are shift-invariant; 1/sqrt(d_h) scales the logits
+    S = rng.normal(size=(3, 7))
+    np.testing.assert_allclose(oracle.softmax_rows(S).sum(axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(oracle.softmax_rows(S + 5.0), oracle.softmax_rows(S), rtol=1e-13)
+    q, k, v = rng.normal(size=(2, 16)), rng.normal(size=(2, 16)), rng.normal(size=(2, 16))
+    w = np.exp(q @ k.T / 4.0)  # d_h = 16: logits divided by 4
+    np.testing.assert_allclose(oracle.attention_core(q, k, v, 1, 1), (w / w.sum(axis=1, keepdims=True)) @ v,
+                               rtol=1e-13)
+    # sequences of a batch do not see each other
+    Q2, K2, V2 = rng.normal(size=(4, dh)), rng.normal(size=(4, dh)), rng.normal(size=(4, dh))
+    both = oracle.attention_core(Q2, K2, V2, 2, 1)
+    np.testing.assert_allclose(both[2:], oracle.attention_core(Q2[2:], K2[2:], V2[2:], 1, 1), rtol=1e-14)
+
+
+def test_head_split_attention_equals_unsplit_for_every_divisor():
+    rng = np.random.default_rng(32)
+    batch, s, D, heads = 2, 4, 12, 6
+    X = rng.normal(size=(batch * s, D))
+    W = [rng.normal(size=(D, D)) * 0.3 for _ in range(4)]
+    ref = oracle.mha(X, batch, *W, heads)
+    for n in (1, 2, 3, 6):
+        shards = oracle.shard_attention(*W, heads, n)
+        Y, parts = oracle.tp_attention(X, batch, shards, heads, return_partials=True)
+        np.testing.assert_allclose(Y, ref, rtol=1e-12, atol=1e-13)
+        # the ranks' head outputs side by side are the unsplit heads (the all-gather of ai-hpc.org §2)
+        O_full = oracle.attention_core(X @ W[0], X @ W[1], X @ W[2], batch, heads)
+        np.testing.assert_allclose(np.concatenate([O for O, _ in parts], axis=1), O_full, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(oracle.tp_attention_rows(X, batch, oracle.shard_attention(*W, heads, 2), heads, [1]),
+                               ref[s:], rtol=1e-12, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle.shard_attention(*W, heads, 4)
+
+
+def test_attention_pins_catch_planted_mistakes():
+    rng = np.random.default_rng(33)
+    batch, s, heads, dh = 1, 5, 2, 4
+    Q, K, V = (rng.normal(size=(s, heads * dh)) for _ in range(3))
+    ref = oracle.attention_core(Q, K, V, batch, heads)
+    c = slice(0, dh)
+    no_scale = oracle.softmax_rows(Q[:, c] @ K[:, c].T) @ V[:, c]
+    wrong_axis = oracle.softmax_rows((Q[:, c] @ K[:, c].T / 2.0).T).T @ V[:, c]
+    assert np.max(np.abs(no_scale - ref[:, c])) > 1e-3 and np.max(np.abs(wrong_axis - ref[:, c])) > 1e-3
+    # a rank taking every n-th column instead of a contiguous block of heads
+    D, n = 8, 2
+    W = [rng.normal(size=(D, D)) for _ in range(4)]
+    X = rng.normal(size=(3, D))
+    good = oracle.tp_attention(X, 1, oracle.shard_attention(*W, 2, n), 2)
+    bad_shards = [(W[0][:, i::n], W[1][:, i::n], W[2][:, i::n], W[3][i::n, :]) for i in range(n)]
+    bad = oracle.tp_attention(X, 1, bad_shards, 2)
+    assert np.max(np.abs(bad - good)) > 1e-3

@@ -17,6 +17,12 @@ scratchllm.com "Tensor-Parallel MLP (Megatron)", section "The problem"):
   large       T=16384, D=4096, F=16384, N=8  bf16   X~N(0,1), A,B~N(0,0.02)
   fwd_bwd     T=8192,  D=8192, F=32768, N=8  bf16   X~N(0,1), A,B~N(0,0.01), dY~N(0,1)
 
+Attention workloads (ATTN_WORKLOADS: batch x seq tokens, D, heads, N ranks;
+duoan.github.io "Tensor Parallelism in Megatron-LM" §4): attn_tiny_fp32
+(2 x 16, D=64, 4 heads, N=2, W~N(0,1/8)) and attn_seq{128,256,512} (8 x seq,
+D=1024, 16 heads of 64, N=4, bf16, X~N(0,1), W~N(0,0.02)); X uses seed+0,
+Wq..Wo seeds +1..+4.
+
 "N(0, s)" means a normal with standard deviation s. Each tensor gets its own
 CPU torch.Generator: X uses seed+0, A seed+1, B seed+2, dY seed+3. Values are
 drawn in float32, scaled, then rounded once to the workload's dtype; the
@@ -114,6 +120,57 @@ def make_block_inputs(w: Workload, seed: int = 0, with_dout: bool | None = None)
     out = {"x": x, "A": inp["A"], "B": inp["B"]}
     if "dY" in inp:
         out["dout"] = inp["dY"]
+    return out
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Head-split attention: X [batch*seq, D], Wq, Wk, Wv, Wo [D, D], `heads`
+    heads of D/heads, N ranks (heads divisible by N)."""
+
+    name: str
+    batch: int
+    seq: int
+    D: int
+    heads: int
+    N: int
+    dtype: str  # "f32" or "bf16"
+    x_std: float
+    w_std: float
+
+    @property
+    def T(self) -> int:
+        return self.batch * self.seq
+
+    @property
+    def dh(self) -> int:
+        return self.D // self.heads
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def fwd_flops(self) -> float:
+        """QKV projection 6 T D^2, scores and weighted values 4 batch seq^2 D, output projection 2 T D^2."""
+        return 8.0 * self.T * self.D * self.D + 4.0 * self.batch * self.seq * self.seq * self.D
+
+
+# The attention counterpart of the sequence sweep: batch 8, D=1024 with
+# GPT-2's head size of 64 (16 heads), 4 ranks; and a tiny fp32 case.
+ATTN_WORKLOADS: dict[str, AttnWorkload] = {
+    "attn_tiny_fp32": AttnWorkload("attn_tiny_fp32", 2, 16, 64, 4, 2, "f32", 1.0, 0.125),
+    "attn_seq128": AttnWorkload("attn_seq128", 8, 128, 1024, 16, 4, "bf16", 1.0, 0.02),
+    "attn_seq256": AttnWorkload("attn_seq256", 8, 256, 1024, 16, 4, "bf16", 1.0, 0.02),
+    "attn_seq512": AttnWorkload("attn_seq512", 8, 512, 1024, 16, 4, "bf16", 1.0, 0.02),
+}
+
+
+def make_attn_inputs(w: AttnWorkload, seed: int = 0) -> dict[str, torch.Tensor]:
+    """X [T, D] (seed+0) and Wq, Wk, Wv, Wo [D, D] (seeds +1..+4) in w's dtype."""
+    dt = w.torch_dtype
+    out = {"X": _draw((w.T, w.D), w.x_std, seed, dt)}
+    for k, name in enumerate(("Wq", "Wk", "Wv", "Wo")):
+        out[name] = _draw((w.D, w.D), w.w_std, seed + 1 + k, dt)
     return out
 
 
