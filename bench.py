@@ -639,6 +639,47 @@ def bench_sp(args, local_rank, peaks):
     return out
 
 
+def bench_attention(args, local_rank, peaks):
+    """Head-split attention over the sequence sweep (batch 8, seq 128/256/512,
+    D=1024, 16 heads of 64, N=4): the whole forward in both modes and the
+    local heads alone (QKV projection, V^T, attention), with the attention
+    core's FLOP (4 batch seq^2 D) growing quadratically in seq."""
+    import torch
+
+    import tensor_transformer_mlp_column_gb300 as tp
+    from tpmlp_inputs import ATTN_WORKLOADS, make_attn_inputs
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for name in ("attn_seq128", "attn_seq256", "attn_seq512"):
+        w = ATTN_WORKLOADS[name]
+        inp = make_attn_inputs(w, seed=0)
+        d = {k: v.to(dev) for k, v in inp.items()}
+        sh = tp.tpmlp_attn_shard(d["Wq"], d["Wk"], d["Wv"], d["Wo"], w.heads, w.N)
+        Y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+        O = torch.empty((w.N, w.T, w.D // w.N), dtype=torch.bfloat16, device=dev)
+        res = {"batch": w.batch, "seq": w.seq, "D": w.D, "heads": w.heads, "N": w.N}
+        ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, None), dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: tp.tpmlp_attn_heads(d["X"], w.batch, sh, O, ws), dev, stream, 50, 5)
+        res["heads_ms"] = round(ms, 4)
+        for mode in ("faithful", "fused"):
+            ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, mode), dtype=torch.uint8, device=dev)
+            ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, stream, 50, 5)
+            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
+        tp.tpmlp_check_status(stream)
+        sh.free()
+        out[name] = res
+    # heads time against seq: least squares on (1, seq, seq^2)
+    import numpy as np
+
+    seqs = np.array([128.0, 256.0, 512.0])
+    ys = np.array([out[f"attn_seq{int(s)}"]["heads_ms"] for s in seqs])
+    coef = np.linalg.solve(np.stack([np.ones(3), seqs, seqs ** 2], axis=1), ys)
+    out["heads_ms_fit"] = {"c0": round(float(coef[0]), 5), "c1_per_seq": float(coef[1]), "c2_per_seq2": float(coef[2])}
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -774,6 +815,7 @@ def main():
         line["gelu"] = bench_gelu(local_rank, peaks)
         line["block"] = bench_block(args, local_rank, peaks)
         line["sequence_parallel"] = bench_sp(args, local_rank, peaks)
+        line["attention"] = bench_attention(args, local_rank, peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline()
     print(json.dumps(line))

@@ -325,6 +325,55 @@ int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices,
                       const tpmlp_shards* shards, void* const* dX_slices, void* const* dA, void* const* dB,
                       tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * Head-split attention ([P3] §4 "Attention: Split Heads"; [P1] §2 steps 2-3):
+ * H heads of size d_h = D / H; rank i owns heads i*H/n .. (i+1)*H/n - 1,
+ * i.e. columns i*D/n .. (i+1)*D/n - 1 of Wq, Wk, Wv [D, D] (column-parallel)
+ * and the same rows of Wo [D, D] (row-parallel). X [T, D] holds `batch`
+ * sequences of `seq` tokens (sequence b in rows b*seq .. (b+1)*seq - 1):
+ *   Q_i = X Wq_i, K_i = X Wk_i, V_i = X Wv_i,
+ *   O_i = softmax(Q_i K_i^T / sqrt(d_h)) V_i per sequence and local head
+ *         (no mask),
+ *   Y   = sum_i O_i Wo_i, summed like the MLP's partials.
+ * bf16: d_h = 64, seq % 8 == 0; fp32: d_h <= 128; both: seq <= 512.
+ * ---------------------------------------------------------------------- */
+
+typedef struct tpmlp_attn_shards tpmlp_attn_shards;
+
+/* Builds the ranks' weights on the current device (enqueued on `stream`).
+ *   Wq, Wk, Wv, Wo  device [D, D] of type dt, read only.
+ *   heads           H; D % H == 0 and H % n == 0 (TPMLP_ERR_DIVISIBILITY).
+ *   n               1 .. TPMLP_MAX_SHARDS ranks.
+ * Layout per rank, bf16: [Wq_i | Wk_i | Wv_i]^T [3D/n, D] and Wo_i^T
+ * [D, D/n] (K-major operands of the tensor cores); fp32: [Wq_i | Wk_i | Wv_i]
+ * [D, 3D/n] and Wo_i [D/n, D]. TPMLP_ERR_UNSUPPORTED for a bf16 head size
+ * other than 64 or an fp32 head size above 128. */
+int tpmlp_attn_shard(const void* Wq, const void* Wk, const void* Wv, const void* Wo, int64_t D, int heads, int n,
+                     tpmlp_dtype dt, tpmlp_stream_t stream, tpmlp_attn_shards** out);
+
+/* Rank i's two weight blocks in the layout above (owned by the handle). */
+int tpmlp_attn_shard_get(const tpmlp_attn_shards* shards, int i, const void** Wqkv_i, const void** Wo_i);
+
+/* Synchronises the handle's device and frees the handle (NULL is a no-op). */
+void tpmlp_attn_shards_free(tpmlp_attn_shards* shards);
+
+/* Workspace bytes of tpmlp_attn_forward in `mode` (TPMLP_FAITHFUL or
+ * TPMLP_FUSED), or of tpmlp_attn_heads for mode = -1; 0 on bad arguments. */
+size_t tpmlp_attn_workspace_bytes(int64_t batch, int64_t seq, const tpmlp_attn_shards* shards, int mode);
+
+/* Every rank's local heads: O device [n][T][D/n] of the handle's dtype, rank
+ * i's block at O + i*T*D/n, head h of the rank in its columns h*d_h ..
+ * (h+1)*d_h - 1. workspace: tpmlp_attn_workspace_bytes(batch, seq, shards, -1). */
+int tpmlp_attn_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards* shards, void* O,
+                     void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
+/* Y = sum_i O_i Wo_i, device [T, D] fp32. FAITHFUL: the partials O_i Wo_i,
+ * then the shard-ordered reduce of tpmlp_allreduce; FUSED: their on-chip
+ * shard-ordered sum. workspace: tpmlp_attn_workspace_bytes(batch, seq,
+ * shards, mode). */
+int tpmlp_attn_forward(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards* shards, void* Y,
+                       tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
+
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit
  * of limit_ms milliseconds (1..10000). The block then stops and records

@@ -68,6 +68,12 @@ SIGNATURES = {
     "tpmlp_block_backward": (_I, [_P, _P, _I64, _P, ctypes.c_float, _P, ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P,
                                   _SZ, _P]),
     "tpmlp_all_gather": (_I, [ctypes.POINTER(_P), _I, _I64, _P, _P]),
+    "tpmlp_attn_shard": (_I, [_P, _P, _P, _P, _I64, _I, _I, _I, _P, ctypes.POINTER(_P)]),
+    "tpmlp_attn_shard_get": (_I, [_P, _I, ctypes.POINTER(_P), ctypes.POINTER(_P)]),
+    "tpmlp_attn_shards_free": (None, [_P]),
+    "tpmlp_attn_workspace_bytes": (_SZ, [_I64, _I64, _P, _I]),
+    "tpmlp_attn_heads": (_I, [_P, _I64, _I64, _P, _P, _P, _SZ, _P]),
+    "tpmlp_attn_forward": (_I, [_P, _I64, _I64, _P, _P, _I, _P, _SZ, _P]),
     "tpmlp_reduce_scatter": (_I, [_P, _I, _I64, ctypes.POINTER(_P), _P]),
     "tpmlp_sp_workspace_bytes": (_SZ, [_I64, _P, _I, _I]),
     "tpmlp_forward_sp": (_I, [ctypes.POINTER(_P), _I64, _P, ctypes.POINTER(_P), _I, _P, _SZ, _P]),
@@ -438,6 +444,75 @@ def tpmlp_backward_sp(X_slices: Sequence[torch.Tensor], dY_slices: Sequence[torc
                                    ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
            "tpmlp_backward_sp")
     return list(dX_slices), dA, dB
+
+
+class AttnShards:
+    """Handle of head-split attention weights (tpmlp_attn_shard)."""
+
+    def __init__(self, handle, D: int, heads: int, n: int, dtype: torch.dtype, device):
+        self.handle = handle
+        self.D, self.heads, self.n, self.dtype, self.device = D, heads, n, dtype, device
+        self.Dn = D // n
+        self.dh = D // heads
+
+    def get(self, i: int):
+        """Rank i's (Wqkv_i, Wo_i) as tensors aliasing the handle's memory (layouts in tpmlp.h)."""
+        a, b = ctypes.c_void_p(), ctypes.c_void_p()
+        _check(lib().tpmlp_attn_shard_get(self.handle, i, ctypes.byref(a), ctypes.byref(b)), "tpmlp_attn_shard_get")
+        if self.dtype == torch.bfloat16:
+            return _alias(a.value, (3 * self.Dn, self.D), self.dtype), _alias(b.value, (self.D, self.Dn), self.dtype)
+        return _alias(a.value, (self.D, 3 * self.Dn), self.dtype), _alias(b.value, (self.Dn, self.D), self.dtype)
+
+    def free(self):
+        if self.handle:
+            lib().tpmlp_attn_shards_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def tpmlp_attn_shard(Wq, Wk, Wv, Wo, heads: int, n: int, stream=None) -> AttnShards:
+    """Split Wq, Wk, Wv by columns and Wo by rows into n ranks of heads/n heads each."""
+    D = Wq.shape[0]
+    h = ctypes.c_void_p()
+    _check(lib().tpmlp_attn_shard(_dev(Wq, "Wq"), _dev(Wk, "Wk"), _dev(Wv, "Wv"), _dev(Wo, "Wo"), D, heads, n,
+                                  _dt(Wq), _stream(stream), ctypes.byref(h)), "tpmlp_attn_shard")
+    return AttnShards(h.value, D, heads, n, Wq.dtype, Wq.device)
+
+
+def tpmlp_attn_workspace_bytes(batch: int, seq: int, shards: AttnShards, mode="faithful") -> int:
+    m = -1 if mode is None else _mode(mode)
+    return int(lib().tpmlp_attn_workspace_bytes(batch, seq, shards.handle, m))
+
+
+def tpmlp_attn_heads(X: torch.Tensor, batch: int, shards: AttnShards, O: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Every rank's local attention heads: O [n, T, D/n] of X's dtype."""
+    T = X.shape[0]
+    seq = T // batch
+    O = torch.empty((shards.n, T, shards.Dn), dtype=X.dtype, device=X.device) if O is None else O
+    ws = _workspace(tpmlp_attn_workspace_bytes(batch, seq, shards, None), workspace)
+    _check(lib().tpmlp_attn_heads(_dev(X, "X"), batch, seq, shards.handle, _dev(O, "O"), ws.data_ptr(),
+                                  ws.numel() * ws.element_size(), _stream(stream)), "tpmlp_attn_heads")
+    return O
+
+
+def tpmlp_attn_forward(X: torch.Tensor, batch: int, shards: AttnShards, mode="faithful",
+                       Y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Y = sum_i O_i Wo_i, fp32 [T, D]."""
+    T = X.shape[0]
+    seq = T // batch
+    Y = torch.empty((T, shards.D), dtype=torch.float32, device=X.device) if Y is None else Y
+    ws = _workspace(tpmlp_attn_workspace_bytes(batch, seq, shards, mode), workspace)
+    _check(lib().tpmlp_attn_forward(_dev(X, "X"), batch, seq, shards.handle, _dev(Y, "Y"), _mode(mode),
+                                    ws.data_ptr(), ws.numel() * ws.element_size(), _stream(stream)),
+           "tpmlp_attn_forward")
+    return Y
 
 
 def tpmlp_selftest_gemm_withheld_fill(X: torch.Tensor, shards: Shards, H: torch.Tensor, fill: int, limit_ms: int,

@@ -128,7 +128,21 @@ __device__ __forceinline__ void add_residual(const uint4 (&r)[4], float (&v)[32]
 
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
-  if constexpr (EPI == kEpiGeluBf16 || EPI == kEpiGeluSaveP) {
+  if constexpr (EPI == kEpiBf16) {
+    // acc rounded to bf16, row-major.
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (n0 + 8 * j + 8 <= p.N) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        store16(out + 8 * j, w, p.stream_out);
+      }
+    }
+  } else if constexpr (EPI == kEpiGeluBf16 || EPI == kEpiGeluSaveP) {
     // H = GeLU(acc), bf16, row-major (and, saving P, acc itself in fp32).
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
 #pragma unroll

@@ -353,6 +353,8 @@ cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
       return launch_impl<kEpiF32Tma, 6, QUAD>(kp, s);
     case kEpiGeluSaveP:
       return launch_impl<kEpiGeluSaveP, 6, QUAD>(kp, s);
+    case kEpiBf16:
+      return launch_impl<kEpiBf16, 6, QUAD>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }

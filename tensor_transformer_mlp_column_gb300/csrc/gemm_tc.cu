@@ -245,6 +245,8 @@ cudaError_t launch_single_epi(const KParams& kp, int epi, cudaStream_t s) {
       return launch_single<BN, kEpiBwdAct>(kp, s);
     case kEpiGeluSaveP:
       return launch_single<BN, kEpiGeluSaveP>(kp, s);
+    case kEpiBf16:
+      return launch_single<BN, kEpiBf16>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }
@@ -298,6 +300,8 @@ int* status_word() {
 }
 
 }  // namespace
+
+int* device_status_word() { return status_word(); }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);

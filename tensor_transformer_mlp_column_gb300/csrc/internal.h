@@ -26,6 +26,7 @@ enum TcEpilogue : int {
   kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), aux_ht = GeLU(P)^T, aux_dpt = out^T (P from aux_p)
   kEpiF32Tma = 3,    // out fp32 = acc through TMA stores (chosen by the launcher when map_out is given)
   kEpiGeluSaveP = 4, // out bf16 = GeLU(acc) and out2 fp32 = acc (the pre-activation), same row stride
+  kEpiBf16 = 5,      // out bf16 = acc
 };
 
 enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
@@ -144,6 +145,26 @@ cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int
 cudaError_t launch_bwd_act_f32(const float* P, float* H, float* dH, int64_t count, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+
+// Attention of head-split tensor parallelism (attention.cu), per rank i:
+// O_i = softmax(Q K^T / sqrt(d_h)) V for each of its local heads and each
+// sequence, Q, K, V from the rank's QKV projection. Tensor-core form: bf16,
+// d_h = 64, seq <= 512 and seq % 8 == 0; V read from its transpose.
+struct AttnLaunch {
+  const CUtensorMap* map_qkv[kMaxGroups];  // QKV_i [T, 3 Dn] bf16, 64 x 128 boxes (make_operand_map, 128 rows)
+  const CUtensorMap* map_vt[kMaxGroups];   // V_i^T [Dn, T] bf16, 64 x 64 boxes (make_operand_map, 64 rows)
+  void* out[kMaxGroups];                   // O_i [T, Dn] bf16
+  int n, batch, seq, Dn, local_heads;
+  uint64_t wait_ns;
+  int* status;
+};
+cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s);
+// fp32 form on the CUDA cores: qkv [n][T][3 Dn], out [n][T][Dn]; d_h <= 128, seq <= 512.
+cudaError_t launch_attention_f32(const float* qkv, int64_t T, int n, int Dn, int dh, int local_heads, int batch,
+                                 int seq, float* out, cudaStream_t s);
+
+// Device address of the status word that bounded waits write on this device.
+int* device_status_word();
 
 // Reads and clears the device status word.
 cudaError_t read_and_clear_status(int* value, cudaStream_t s);

@@ -165,3 +165,23 @@ def test_sequence_parallel_argument_errors(tp):
     assert l.tpmlp_sp_workspace_bytes(16, None, 0, 0) == 0
     assert l.tpmlp_forward_sp(good, 16, None, good, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
     assert l.tpmlp_backward_sp(good, good, 16, None, good, None, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+
+
+def test_attention_argument_errors_without_gpu(tp):
+    import ctypes
+
+    l = tp.lib()
+    h = ctypes.c_void_p()
+    assert l.tpmlp_attn_shard(FAKE, FAKE, FAKE, FAKE, 128, 2, 2, 1, None, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_attn_shard(None, FAKE, FAKE, FAKE, 128, 2, 2, 1, None, ctypes.byref(h)) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_attn_shard(FAKE, FAKE, FAKE, FAKE, 128, 3, 1, 1, None, ctypes.byref(h)) == tp.TPMLP_ERR_DIVISIBILITY
+    assert l.tpmlp_attn_shard(FAKE, FAKE, FAKE, FAKE, 128, 2, 4, 1, None, ctypes.byref(h)) == tp.TPMLP_ERR_DIVISIBILITY
+    assert l.tpmlp_attn_shard(FAKE, FAKE, FAKE, FAKE, 128, 4, 2, 1, None, ctypes.byref(h)) == tp.TPMLP_ERR_UNSUPPORTED
+    assert l.tpmlp_attn_shard(FAKE, FAKE, FAKE, FAKE, 1024, 32, 32, 1, None,
+                              ctypes.byref(h)) == tp.TPMLP_ERR_UNSUPPORTED
+    assert l.tpmlp_attn_shard(FAKE + 2, FAKE, FAKE, FAKE, 128, 2, 2, 1, None, ctypes.byref(h)) == tp.TPMLP_ERR_ALIGN
+    assert l.tpmlp_attn_workspace_bytes(2, 8, None, 0) == 0
+    assert l.tpmlp_attn_heads(FAKE, 2, 8, None, FAKE, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_attn_forward(FAKE, 2, 8, None, FAKE, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+    assert l.tpmlp_attn_shard_get(None, 0, None, None) == tp.TPMLP_ERR_ARG
+    l.tpmlp_attn_shards_free(None)
