@@ -691,8 +691,20 @@ def main():
     ap.add_argument("--N", type=int, default=0, help="override the shard count (experiments)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement (fwd+bwd workload)")
+    ap.add_argument("--only", choices=["backward", "gelu", "block", "sp", "attention", "small"], default=None,
+                    help="run one secondary measurement alone and print it (smaller profiling commands)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.only:
+        import torch
+
+        torch.cuda.set_device(0)
+        peaks = load_peaks()
+        fn = {"backward": lambda: bench_backward(args, 0, peaks), "gelu": lambda: bench_gelu(0, peaks),
+              "block": lambda: bench_block(args, 0, peaks), "sp": lambda: bench_sp(args, 0, peaks),
+              "attention": lambda: bench_attention(args, 0, peaks), "small": lambda: bench_small_workloads(0)}
+        print(json.dumps({"only": args.only, args.only: fn[args.only]()}))
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
