@@ -5,18 +5,21 @@
 // its transpose V^T [D/n, T], and writing O into the rank's [T, D/n] block.
 //
 // Tensor-core kernel (bf16, d_h = 64, seq <= 512, seq % 8 == 0): one CTA of
-// four warps per (128-query tile, head, sequence).
+// 16 warps per (128-query tile, head, sequence).
 //   thread 0 : TMA-loads the Q tile, all keys and all of V^T for the head
 //              into 128-byte-swizzled shared memory (one mbarrier), then
 //              issues S = Q K^T (M=128, N=128 per key block, K=16 steps)
 //              into tensor memory: the whole score row, up to 512 columns
-//   all 128  : thread r owns query row r (TMEM lane r): one pass over its
-//              scores for the row maximum, a second for p = 2^((s - max) *
-//              log2(e) / sqrt(d_h)) and their fp32 sum, writing p as bf16
-//              into shared memory in the 128-byte-swizzled K-major layout of
-//              an MMA operand; then O (+)= P V^T-chunk (M=128, N=64) into
-//              TMEM columns 0..63, in phases of 256 keys (P buffer of
-//              64 KB); finally O / sum rounded to bf16.
+//   16 warps : warp w reads TMEM lanes 32 (w % 4) .. (its query rows) and
+//              column quarter w / 4 of the scores: one pass for the maximum,
+//              a second for p = 2^((s - max) * log2(e) / sqrt(d_h)) and its
+//              fp32 sum, writing p as bf16 into shared memory in the
+//              128-byte-swizzled K-major layout of an MMA operand (chunks
+//              4..7 reuse the key buffer, dead once S is computed); the four
+//              quarters' maxima and sums meet in shared memory. Then
+//              O = P V (M=128, N=64, one chunk of 64 keys per 4 MMAs) into
+//              TMEM columns 0..63, and O / sum rounded to bf16, each warp
+//              writing 16 of the 64 columns of its rows.
 // The softmax is exact (the full row is in tensor memory), not the running
 // rescale of a streaming kernel. Every wait is bounded; on a timeout the CTA
 // records the site, drains its copies and MMAs and frees its tensor memory.
@@ -30,12 +33,13 @@ namespace tpmlp {
 
 namespace {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 512;  // 16 warps: 4 TMEM lane quarters x 4 column groups
+constexpr int kF32Threads = 128;   // fp32 kernel: 4 warps, one query row each
 constexpr uint32_t kQBytes = 128 * 128;       // 128 query rows x 64 bf16
 constexpr uint32_t kKBlockBytes = 128 * 128;  // 128 key rows x 64 bf16
 constexpr uint32_t kVtChunkBytes = 64 * 128;  // 64 d-rows x 64 keys
 constexpr uint32_t kPChunkBytes = 128 * 128;  // 128 query rows x 64 keys
-constexpr int kPhaseChunks = 4;               // P chunks per phase (256 keys)
+constexpr int kPhaseChunks = 4;               // P chunks in the P buffer; the rest reuse the key buffer
 
 struct AttnParams {
   CUtensorMap map_qkv[kMaxGroups];  // QKV_i [T, 3 Dn] bf16, boxes 64 x 128
@@ -54,7 +58,28 @@ __device__ __forceinline__ uint32_t pack2_bf16(float a, float b) {
 
 __host__ __device__ constexpr uint32_t attn_smem_bytes(int nkv, int nch) {
   return 1024 + kQBytes + uint32_t(nkv) * kKBlockBytes + uint32_t(nch) * kVtChunkBytes +
-         uint32_t(nch < kPhaseChunks ? nch : kPhaseChunks) * kPChunkBytes + 64;
+         uint32_t(nch < kPhaseChunks ? nch : kPhaseChunks) * kPChunkBytes + 2 * 4 * 128 * 4 + 64;
+}
+
+// 16 consecutive 32-bit TMEM columns of this warp's 32 lanes.
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory address of P chunk c (64 keys x 128 query rows): chunks 0..3
+// in the P buffer, chunks 4..7 in the key buffer, free once S is computed.
+__device__ __forceinline__ uint8_t* p_chunk(uint8_t* sP, uint8_t* sK, int c) {
+  return c < kPhaseChunks ? sP + c * kPChunkBytes : sK + (c - kPhaseChunks) * kPChunkBytes;
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
@@ -66,7 +91,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   uint8_t* sK = sQ + kQBytes;
   uint8_t* sVt = sK + nkv * kKBlockBytes;
   uint8_t* sP = sVt + nch * kVtChunkBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + (nch < kPhaseChunks ? nch : kPhaseChunks) * kPChunkBytes);
+  float* red_max = reinterpret_cast<float*>(sP + (nch < kPhaseChunks ? nch : kPhaseChunks) * kPChunkBytes);  // [4][128]
+  float* red_sum = red_max + 4 * 128;                                                                         // [4][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 4 * 128);
   uint64_t* bar_load = bars;
   uint64_t* bar_mma = bars + 1;
   uint64_t* bar_drain = bars + 2;
@@ -75,7 +102,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / p.local_heads, hl = gh % p.local_heads;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3;      // TMEM lanes (= query rows) 32*quarter .. +31
+  const int cgroup = warp >> 2;      // column group 0..3 of the score row
+  const int row = quarter * 32 + lane;
   const uint32_t tmem_cols = nkv <= 1 ? 128u : (nkv <= 2 ? 256u : 512u);
 
   if (tid == 0) {
@@ -102,7 +132,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
     for (int c = 0; c < nch; ++c) tma_load_2d(sVt + c * kVtChunkBytes, mv, row0 + c * 64, hl * 64, bar_load);
   }
   bool ok = wait_bounded(bar_load, 0, guard, kSiteProducer);
-  uint32_t mma_phase = 0;
   if (ok && tid == 0) {
     tc_fence_after_sync();
     const uint64_t dq = smem_desc_sw128(smem_addr(sQ));
@@ -114,93 +143,85 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
     }
     tc_commit(bar_mma);
   }
-  ok = ok && wait_bounded(bar_mma, mma_phase, guard, kSiteMmaFull);
-  mma_phase ^= 1u;
+  ok = ok && wait_bounded(bar_mma, 0, guard, kSiteMmaFull);
 
-  // ---- softmax: thread tid owns query row tid (TMEM lane tid)
+  // ---- softmax: warp (quarter, cgroup) owns rows 32*quarter.. and a quarter
+  // of the score columns; the row's maximum and sum combine the four groups.
   tc_fence_after_sync();
-  const uint32_t t_row = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const uint32_t t_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const int gcols = nkv * 32;  // columns per group (a multiple of 32)
+  const int col0 = cgroup * gcols;
   float mx = -INFINITY;
   if (ok) {
-    for (int g = 0; g < nkv * 4; ++g) {
+    for (int g = 0; g < gcols; g += 32) {
       float v[32];
-      tmem_ld_32cols(t_row + g * 32, v);
+      tmem_ld_32cols(t_row + col0 + g, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (g * 32 + j < p.seq) mx = fmaxf(mx, v[j]);
+        if (col0 + g + j < p.seq) mx = fmaxf(mx, v[j]);
     }
   }
+  red_max[cgroup * 128 + row] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(red_max[row], red_max[128 + row]), fmaxf(red_max[256 + row], red_max[384 + row]));
   const float mb = mx * p.scale_log2;
   float sum = 0.f;
-  for (int ph = 0; ph * kPhaseChunks < nch; ++ph) {
-    if (ph > 0) {  // the previous phase's products must have read P before it is overwritten
-      ok = ok && wait_bounded(bar_mma, mma_phase, guard, kSiteMmaAcc);
-      mma_phase ^= 1u;
-    }
-    const int c0 = ph * kPhaseChunks;
-    const int c1 = (c0 + kPhaseChunks < nch) ? c0 + kPhaseChunks : nch;
-    if (ok) {
-      for (int c = c0; c < c1; ++c) {
-        uint8_t* prow = sP + (c - c0) * kPChunkBytes + tid * 128;
+  if (ok) {
+    for (int g = 0; g < gcols; g += 32) {
+      const int col = col0 + g;  // first of 32 columns: half (col % 64) / 32 of chunk col / 64
+      if (col >= nch * 64) break;
+      float v[32];
+      tmem_ld_32cols(t_row + col, v);
+      uint32_t w[16];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float v[32];
-          tmem_ld_32cols(t_row + c * 64 + half * 32, v);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int col = c * 64 + half * 32 + j;
-            const float e0 = col < p.seq ? exp2f(fmaf(v[j], p.scale_log2, -mb)) : 0.f;
-            const float e1 = col + 1 < p.seq ? exp2f(fmaf(v[j + 1], p.scale_log2, -mb)) : 0.f;
-            sum += e0 + e1;
-            w[j / 2] = pack2_bf16(e0, e1);
-          }
-          // 16-byte unit u of a 128-byte row r sits at unit u ^ (r % 8).
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(prow + ((((half * 4 + q) ^ (tid & 7))) << 4)) =
-                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
+      for (int j = 0; j < 32; j += 2) {
+        const float e0 = col + j < p.seq ? exp2f(fmaf(v[j], p.scale_log2, -mb)) : 0.f;
+        const float e1 = col + j + 1 < p.seq ? exp2f(fmaf(v[j + 1], p.scale_log2, -mb)) : 0.f;
+        sum += e0 + e1;
+        w[j / 2] = pack2_bf16(e0, e1);
       }
-    }
-    fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
-    tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0 && ok && !*abort_flag) {
-      tc_fence_after_sync();
-      constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
-      for (int c = c0; c < c1; ++c) {
-        const uint64_t dp = smem_desc_sw128(smem_addr(sP + (c - c0) * kPChunkBytes));
-        const uint64_t dv = smem_desc_sw128(smem_addr(sVt + c * kVtChunkBytes));
+      uint8_t* prow = p_chunk(sP, sK, col / 64) + row * 128;
+      const int half = (col % 64) / 32;
+      // 16-byte unit u of a 128-byte row r sits at unit u ^ (r % 8).
 #pragma unroll
-        for (int k = 0; k < 4; ++k) tc_mma_bf16(tmem, dp + 2 * k, dv + 2 * k, kIdO, (c > 0 || k > 0) ? 1u : 0u);
-      }
-      tc_commit(bar_mma);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(prow + (((half * 4 + q) ^ (row & 7)) << 4)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
     }
   }
-  ok = ok && !*abort_flag && wait_bounded(bar_mma, mma_phase, guard, kSiteEpilogue);
+  red_sum[cgroup * 128 + row] = sum;
+  fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
+  tc_fence_before_sync();
+  __syncthreads();
+  if (tid == 0 && ok && !*abort_flag) {
+    tc_fence_after_sync();
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
+    for (int c = 0; c < nch; ++c) {
+      const uint64_t dp = smem_desc_sw128(smem_addr(p_chunk(sP, sK, c)));
+      const uint64_t dv = smem_desc_sw128(smem_addr(sVt + c * kVtChunkBytes));
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tc_mma_bf16(tmem, dp + 2 * k, dv + 2 * k, kIdO, (c > 0 || k > 0) ? 1u : 0u);
+    }
+    tc_commit(bar_mma);
+  }
+  ok = ok && !*abort_flag && wait_bounded(bar_mma, 1, guard, kSiteEpilogue);
 
-  // ---- O / sum -> bf16
+  // ---- O / sum -> bf16: warp (quarter, cgroup) writes columns 16*cgroup .. +15 of its rows
   if (ok) {
     tc_fence_after_sync();
-    float o0[32], o1[32];
-    tmem_ld_32cols(t_row, o0);
-    tmem_ld_32cols(t_row + 32, o1);
-    const int qi = qt * 128 + tid;
+    float o[16];
+    tmem_ld_16cols(t_row + cgroup * 16, o);
+    const int qi = qt * 128 + row;
     if (qi < p.seq) {
-      const float inv = 1.0f / sum;
-      __nv_bfloat16* dst =
-          static_cast<__nv_bfloat16*>(p.out[shard]) + (static_cast<int64_t>(row0) + qi) * p.Dn + hl * 64;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        reinterpret_cast<uint4*>(dst)[u] =
-            make_uint4(pack2_bf16(o0[8 * u] * inv, o0[8 * u + 1] * inv), pack2_bf16(o0[8 * u + 2] * inv, o0[8 * u + 3] * inv),
-                       pack2_bf16(o0[8 * u + 4] * inv, o0[8 * u + 5] * inv), pack2_bf16(o0[8 * u + 6] * inv, o0[8 * u + 7] * inv));
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        reinterpret_cast<uint4*>(dst)[4 + u] =
-            make_uint4(pack2_bf16(o1[8 * u] * inv, o1[8 * u + 1] * inv), pack2_bf16(o1[8 * u + 2] * inv, o1[8 * u + 3] * inv),
-                       pack2_bf16(o1[8 * u + 4] * inv, o1[8 * u + 5] * inv), pack2_bf16(o1[8 * u + 6] * inv, o1[8 * u + 7] * inv));
+      const float inv = 1.0f / (((red_sum[row] + red_sum[128 + row]) + red_sum[256 + row]) + red_sum[384 + row]);
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + (static_cast<int64_t>(row0) + qi) * p.Dn +
+                           hl * 64 + cgroup * 16;
+      reinterpret_cast<uint4*>(dst)[0] =
+          make_uint4(pack2_bf16(o[0] * inv, o[1] * inv), pack2_bf16(o[2] * inv, o[3] * inv),
+                     pack2_bf16(o[4] * inv, o[5] * inv), pack2_bf16(o[6] * inv, o[7] * inv));
+      reinterpret_cast<uint4*>(dst)[1] =
+          make_uint4(pack2_bf16(o[8] * inv, o[9] * inv), pack2_bf16(o[10] * inv, o[11] * inv),
+                     pack2_bf16(o[12] * inv, o[13] * inv), pack2_bf16(o[14] * inv, o[15] * inv));
     }
   }
 
@@ -222,7 +243,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 // ------------------------------------------------------------------ fp32 (CUDA cores)
 
 template <int DHMAX>
-__global__ void __launch_bounds__(kAttnThreads) attn_f32_kernel(const float* __restrict__ qkv, int64_t ld_qkv,
+__global__ void __launch_bounds__(kF32Threads) attn_f32_kernel(const float* __restrict__ qkv, int64_t ld_qkv,
                                                                 int64_t shard_stride_qkv, float* __restrict__ out,
                                                                 int64_t shard_stride_out, int seq, int Dn, int dh,
                                                                 int local_heads, float scale) {
@@ -231,7 +252,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_f32_kernel(const float* __r
   float* sc = smem_f + warp * seq;  // this warp's score row
   const int gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / local_heads, hl = gh % local_heads;
-  const int qi = blockIdx.x * (kAttnThreads / 32) + warp;
+  const int qi = blockIdx.x * (kF32Threads / 32) + warp;
   if (qi >= seq) return;
   const float* base = qkv + shard * shard_stride_qkv;
   const int64_t row0 = int64_t(b) * seq;
@@ -311,16 +332,16 @@ cudaError_t launch_attention_f32(const float* qkv, int64_t T, int n, int Dn, int
                                  int seq, float* out, cudaStream_t s) {
   if (batch <= 0 || seq <= 0) return cudaSuccess;
   if (dh > 128 || seq > 512) return cudaErrorInvalidValue;
-  const size_t smem = size_t(kAttnThreads / 32) * seq * sizeof(float);
+  const size_t smem = size_t(kF32Threads / 32) * seq * sizeof(float);
   dim3 grid(static_cast<unsigned>((seq + 3) / 4), static_cast<unsigned>(n * local_heads), static_cast<unsigned>(batch));
   const float scale = 1.0f / sqrtf(static_cast<float>(dh));
   const int64_t ld = 3 * int64_t(Dn);
   if (dh <= 32)
-    attn_f32_kernel<32><<<grid, kAttnThreads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads, scale);
+    attn_f32_kernel<32><<<grid, kF32Threads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads, scale);
   else if (dh <= 64)
-    attn_f32_kernel<64><<<grid, kAttnThreads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads, scale);
+    attn_f32_kernel<64><<<grid, kF32Threads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads, scale);
   else
-    attn_f32_kernel<128><<<grid, kAttnThreads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads,
+    attn_f32_kernel<128><<<grid, kF32Threads, smem, s>>>(qkv, ld, T * ld, out, T * Dn, seq, Dn, dh, local_heads,
                                                           scale);
   return cudaGetLastError();
 }
