@@ -1,9 +1,10 @@
 // attn_api.cu — C ABI of head-split attention (include/tpmlp.h, "Head-split
 // attention"): the per-rank weight handle and the forward call. Every step
-// runs in kernels: the QKV projection and the output projection on the
-// tensor-core GEMM (gemm_pair.cu / gemm_tc.cu; fp32: simt.cu), the transpose
-// of V (elementwise.cu), the attention itself (attention.cu) and the sum of
-// the output projection's partials (elementwise.cu).
+// runs in kernels: the QKV projection (whose epilogue also writes V
+// transposed) and the output projection on the tensor-core GEMM
+// (gemm_pair.cu / gemm_tc.cu; fp32: simt.cu), the attention itself
+// (attention.cu) and the sum of the output projection's partials
+// (elementwise.cu); the weight set-up transposes with elementwise.cu.
 #include "tpmlp.h"
 
 #include <cmath>
@@ -122,17 +123,22 @@ int run_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards
     return TPMLP_OK;
   }
   // bf16: the QKV projection of every rank in one grouped tensor-core product
-  // (X shared by all ranks), V^T per rank, then the attention kernel.
+  // (X shared by all ranks) whose epilogue writes Q, K row-major and V
+  // transposed, then the attention kernel.
   CUtensorMap mx;
   if (!make_operand_map(&mx, X, T, D, D, tc_box_rows_a()))
     return set_error(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the map of X");
   TcGemm g{};
   g.groups = n;
+  const int64_t T8 = rup8(T);
   for (int i = 0; i < n; ++i) {
     g.map_a[i] = &mx;
     g.map_b[i] = &sh->map_wqkv[i];
     g.out[i] = at<uint16_t>(qkv, 0) + static_cast<size_t>(i) * T * 3 * Dn;
+    g.aux_ht[i] = at<uint16_t>(ws, pl.vt) + static_cast<size_t>(i) * Dn * T8;  // V_i^T [Dn, T8] from the epilogue
   }
+  g.vt_col0 = static_cast<int>(2 * Dn);
+  g.ldt = T8;
   g.ldo = 3 * Dn;
   g.M = static_cast<int>(T);
   g.N = static_cast<int>(3 * Dn);
@@ -141,13 +147,11 @@ int run_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards
   g.shared = kSharedA;
   g.group_m = 16;
   ATTN_TRY(launch_tc_gemm(g, attn_wait_ns(), s));
-  const int64_t T8 = rup8(T);
   std::vector<CUtensorMap> mq(n), mv(n);
   AttnLaunch a{};
   for (int i = 0; i < n; ++i) {
     uint16_t* qkv_i = at<uint16_t>(qkv, 0) + static_cast<size_t>(i) * T * 3 * Dn;
     uint16_t* vt_i = at<uint16_t>(ws, pl.vt) + static_cast<size_t>(i) * Dn * T8;
-    ATTN_TRY(launch_transpose_u16(qkv_i + 2 * Dn, T, Dn, 3 * Dn, vt_i, T8, s));  // V_i^T [Dn, T]
     if (!make_operand_map(&mq[i], qkv_i, T, 3 * Dn, 3 * Dn, 128) || !make_operand_map(&mv[i], vt_i, Dn, T, T8, 64))
       return set_error(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected a map of rank %d's Q, K or V^T", i);
     a.map_qkv[i] = &mq[i];

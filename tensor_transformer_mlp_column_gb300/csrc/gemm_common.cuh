@@ -35,6 +35,7 @@ struct KParams {
   int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
   const __nv_bfloat16* resid;  // kEpiF32 / kEpiF32Tma: residual [M][ldo] added to the accumulator, or null
   int64_t slice_rows;          // kEpiF32, chain: output row m goes to row m % slice_rows of out[m / slice_rows]
+  int vt_col0;                 // kEpiBf16 with aux_ht: columns >= vt_col0 go transposed to aux_ht (row pitch ldt)
 };
 
 // Maps a tile index to (group, M block, N block). The tiles form a grid of
@@ -129,11 +130,19 @@ __device__ __forceinline__ void add_residual(const uint4 (&r)[4], float (&v)[32]
 template <int EPI>
 __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t m, int n0, const float (&v)[32]) {
   if constexpr (EPI == kEpiBf16) {
-    // acc rounded to bf16, row-major.
+    // acc rounded to bf16, row-major; with aux_ht, columns from vt_col0 on
+    // are written transposed instead (column c - vt_col0 of aux_ht's rows;
+    // the 32 lanes hold 32 consecutive rows, so each column is 64 contiguous
+    // bytes per warp).
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
+    __nv_bfloat16* vt = static_cast<__nv_bfloat16*>(p.aux_ht[g]);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if (n0 + 8 * j + 8 <= p.N) {
+      if (vt && n0 + 8 * j >= p.vt_col0 && n0 + 8 * j + 8 <= p.N) {
+        __nv_bfloat16* t = vt + int64_t(n0 + 8 * j - p.vt_col0) * p.ldt + m;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[int64_t(e) * p.ldt] = __float2bfloat16_rn(v[8 * j + e]);
+      } else if (n0 + 8 * j + 8 <= p.N) {
         uint4 w;
         w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
         w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);

@@ -406,6 +406,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.resid = static_cast<const __nv_bfloat16*>(g.resid);
   if (kp.resid && g.epi != kEpiF32) return cudaErrorInvalidValue;
   kp.slice_rows = g.slice_rows;
+  kp.vt_col0 = g.vt_col0;
   if (g.slice_rows && (g.epi != kEpiF32 || !g.chain || g.resid)) return cudaErrorInvalidValue;
   if (!kp.status) return cudaErrorInvalidSymbol;
   if (kp.tiles == 0) return cudaSuccess;

@@ -59,6 +59,8 @@ struct TcGemm {
   const void* resid;  // kEpiF32 (and its TMA-store form): bf16 residual [M][ldo] added to acc, or null
   int64_t slice_rows;  // chain == 1, kEpiF32: rows m go to out[m / slice_rows] (with output maps, one map per
                        // slice of slice_rows rows); 0 = off
+  int vt_col0;         // kEpiBf16 with aux_ht[g]: output columns >= vt_col0 are written transposed to aux_ht[g]
+                       // (bf16, row pitch ldt) instead of to out[g]
 };
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
