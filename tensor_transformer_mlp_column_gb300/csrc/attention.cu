@@ -76,6 +76,15 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 2^x on the special-function unit (relative error about 2^-22, flushes
+// subnormal results to zero), used for the softmax weights, which are rounded
+// to bf16 afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Shared-memory address of P chunk c (64 keys x 128 query rows): chunks 0..3
 // in the P buffer, chunks 4..7 in the key buffer, free once S is computed.
 __device__ __forceinline__ uint8_t* p_chunk(uint8_t* sP, uint8_t* sK, int c) {
@@ -94,11 +103,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   float* red_max = reinterpret_cast<float*>(sP + (nch < kPhaseChunks ? nch : kPhaseChunks) * kPChunkBytes);  // [4][128]
   float* red_sum = red_max + 4 * 128;                                                                         // [4][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 4 * 128);
-  uint64_t* bar_load = bars;
+  uint64_t* bar_load = bars;      // Q and the keys
   uint64_t* bar_mma = bars + 1;
   uint64_t* bar_drain = bars + 2;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 3);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 4);
+  uint64_t* bar_v = bars + 3;      // V^T, needed only by the P V product
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 5);
 
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / p.local_heads, hl = gh % p.local_heads;
@@ -112,6 +122,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
     mbar_init(bar_load, 1);
     mbar_init(bar_mma, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_v, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -126,10 +137,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   if (tid == 0) {
     const CUtensorMap* mq = &p.map_qkv[shard];
     const CUtensorMap* mv = &p.map_vt[shard];
-    mbar_arrive_expect_tx(bar_load, kQBytes + nkv * kKBlockBytes + nch * kVtChunkBytes);
+    mbar_arrive_expect_tx(bar_load, kQBytes + nkv * kKBlockBytes);
     tma_load_2d(sQ, mq, hl * 64, row0 + qt * 128, bar_load);
     for (int j = 0; j < nkv; ++j) tma_load_2d(sK + j * kKBlockBytes, mq, p.Dn + hl * 64, row0 + j * 128, bar_load);
-    for (int c = 0; c < nch; ++c) tma_load_2d(sVt + c * kVtChunkBytes, mv, row0 + c * 64, hl * 64, bar_load);
+    mbar_arrive_expect_tx(bar_v, nch * kVtChunkBytes);
+    for (int c = 0; c < nch; ++c) tma_load_2d(sVt + c * kVtChunkBytes, mv, row0 + c * 64, hl * 64, bar_v);
   }
   bool ok = wait_bounded(bar_load, 0, guard, kSiteProducer);
   if (ok && tid == 0) {
@@ -153,13 +165,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   const int col0 = cgroup * gcols;
   float mx = -INFINITY;
   if (ok) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
     for (int g = 0; g < gcols; g += 32) {
       float v[32];
       tmem_ld_32cols(t_row + col0 + g, v);
+      if (col0 + g + 32 <= p.seq) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (col0 + g + j < p.seq) mx = fmaxf(mx, v[j]);
+        for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col0 + g + j < p.seq) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
+      }
     }
+    mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
   }
   red_max[cgroup * 128 + row] = mx;
   __syncthreads();
@@ -173,13 +192,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       float v[32];
       tmem_ld_32cols(t_row + col, v);
       uint32_t w[16];
+      float s2[2] = {0.f, 0.f};
+      const bool full = col + 32 <= p.seq;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        const float e0 = col + j < p.seq ? exp2f(fmaf(v[j], p.scale_log2, -mb)) : 0.f;
-        const float e1 = col + j + 1 < p.seq ? exp2f(fmaf(v[j + 1], p.scale_log2, -mb)) : 0.f;
-        sum += e0 + e1;
+        float e0 = ex2_approx(fmaf(v[j], p.scale_log2, -mb));
+        float e1 = ex2_approx(fmaf(v[j + 1], p.scale_log2, -mb));
+        if (!full) {
+          e0 = col + j < p.seq ? e0 : 0.f;
+          e1 = col + j + 1 < p.seq ? e1 : 0.f;
+        }
+        s2[0] += e0;
+        s2[1] += e1;
         w[j / 2] = pack2_bf16(e0, e1);
       }
+      sum += s2[0] + s2[1];
       uint8_t* prow = p_chunk(sP, sK, col / 64) + row * 128;
       const int half = (col % 64) / 32;
       // 16-byte unit u of a 128-byte row r sits at unit u ^ (r % 8).
@@ -193,7 +220,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
   tc_fence_before_sync();
   __syncthreads();
-  if (tid == 0 && ok && !*abort_flag) {
+  if (tid == 0 && ok && !*abort_flag && wait_bounded(bar_v, 0, guard, kSiteProducer)) {
     tc_fence_after_sync();
     constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
     for (int c = 0; c < nch; ++c) {
@@ -229,6 +256,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   __syncthreads();
   if (*abort_flag && tid == 0) {
     wait_drain(bar_load, 0, p.wait_ns);
+    wait_drain(bar_v, 0, p.wait_ns);
     tc_commit(bar_drain);
     wait_drain(bar_drain, 0, p.wait_ns);
   }
