@@ -37,13 +37,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # one pass; command and figures in profiles/traffic_large_forward.md). Valid
 # only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
-TRAFFIC_SOURCE_HASH = "8c4ae2e86b281988"
+TRAFFIC_SOURCE_HASH = "63a1e03fc373f847"
 TRAFFIC_BYTES = {
-    "gemm1_gelu(faithful)": 1_432_057_856,
-    "gemm2_partials": 3_003_428_352,
-    "allreduce": 2_400_385_536,
-    "gemm1_gelu(fused)": 1_432_737_024,
-    "gemm2_fused_sum": 3_717_289_216,
+    "gemm1_gelu(faithful)": 1_304_017_664,
+    "gemm2_partials": 3_029_028_096,
+    "allreduce": 2_401_554_688,
+    "gemm1_gelu(fused)": 1_304_647_424,
+    "gemm2_fused_sum": 2_778_154_752,
 }
 
 
@@ -429,7 +429,9 @@ def bench_small_workloads(local_rank):
             e1.record(stream)
             torch.cuda.synchronize(dev)
             ms = e0.elapsed_time(e1) / reps
-            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
+            gms = _time_graph_ms(lambda: tp.tpmlp_forward(X, sh, mode, Y, ws), dev, reps)
+            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1),
+                         "graph_ms": round(gms, 4), "graph_TFLOP/s": round(w.fwd_flops() / (gms * 1e-3) / 1e12, 1)}
         tp.tpmlp_check_status(stream)
         sh.free()
         out[name] = res
@@ -511,6 +513,29 @@ def _time_ms(fn, dev, stream, reps: int, warm: int = 3) -> float:
     e0.record(stream)
     for _ in range(reps):
         fn()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / reps
+
+
+def _time_graph_ms(fn, dev, reps: int) -> float:
+    """Mean device time of fn replayed from a CUDA graph of `reps` calls (the
+    library's calls only enqueue work, so they capture as they are); the
+    graph removes the host's per-call launch and argument costs."""
+    import torch
+
+    fn()  # warm: one-time attributes and caches outside the capture
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     return e0.elapsed_time(e1) / reps
@@ -670,7 +695,9 @@ def bench_attention(args, local_rank, peaks):
         for mode in ("faithful", "fused"):
             ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, mode), dtype=torch.uint8, device=dev)
             ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, stream, 50, 5)
-            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}
+            gms = _time_graph_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, 50)
+            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1),
+                         "graph_ms": round(gms, 4), "graph_TFLOP/s": round(w.fwd_flops() / (gms * 1e-3) / 1e12, 1)}
         tp.tpmlp_check_status(stream)
         sh.free()
         out[name] = res

@@ -350,3 +350,31 @@ def test_forward_save_and_backward_saved(tp, case, dtype):
             check(f64(g_sv[1][i]), dA_ref[i], dtype, f"dA_{i} {mode}")
             check(f64(g_sv[2][i]), dB_ref[i], dtype, f"dB_{i} {mode}")
     tp.tpmlp_check_status()
+
+
+# ----------------------------------------------------------------- CUDA graphs
+
+def test_forward_replays_from_a_cuda_graph(tp):
+    # The calls only enqueue work on the given stream, so a CUDA graph of them
+    # replays the same computation: bit-identical to eager calls.
+    w = small_workload("graph", 1000, 512, 4096, 4, "bf16")
+    d = on_gpu(make_inputs(w, seed=61))
+    sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
+    for mode in ("faithful", "fused"):
+        ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, mode), dtype=torch.uint8, device="cuda")
+        Y = torch.empty((w.T, w.D), dtype=torch.float32, device="cuda")
+        ref = tp.tpmlp_forward(d["X"], sh, mode)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            tp.tpmlp_forward(d["X"], sh, mode, Y, ws)
+        Y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Y, ref)
+        d["X"].mul_(-1.0)  # new input, same buffers: the replay sees it
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(Y, tp.tpmlp_forward(d["X"], sh, mode))
+        d["X"].mul_(-1.0)
+    tp.tpmlp_check_status()
