@@ -701,6 +701,20 @@ def bench_attention(args, local_rank, peaks):
         tp.tpmlp_check_status(stream)
         sh.free()
         out[name] = res
+    # Longer sequences at the same 4096 tokens (batch x seq = 4096): the
+    # attention core's FLOP grow linearly in seq here, the projections not at all.
+    for name in ("attn_long1024", "attn_long2048", "attn_long4096"):
+        w = ATTN_WORKLOADS[name]
+        inp = make_attn_inputs(w, seed=0)
+        d = {k: v.to(dev) for k, v in inp.items()}
+        sh = tp.tpmlp_attn_shard(d["Wq"], d["Wk"], d["Wv"], d["Wo"], w.heads, w.N)
+        Y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
+        ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, "fused"), dtype=torch.uint8, device=dev)
+        ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, "fused", Y, ws), dev, stream, 20, 3)
+        out[name] = {"batch": w.batch, "seq": w.seq, "fused": {"ms": round(ms, 4),
+                     "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}}
+        tp.tpmlp_check_status(stream)
+        sh.free()
     # heads time against seq: least squares on (1, seq, seq^2)
     import numpy as np
 

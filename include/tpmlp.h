@@ -335,7 +335,10 @@ int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices,
  *   O_i = softmax(Q_i K_i^T / sqrt(d_h)) V_i per sequence and local head
  *         (no mask),
  *   Y   = sum_i O_i Wo_i, summed like the MLP's partials.
- * bf16: d_h = 64, seq % 8 == 0; fp32: d_h <= 128; both: seq <= 512.
+ * bf16: d_h = 64, seq % 8 == 0, any length (a streaming kernel with a running
+ * maximum; environment variable TPMLP_ATTN_KERNEL=0 selects, up to 512
+ * tokens, an exact kernel that holds the whole score row); fp32: d_h <= 128,
+ * seq <= 8192.
  * ---------------------------------------------------------------------- */
 
 typedef struct tpmlp_attn_shards tpmlp_attn_shards;

@@ -4,8 +4,8 @@
 // no mask, reading Q, K from the rank's QKV projection [T, 3 D/n] and V from
 // its transpose V^T [D/n, T], and writing O into the rank's [T, D/n] block.
 //
-// Tensor-core kernel (bf16, d_h = 64, seq <= 512, seq % 8 == 0): one CTA of
-// 16 warps per (128-query tile, head, sequence).
+// Exact tensor-core kernel (bf16, d_h = 64, seq <= 512, seq % 8 == 0): one
+// CTA of 16 warps per (128-query tile, head, sequence).
 //   thread 0 : TMA-loads the Q tile, all keys and all of V^T for the head
 //              into 128-byte-swizzled shared memory (one mbarrier), then
 //              issues S = Q K^T (M=128, N=128 per key block, K=16 steps)
@@ -24,8 +24,10 @@
 // rescale of a streaming kernel. Every wait is bounded; on a timeout the CTA
 // records the site, drains its copies and MMAs and frees its tensor memory.
 //
-// fp32 kernel (any d_h <= 128, seq <= 512): one warp per query row, scores
+// fp32 kernel (any d_h <= 128, seq <= 8192): one warp per query row, scores
 // in shared memory, the same two passes, on the CUDA cores.
+#include <cstdlib>
+
 #include "device.cuh"
 #include "internal.h"
 
@@ -268,6 +270,284 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   }
 }
 
+// ------------------------------------------------------------------ streaming form (any seq)
+//
+// One CTA of 8 softmax warps + 1 control warp per (128-query tile, head,
+// sequence), 99 KB of shared memory and 256 TMEM columns, so two CTAs share an
+// SM and one's loads and products overlap the other's softmax. Keys go in
+// blocks of 128 with a running maximum m and sum l per query row:
+//   control thread: TMA loads (Q once; K through a 2-slot ring; V^T of one
+//     block), S_j = Q K_j^T into TMEM columns 0..127, and P_{j-1} V_{j-1}
+//     accumulated into O (TMEM columns 128..191) once the softmax has written
+//     P_{j-1}; every wait bounded.
+//   softmax warp w: TMEM lanes 32 (w % 4) (its query rows) and key half w / 4
+//     of the block. Block maximum (the two halves meet in shared memory), new
+//     running maximum m', a = 2^((m - m') log2(e)/sqrt(d_h)), p = 2^((s - m')
+//     log2(e)/sqrt(d_h)) written as bf16 into the swizzled P operand once the
+//     previous P V has finished, l <- a l + sum p, and O <- a O in TMEM when
+//     the maximum moved.
+// At the end O / l is rounded to bf16. The same result as the exact kernel up
+// to rounding (the weights of earlier blocks are rescaled in fp32).
+
+constexpr int kStrmSoftmaxWarps = 8;
+constexpr int kStrmThreads = (kStrmSoftmaxWarps + 1) * 32;
+constexpr uint32_t kStrmKBytes = 128 * 128;             // 128 keys x 64 bf16
+constexpr uint32_t kStrmVtBytes = 2 * kVtChunkBytes;    // V^T of 128 keys
+constexpr uint32_t kStrmPBytes = 2 * kPChunkBytes;      // P of 128 keys
+constexpr uint32_t kStrmSmem = 1024 + kQBytes + 2 * kStrmKBytes + kStrmVtBytes + kStrmPBytes + 2 * 2 * 128 * 4 + 128;
+
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + kQBytes;  // two slots
+  uint8_t* sVt = sK + 2 * kStrmKBytes;
+  uint8_t* sP = sVt + kStrmVtBytes;
+  float* red_max = reinterpret_cast<float*>(sP + kStrmPBytes);  // [2][128]
+  float* red_sum = red_max + 256;                                // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 256);
+  uint64_t* bar_q = bars + 0;
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;
+  uint64_t* s_full = bars + 6;
+  uint64_t* s_free = bars + 7;   // one arrival per softmax warp: S read, P written, O rescaled
+  uint64_t* o_done = bars + 8;
+  uint64_t* x_bar = bars + 9;    // one arrival per softmax warp: the halves' partial maxima (sums) written
+  uint64_t* drain = bars + 10;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+
+  const int nkv = (p.seq + 127) / 128;
+  const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
+  const int shard = gh / p.local_heads, hl = gh % p.local_heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr uint32_t kCols = 256;  // S: columns 0..127, O: 128..191
+
+  if (tid == 0) {
+    mbar_init(bar_q, 1);
+    mbar_init(k_full, 1);
+    mbar_init(k_full + 1, 1);
+    mbar_init(k_empty, 1);
+    mbar_init(k_empty + 1, 1);
+    mbar_init(v_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, kStrmSoftmaxWarps);
+    mbar_init(o_done, 1);
+    mbar_init(x_bar, kStrmSoftmaxWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kStrmSoftmaxWarps) tmem_alloc(tmem_slot, kCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + 128;
+  const WaitGuard guard{abort_flag, p.wait_ns, p.status};
+  const int32_t row0 = b * p.seq;
+
+  if (warp == kStrmSoftmaxWarps) {
+    if (lane == 0) {
+      // ---------------- control: loads and products
+      const CUtensorMap* mq = &p.map_qkv[shard];
+      const CUtensorMap* mv = &p.map_vt[shard];
+      const int kx = p.Dn + hl * 64;
+      mbar_arrive_expect_tx(bar_q, kQBytes);
+      tma_load_2d(sQ, mq, hl * 64, row0 + qt * 128, bar_q);
+      for (int j = 0; j < 2 && j < nkv; ++j) {
+        mbar_arrive_expect_tx(k_full + j, kStrmKBytes);
+        tma_load_2d(sK + j * kStrmKBytes, mq, kx, row0 + j * 128, k_full + j);
+      }
+      mbar_arrive_expect_tx(v_full, kStrmVtBytes);
+      tma_load_2d(sVt, mv, row0, hl * 64, v_full);
+      tma_load_2d(sVt + kVtChunkBytes, mv, row0 + 64, hl * 64, v_full);
+      bool ok = wait_bounded(bar_q, 0, guard, kSiteProducer);
+      const uint64_t dq = smem_desc_sw128(smem_addr(sQ));
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128);
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
+      for (int j = 0; ok && j <= nkv; ++j) {
+        if (j < nkv) {
+          const int slot = j & 1;
+          ok = wait_bounded(k_full + slot, (j >> 1) & 1, guard, kSiteProducer);
+          if (ok && j > 0) ok = wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);  // S of block j-1 read
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint64_t dk = smem_desc_sw128(smem_addr(sK + slot * kStrmKBytes));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) tc_mma_bf16(tS, dq + 2 * k, dk + 2 * k, kIdS, k > 0 ? 1u : 0u);
+          tc_commit(s_full);
+          tc_commit(k_empty + slot);
+        } else {
+          ok = wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);  // the last block's P written
+          if (!ok) break;
+        }
+        if (j > 0) {  // O (+)= P_{j-1} V_{j-1}
+          ok = wait_bounded(v_full, (j - 1) & 1, guard, kSiteProducer);
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint64_t dp = smem_desc_sw128(smem_addr(sP + c * kPChunkBytes));
+            const uint64_t dv = smem_desc_sw128(smem_addr(sVt + c * kVtChunkBytes));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              tc_mma_bf16(tO, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || c > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(o_done);
+          if (j < nkv) {  // V^T of block j into the slot once that product has read it
+            ok = wait_bounded(o_done, (j - 1) & 1, guard, kSiteMmaAcc);
+            if (!ok) break;
+            mbar_arrive_expect_tx(v_full, kStrmVtBytes);
+            tma_load_2d(sVt, mv, row0 + j * 128, hl * 64, v_full);
+            tma_load_2d(sVt + kVtChunkBytes, mv, row0 + j * 128 + 64, hl * 64, v_full);
+          }
+        }
+        if (j + 2 < nkv) {  // K of block j+2 into block j's slot once S_j has read it
+          ok = wait_bounded(k_empty + (j & 1), (j >> 1) & 1, guard, kSiteProducer);
+          if (!ok) break;
+          mbar_arrive_expect_tx(k_full + (j & 1), kStrmKBytes);
+          tma_load_2d(sK + (j & 1) * kStrmKBytes, mq, kx, row0 + (j + 2) * 128, k_full + (j & 1));
+        }
+      }
+    }
+  } else {
+    // ---------------- softmax warps
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float m_run = -INFINITY, l_half = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      ok = __all_sync(0xffffffffu, ok && wait_bounded(s_full, j & 1, guard, kSiteMmaFull));
+      if (!ok) break;
+      tc_fence_after_sync();
+      float v[64];
+      {
+        float v0[32], v1[32];
+        tmem_ld_32cols(tS + lane_off + half * 64, v0);
+        tmem_ld_32cols(tS + lane_off + half * 64 + 32, v1);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = v0[i];
+          v[32 + i] = v1[i];
+        }
+      }
+      const int kbase = j * 128 + half * 64;  // key of column 0 of this half
+      const bool full = kbase + 64 <= p.seq;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (full || kbase + i < p.seq) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+      red_max[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_bar);
+      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, j & 1, guard, kSiteEpilogue));
+      if (!ok) break;
+      const float m_new = fmaxf(m_run, fmaxf(red_max[row], red_max[128 + row]));
+      const float alpha = ex2_approx((m_run - m_new) * p.scale_log2);  // 0 on the first block
+      const float mb = m_new * p.scale_log2;
+      uint32_t w[32];
+      float s2[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        float e0 = ex2_approx(fmaf(v[i], p.scale_log2, -mb));
+        float e1 = ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb));
+        if (!full) {
+          e0 = kbase + i < p.seq ? e0 : 0.f;
+          e1 = kbase + i + 1 < p.seq ? e1 : 0.f;
+        }
+        s2[0] += e0;
+        s2[1] += e1;
+        w[i / 2] = pack2_bf16(e0, e1);
+      }
+      l_half = l_half * alpha + (s2[0] + s2[1]);
+      if (j > 0) {  // the previous P V has read P and finished writing O
+        ok = __all_sync(0xffffffffu, wait_bounded(o_done, (j - 1) & 1, guard, kSiteMmaAcc));
+        if (!ok) break;
+        tc_fence_after_sync();
+      }
+      uint8_t* prow = sP + half * kPChunkBytes + row * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
+            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's 32 columns of O
+        float o[32];
+        tmem_ld_32cols(tO + lane_off + half * 32, o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        tmem_st_32cols(tO + lane_off + half * 32, o);
+      }
+      m_run = m_new;
+      fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+    }
+    // ---- O / l -> bf16
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_done, (nkv - 1) & 1, guard, kSiteEpilogue));
+    if (ok) {
+      red_sum[half * 128 + row] = l_half;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x_bar);
+      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, nkv & 1, guard, kSiteEpilogue));
+    }
+    if (ok) {
+      tc_fence_after_sync();
+      float o[32];
+      tmem_ld_32cols(tO + lane_off + half * 32, o);
+      const int qi = qt * 128 + row;
+      if (qi < p.seq) {
+        const float inv = 1.0f / (red_sum[row] + red_sum[128 + row]);
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + (static_cast<int64_t>(row0) + qi) * p.Dn +
+                             hl * 64 + half * 32;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          reinterpret_cast<uint4*>(dst)[u] = make_uint4(
+              pack2_bf16(o[8 * u] * inv, o[8 * u + 1] * inv), pack2_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
+              pack2_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv), pack2_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+      }
+    }
+  }
+
+  // ---- clean-up: after an abort, copies and products in flight finish first
+  __syncthreads();
+  if (*abort_flag && tid == kStrmSoftmaxWarps * 32) {
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 200000ull) {
+    }
+    tc_commit(drain);
+    wait_drain(drain, 0, p.wait_ns);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kStrmSoftmaxWarps) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
 // ------------------------------------------------------------------ fp32 (CUDA cores)
 
 template <int DHMAX>
@@ -329,9 +609,18 @@ __global__ void __launch_bounds__(kF32Threads) attn_f32_kernel(const float* __re
 
 }  // namespace
 
+// The streaming kernel by default (any length; as fast as the exact one up to
+// 512 tokens); TPMLP_ATTN_KERNEL=0 selects the exact kernel where it applies
+// (seq <= 512). Read at every launch, so a process can compare the two.
+int attn_kernel_choice(int seq) {
+  if (seq > 512) return 1;
+  const char* v = getenv("TPMLP_ATTN_KERNEL");
+  return (v && atoi(v) == 0) ? 0 : 1;
+}
+
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s) {
   if (a.batch <= 0 || a.seq <= 0) return cudaSuccess;
-  if (a.seq > 512 || a.seq % 8 != 0 || a.n < 1 || a.n > kMaxGroups) return cudaErrorInvalidValue;
+  if (a.seq % 8 != 0 || a.n < 1 || a.n > kMaxGroups) return cudaErrorInvalidValue;
   AttnParams p;
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < a.n; ++i) {
@@ -345,13 +634,20 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s) {
   p.scale_log2 = 1.4426950408889634f / sqrtf(64.0f);
   p.wait_ns = a.wait_ns;
   p.status = a.status;
+  dim3 grid(static_cast<unsigned>((a.seq + 127) / 128), static_cast<unsigned>(a.n * a.local_heads),
+            static_cast<unsigned>(a.batch));
+  if (attn_kernel_choice(a.seq) == 1) {
+    cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kStrmSmem));
+    if (e != cudaSuccess) return e;
+    attn_stream_kernel<<<grid, kStrmThreads, kStrmSmem, s>>>(p);
+    return cudaGetLastError();
+  }
   const int nkv = (a.seq + 127) / 128, nch = (a.seq + 63) / 64;
   const uint32_t smem = attn_smem_bytes(nkv, nch);
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(attn_smem_bytes(4, 8)));
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.seq + 127) / 128), static_cast<unsigned>(a.n * a.local_heads),
-            static_cast<unsigned>(a.batch));
   attn_tc_kernel<<<grid, kAttnThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
@@ -359,8 +655,12 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s) {
 cudaError_t launch_attention_f32(const float* qkv, int64_t T, int n, int Dn, int dh, int local_heads, int batch,
                                  int seq, float* out, cudaStream_t s) {
   if (batch <= 0 || seq <= 0) return cudaSuccess;
-  if (dh > 128 || seq > 512) return cudaErrorInvalidValue;
+  if (dh > 128 || seq > 8192) return cudaErrorInvalidValue;
   const size_t smem = size_t(kF32Threads / 32) * seq * sizeof(float);
+  for (auto k : {attn_f32_kernel<32>, attn_f32_kernel<64>, attn_f32_kernel<128>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 4 * 8192 * 4);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid(static_cast<unsigned>((seq + 3) / 4), static_cast<unsigned>(n * local_heads), static_cast<unsigned>(batch));
   const float scale = 1.0f / sqrtf(static_cast<float>(dh));
   const int64_t ld = 3 * int64_t(Dn);

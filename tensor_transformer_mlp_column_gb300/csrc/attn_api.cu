@@ -92,7 +92,8 @@ T* at(void* base, size_t off) {
 int check_attn(const tpmlp_attn_shards* sh, int64_t batch, int64_t seq) {
   if (!sh) return set_error(TPMLP_ERR_ARG, "attention shards handle is NULL");
   if (batch < 1 || seq < 1) return set_error(TPMLP_ERR_ARG, "batch and seq must be >= 1");
-  if (seq > 512) return set_error(TPMLP_ERR_SHAPE, "seq = %lld exceeds 512", static_cast<long long>(seq));
+  if (sh->dt == TPMLP_F32 && seq > 8192)
+    return set_error(TPMLP_ERR_SHAPE, "fp32 attention supports seq up to 8192 (seq = %lld)", static_cast<long long>(seq));
   if (batch * seq > (int64_t(1) << 30)) return set_error(TPMLP_ERR_ARG, "batch * seq is too large");
   if (sh->dt == TPMLP_BF16 && seq % 8 != 0)
     return set_error(TPMLP_ERR_SHAPE, "bf16 attention needs seq %% 8 == 0 (seq = %lld)", static_cast<long long>(seq));

@@ -151,7 +151,8 @@ cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 // Attention of head-split tensor parallelism (attention.cu), per rank i:
 // O_i = softmax(Q K^T / sqrt(d_h)) V for each of its local heads and each
 // sequence, Q, K, V from the rank's QKV projection. Tensor-core form: bf16,
-// d_h = 64, seq <= 512 and seq % 8 == 0; V read from its transpose.
+// d_h = 64, seq % 8 == 0 (the streaming kernel; TPMLP_ATTN_KERNEL=0 selects the
+// exact one up to 512 tokens); V read from its transpose.
 struct AttnLaunch {
   const CUtensorMap* map_qkv[kMaxGroups];  // QKV_i [T, 3 Dn] bf16, 64 x 128 boxes (make_operand_map, 128 rows)
   const CUtensorMap* map_vt[kMaxGroups];   // V_i^T [Dn, T] bf16, 64 x 64 boxes (make_operand_map, 64 rows)
@@ -161,7 +162,7 @@ struct AttnLaunch {
   int* status;
 };
 cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s);
-// fp32 form on the CUDA cores: qkv [n][T][3 Dn], out [n][T][Dn]; d_h <= 128, seq <= 512.
+// fp32 form on the CUDA cores: qkv [n][T][3 Dn], out [n][T][Dn]; d_h <= 128, seq <= 8192.
 cudaError_t launch_attention_f32(const float* qkv, int64_t T, int n, int Dn, int dh, int local_heads, int batch,
                                  int seq, float* out, cudaStream_t s);
 

@@ -60,12 +60,16 @@ SMALL_BF16 = [
     ("three_blocks", 2, 384, 128, 2, 2),
     ("phase_tail", 1, 264, 64, 1, 1),       # 5 key chunks: phases of 4 and 1
     ("many_ranks", 2, 64, 1024, 16, 16),
+    ("long_seq", 2, 640, 128, 2, 1),        # streaming kernel: 5 key blocks
+    ("seq1024", 1, 1024, 256, 4, 2),
+    ("long_ragged", 1, 1000, 64, 1, 1),     # streaming kernel, partial last key block
 ]
 SMALL_F32 = [
     ("two_ranks", 2, 16, 64, 4, 2),
     ("dh16", 3, 33, 48, 3, 3),
     ("dh128", 1, 100, 256, 2, 2),
     ("seq512", 2, 512, 64, 1, 1),
+    ("seq700", 1, 700, 64, 2, 2),
 ]
 CASES = [c + ("bf16",) for c in SMALL_BF16] + [c + ("f32",) for c in SMALL_F32]
 
@@ -113,7 +117,8 @@ def test_attention_weight_layout_bit_exact(tp, dtype):
     sh.free()
 
 
-@pytest.mark.parametrize("name", ["attn_tiny_fp32", "attn_seq128", "attn_seq256", "attn_seq512"])
+@pytest.mark.parametrize("name", ["attn_tiny_fp32", "attn_seq128", "attn_seq256", "attn_seq512", "attn_long1024",
+                                  "attn_long4096"])
 def test_attention_workload_full_oracle(tp, name):
     w = ATTN_WORKLOADS[name]
     inp = make_attn_inputs(w, seed=0)
@@ -140,7 +145,51 @@ def test_attention_argument_errors(tp):
     X = torch.zeros((2 * 12, D), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(tp.TpmlpError):  # bf16 needs seq % 8 == 0
         tp.tpmlp_attn_forward(X, 2, sh)
-    X = torch.zeros((1024, D), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(tp.TpmlpError):  # seq 1024 > 512
-        tp.tpmlp_attn_forward(X, 1, sh)
+    sh.free()
+    Wf = [torch.zeros((D, D), dtype=torch.float32, device="cuda") for _ in range(4)]
+    shf = tp.tpmlp_attn_shard(*Wf, 2, 2)
+    X = torch.zeros((8200, D), dtype=torch.float32, device="cuda")
+    with pytest.raises(tp.TpmlpError):  # fp32 seq 8200 > 8192
+        tp.tpmlp_attn_forward(X, 1, shf)
+    shf.free()
+
+
+@pytest.mark.parametrize("case", [c + ("bf16",) for c in SMALL_BF16 if c[2] <= 512], ids=lambda c: c[0])
+def test_exact_kernel_matches_oracle(tp, case, monkeypatch):
+    # TPMLP_ATTN_KERNEL=0 runs the exact kernel (whole score row in tensor
+    # memory, up to 512 tokens) instead of the default streaming one; both
+    # must meet the same tolerance.
+    monkeypatch.setenv("TPMLP_ATTN_KERNEL", "0")
+    w = workload(*case)
+    inp = make_attn_inputs(w, seed=52)
+    Y_ref, parts = oracle_parts(inp, w)
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_attn_shard(d["Wq"], d["Wk"], d["Wv"], d["Wo"], w.heads, w.N)
+    O = tp.tpmlp_attn_heads(d["X"], w.batch, sh)
+    tp.tpmlp_check_status()
+    for i, (O_ref, _) in enumerate(parts):
+        check(f64(O[i]), O_ref, "bf16", f"exact-kernel O_{i}")
+    check(f64(tp.tpmlp_attn_forward(d["X"], w.batch, sh, "fused")), Y_ref, "bf16", "exact-kernel Y")
+    sh.free()
+
+
+def test_streaming_kernel_handles_large_logits(tp, monkeypatch):
+    # Logits of tens: the streaming kernel's running maximum rescales earlier
+    # blocks by tiny factors. Both kernels see the same bf16 Q, K, V here, so
+    # they must agree closely (the oracle's exact Q, K differ from the rounded
+    # ones by more than the tolerance once logits are this large), and every
+    # output must be finite.
+    w = workload("large_logits", 2, 512, 128, 2, 1, "bf16")
+    inp = make_attn_inputs(w, seed=53)
+    inp["X"] = (inp["X"].float() * 6.0).to(torch.bfloat16)
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_attn_shard(d["Wq"], d["Wk"], d["Wv"], d["Wo"], w.heads, w.N)
+    monkeypatch.setenv("TPMLP_ATTN_KERNEL", "0")
+    O_exact = tp.tpmlp_attn_heads(d["X"], w.batch, sh).float()
+    monkeypatch.setenv("TPMLP_ATTN_KERNEL", "1")
+    O_strm = tp.tpmlp_attn_heads(d["X"], w.batch, sh).float()
+    tp.tpmlp_check_status()
+    assert torch.isfinite(O_exact).all() and torch.isfinite(O_strm).all()
+    rel = (torch.linalg.norm(O_strm - O_exact) / torch.linalg.norm(O_exact)).item()
+    assert rel <= 1e-2, rel
     sh.free()

@@ -20,7 +20,9 @@ scratchllm.com "Tensor-Parallel MLP (Megatron)", section "The problem"):
 Attention workloads (ATTN_WORKLOADS: batch x seq tokens, D, heads, N ranks;
 duoan.github.io "Tensor Parallelism in Megatron-LM" §4): attn_tiny_fp32
 (2 x 16, D=64, 4 heads, N=2, W~N(0,1/8)) and attn_seq{128,256,512} (8 x seq,
-D=1024, 16 heads of 64, N=4, bf16, X~N(0,1), W~N(0,0.02)); X uses seed+0,
+D=1024, 16 heads of 64, N=4, bf16, X~N(0,1), W~N(0,0.02)), and
+attn_long{1024,2048,4096} (4096 tokens as 4 x 1024, 2 x 2048, 1 x 4096,
+otherwise the same); X uses seed+0,
 Wq..Wo seeds +1..+4.
 
 "N(0, s)" means a normal with standard deviation s. Each tensor gets its own
@@ -162,6 +164,10 @@ ATTN_WORKLOADS: dict[str, AttnWorkload] = {
     "attn_seq128": AttnWorkload("attn_seq128", 8, 128, 1024, 16, 4, "bf16", 1.0, 0.02),
     "attn_seq256": AttnWorkload("attn_seq256", 8, 256, 1024, 16, 4, "bf16", 1.0, 0.02),
     "attn_seq512": AttnWorkload("attn_seq512", 8, 512, 1024, 16, 4, "bf16", 1.0, 0.02),
+    # Longer sequences at the same 4096 tokens: the attention core grows with seq.
+    "attn_long1024": AttnWorkload("attn_long1024", 4, 1024, 1024, 16, 4, "bf16", 1.0, 0.02),
+    "attn_long2048": AttnWorkload("attn_long2048", 2, 2048, 1024, 16, 4, "bf16", 1.0, 0.02),
+    "attn_long4096": AttnWorkload("attn_long4096", 1, 4096, 1024, 16, 4, "bf16", 1.0, 0.02),
 }
 
 
