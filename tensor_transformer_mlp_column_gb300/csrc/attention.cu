@@ -87,6 +87,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Shared-memory address of P chunk c (64 keys x 128 query rows): chunks 0..3
 // in the P buffer, chunks 4..7 in the key buffer, free once S is computed.
 __device__ __forceinline__ uint8_t* p_chunk(uint8_t* sP, uint8_t* sK, int c) {
@@ -477,9 +484,14 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       const int kbase = j * 128 + half * 64;  // key of column 0 of this half
       const bool full = kbase + 64 <= p.seq;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (full) {  // every column a key of the sequence: two values per max
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (full || kbase + i < p.seq) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+        for (int i = 0; i < 64; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], v[i], v[i + 1]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (kbase + i < p.seq) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
+      }
       red_max[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       __syncwarp();
       if (lane == 0) mbar_arrive(x_bar);
@@ -495,17 +507,24 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       const float mb = m_new * p.scale_log2;
       uint32_t w[32];
       float s2[2] = {0.f, 0.f};
+      if (full) {
 #pragma unroll
-      for (int i = 0; i < 64; i += 2) {
-        float e0 = ex2_approx(fmaf(v[i], p.scale_log2, -mb));
-        float e1 = ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb));
-        if (!full) {
-          e0 = kbase + i < p.seq ? e0 : 0.f;
-          e1 = kbase + i + 1 < p.seq ? e1 : 0.f;
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = ex2_approx(fmaf(v[i], p.scale_log2, -mb));
+          const float e1 = ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb));
+          s2[0] += e0;
+          s2[1] += e1;
+          w[i / 2] = pack2_bf16(e0, e1);
         }
-        s2[0] += e0;
-        s2[1] += e1;
-        w[i / 2] = pack2_bf16(e0, e1);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float e0 = kbase + i < p.seq ? ex2_approx(fmaf(v[i], p.scale_log2, -mb)) : 0.f;
+          const float e1 = kbase + i + 1 < p.seq ? ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb)) : 0.f;
+          s2[0] += e0;
+          s2[1] += e1;
+          w[i / 2] = pack2_bf16(e0, e1);
+        }
       }
       l_half = l_half * alpha + (s2[0] + s2[1]);
       if (j > 0) {  // the previous P V has read P and finished writing O
