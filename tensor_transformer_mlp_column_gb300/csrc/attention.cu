@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       tmem_ld_32cols(t_row + col0 + g, v);
       if (col0 + g + 32 <= p.seq) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], v[j]);
+        for (int j = 0; j < 32; j += 2) m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], v[j], v[j + 1]);
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -202,18 +202,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
       tmem_ld_32cols(t_row + col, v);
       uint32_t w[16];
       float s2[2] = {0.f, 0.f};
-      const bool full = col + 32 <= p.seq;
+      if (col + 32 <= p.seq) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float e0 = ex2_approx(fmaf(v[j], p.scale_log2, -mb));
-        float e1 = ex2_approx(fmaf(v[j + 1], p.scale_log2, -mb));
-        if (!full) {
-          e0 = col + j < p.seq ? e0 : 0.f;
-          e1 = col + j + 1 < p.seq ? e1 : 0.f;
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = ex2_approx(fmaf(v[j], p.scale_log2, -mb));
+          const float e1 = ex2_approx(fmaf(v[j + 1], p.scale_log2, -mb));
+          s2[0] += e0;
+          s2[1] += e1;
+          w[j / 2] = pack2_bf16(e0, e1);
         }
-        s2[0] += e0;
-        s2[1] += e1;
-        w[j / 2] = pack2_bf16(e0, e1);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float e0 = col + j < p.seq ? ex2_approx(fmaf(v[j], p.scale_log2, -mb)) : 0.f;
+          const float e1 = col + j + 1 < p.seq ? ex2_approx(fmaf(v[j + 1], p.scale_log2, -mb)) : 0.f;
+          s2[0] += e0;
+          s2[1] += e1;
+          w[j / 2] = pack2_bf16(e0, e1);
+        }
       }
       sum += s2[0] + s2[1];
       uint8_t* prow = p_chunk(sP, sK, col / 64) + row * 128;
