@@ -183,6 +183,34 @@ def _oracle_worker(target_s: float, reps: int, out_path: str):
     json.dump({"seconds": times, "rows": rows, "checksum": check}, open(out_path, "w"))
 
 
+def _oracle_rows_worker(out_path: str):
+    """Runs in a fresh interpreter: the oracle of the block and of attention on
+    bounded samples (a few seconds each), for the rows beside the MLP."""
+    import torch
+
+    import oracle
+    from tpmlp_inputs import ATTN_WORKLOADS, WORKLOADS, make_attn_inputs, make_block_inputs
+
+    res = {}
+    w = WORKLOADS["large"]
+    inp = make_block_inputs(w, seed=0)
+    x = inp["x"][:1024].to(torch.float64).numpy()
+    shards = oracle.shard_mlp(inp["A"].to(torch.float64).numpy(), inp["B"].to(torch.float64).numpy(), w.N)
+    del inp
+    t0 = time.perf_counter()
+    oracle.block_mlp(x, shards)
+    res["block"] = {"seconds": time.perf_counter() - t0, "rows": 1024}
+    del shards
+    a = ATTN_WORKLOADS["attn_seq512"]
+    ai = make_attn_inputs(a, seed=0)
+    f = {k: v.to(torch.float64).numpy() for k, v in ai.items()}
+    ash = oracle.shard_attention(f["Wq"], f["Wk"], f["Wv"], f["Wo"], a.heads, a.N)
+    t0 = time.perf_counter()
+    oracle.tp_attention(f["X"], a.batch, ash, a.heads)
+    res["attention"] = {"seconds": time.perf_counter() - t0, "sequences": a.batch}
+    json.dump(res, open(out_path, "w"))
+
+
 def run_oracle(target_s: float, reps: int, cores: int) -> dict:
     out = os.path.join("/tmp", f"tpmlp_oracle_{os.getpid()}.json")
     env = dict(os.environ)
@@ -204,9 +232,33 @@ def cpu_baseline(target_s: float = 12.0) -> dict:
     cores = len(os.sched_getaffinity(0))
     r = run_oracle(target_s, 1, cores)
     flops = 4.0 * r["rows"] * w.D * w.F
-    return {"value": flops / r["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"{r['rows']} of {w.T} token rows of the large workload, one float64 forward "
-                      f"(numpy, {r['seconds'][0]:.1f} s)"}
+    out = {"value": flops / r["seconds"][0] / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+           "sample": f"{r['rows']} of {w.T} token rows of the large workload, one float64 forward "
+                     f"(numpy, {r['seconds'][0]:.1f} s)"}
+    # The block's FFN half and head-split attention, timed the same way on small samples.
+    path = os.path.join("/tmp", f"tpmlp_oracle_rows_{os.getpid()}.json")
+    env = dict(os.environ)
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    subprocess.run([sys.executable, "-c", f"import bench; bench._oracle_rows_worker({path!r})"], cwd=ROOT, env=env,
+                   check=True)
+    rr = json.load(open(path))
+    os.remove(path)
+    from tpmlp_inputs import ATTN_WORKLOADS
+
+    a = ATTN_WORKLOADS["attn_seq512"]
+    per_seq_flops = a.fwd_flops() / a.batch
+    out["rows"] = {
+        "block": {"value": round(4.0 * rr["block"]["rows"] * w.D * w.F / rr["block"]["seconds"] / 1e12, 4),
+                  "unit": "TFLOP/s", "sample": f"{rr['block']['rows']} token rows of the large workload "
+                                               f"({rr['block']['seconds']:.1f} s)"},
+        "attention": {"value": round(rr["attention"]["sequences"] * per_seq_flops / rr["attention"]["seconds"] / 1e12,
+                                     4),
+                      "unit": "TFLOP/s", "sample": f"the seq-512 attention workload, {rr['attention']['sequences']} "
+                                                   f"sequences ({rr['attention']['seconds']:.1f} s)"},
+    }
+    return out
 
 
 # ------------------------------------------------------------------ GPU arm
