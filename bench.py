@@ -748,7 +748,9 @@ def bench_attention(args, local_rank, peaks):
             ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, mode), dtype=torch.uint8, device=dev)
             ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, stream, 50, 5)
             gms = _time_graph_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, 50)
-            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1),
+            tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+            res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                         "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4),
                          "graph_ms": round(gms, 4), "graph_TFLOP/s": round(w.fwd_flops() / (gms * 1e-3) / 1e12, 1)}
         tp.tpmlp_check_status(stream)
         sh.free()
@@ -763,8 +765,9 @@ def bench_attention(args, local_rank, peaks):
         Y = torch.empty((w.T, w.D), dtype=torch.float32, device=dev)
         ws = torch.empty(tp.tpmlp_attn_workspace_bytes(w.batch, w.seq, sh, "fused"), dtype=torch.uint8, device=dev)
         ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, "fused", Y, ws), dev, stream, 20, 3)
-        out[name] = {"batch": w.batch, "seq": w.seq, "fused": {"ms": round(ms, 4),
-                     "TFLOP/s": round(w.fwd_flops() / (ms * 1e-3) / 1e12, 1)}}
+        tf = w.fwd_flops() / (ms * 1e-3) / 1e12
+        out[name] = {"batch": w.batch, "seq": w.seq, "fused": {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
+                     "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4)}}
         tp.tpmlp_check_status(stream)
         sh.free()
     # heads time against seq: least squares on (1, seq, seq^2)
