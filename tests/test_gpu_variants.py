@@ -1,0 +1,86 @@
+"""The tensor-core GEMM variants that the environment selects (read once per
+process, so each runs in a child process): TPMLP_TC_KERNEL=0 (single-CTA
+tiles everywhere) and =2 (CTA quads sharing the M x K operand through TMA
+multicast). Each child checks, against the float64 oracle with the bf16
+tolerances, every epilogue the default pair kernel is tested with: GeLU,
+fp32 partials and the fused sum (TMA stores), the backward's activation step,
+the saved pre-activation, the block's residual, the sequence-parallel slice
+outputs and attention's QKV projection with V written transposed."""
+
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import numpy as np, torch
+import oracle
+import tensor_transformer_mlp_column_gb300 as tp
+from tpmlp_inputs import Workload, make_inputs, make_block_inputs, AttnWorkload, make_attn_inputs
+
+def check(got, ref, what):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    fro = np.linalg.norm(got - ref) / np.linalg.norm(ref); mx = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
+    assert fro <= 5e-3 and mx <= 2e-2, (what, fro, mx)
+
+f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+torch.cuda.set_device(0)
+# T=2048, D=2048, F=4096, N=4: every product has enough 256 x 256 tiles for pairs (or quads).
+w = Workload("v", 2048, 2048, 4096, 4, "bf16", 1.0, 0.02, 0.02, 1.0, True)
+inp = make_inputs(w, seed=71)
+X, A, B, dY = (f64(inp[k]) for k in ("X", "A", "B", "dY"))
+shards = oracle.shard_mlp(A, B, w.N)
+rows = list(range(0, w.T, 17))
+Y_ref = oracle.tp_mlp_rows(X, shards, rows)
+d = {k: v.cuda() for k, v in inp.items()}
+sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
+idx = torch.tensor(rows, device="cuda")
+for mode in ("faithful", "fused"):
+    check(f64(tp.tpmlp_forward(d["X"], sh, mode).index_select(0, idx)), Y_ref, "Y " + mode)
+Y, P = tp.tpmlp_forward_save(d["X"], sh, "fused")
+check(f64(P[1].index_select(0, idx)), X[rows] @ shards[1][0], "saved P")
+dX, dA, dB = tp.tpmlp_backward(d["X"], d["dY"], sh, "fused")
+check(f64(dX.index_select(0, idx)), oracle.tp_mlp_backward_dx_rows(X, dY, shards, rows), "dX")
+cols = list(range(0, w.Fs, 37))
+cidx = torch.tensor(cols, device="cuda")
+check(f64(dA[2].index_select(1, cidx)), oracle.grad_A_cols(X, dY, shards[2][0], shards[2][1], cols), "dA_2")
+check(f64(dB[3].index_select(0, cidx)), oracle.grad_B_rows(X, dY, shards[3][0], cols), "dB_3")
+bi = make_block_inputs(w, seed=72)
+x = f64(bi["x"])
+out = tp.tpmlp_block_forward(bi["x"].cuda(), tp.tpmlp_shard(bi["A"].cuda(), bi["B"].cuda(), w.N), "fused")
+check(f64(out.index_select(0, idx)), oracle.block_mlp_rows(x, oracle.shard_mlp(f64(bi["A"]), f64(bi["B"]), w.N), rows), "block")
+Ys = tp.tpmlp_forward_sp([c.clone() for c in torch.chunk(d["X"], w.N)], sh, "fused")
+assert torch.equal(torch.cat(Ys), tp.tpmlp_forward(d["X"], sh, "fused")), "sequence-parallel slices"
+aw = AttnWorkload("va", 4, 512, 1024, 16, 4, "bf16", 1.0, 0.03)
+ai = make_attn_inputs(aw, seed=73)
+a64 = {k: f64(v) for k, v in ai.items()}
+ash = oracle.shard_attention(a64["Wq"], a64["Wk"], a64["Wv"], a64["Wo"], aw.heads, aw.N)
+Ya_ref, parts = oracle.tp_attention(a64["X"], aw.batch, ash, aw.heads, return_partials=True)
+ad = {k: v.cuda() for k, v in ai.items()}
+sha = tp.tpmlp_attn_shard(ad["Wq"], ad["Wk"], ad["Wv"], ad["Wo"], aw.heads, aw.N)
+O = tp.tpmlp_attn_heads(ad["X"], aw.batch, sha)
+for i, (O_ref, _) in enumerate(parts):
+    check(f64(O[i]), O_ref, f"attention O_{i}")
+check(f64(tp.tpmlp_attn_forward(ad["X"], aw.batch, sha, "faithful")), Ya_ref, "attention Y")
+tp.tpmlp_check_status()
+print("ok")
+'''
+
+
+@pytest.mark.parametrize("family", ["0", "2"], ids=["single_cta", "quad"])
+def test_gemm_variant_against_oracle(family):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    env = dict(os.environ, TPMLP_TC_KERNEL=family)
+    r = subprocess.run([sys.executable, "-c", CHILD], env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
