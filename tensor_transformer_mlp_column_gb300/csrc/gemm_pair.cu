@@ -27,11 +27,27 @@ namespace tpmlp {
 
 namespace {
 
-template <int STAGES_>
+// A stage holds KSUB consecutive 64-column K blocks (each a 128-row tile of
+// 128-byte swizzled rows): two for the epilogues that need no output staging
+// (three stages of 64 KB: half the barrier round trips per MMA), one for the
+// TMA-store epilogue (six stages of 32 KB beside its 32 KB of staging) -
+// whichever measured faster.
+constexpr uint32_t kSubBytes = 128 * BK * 2;
+template <int EPI>
+constexpr int ksub_of() {
+  return EPI == kEpiF32Tma ? 1 : 2;
+}
+template <int EPI>
+constexpr int stages_of() {
+  return EPI == kEpiF32Tma ? 6 : 3;
+}
+
+template <int STAGES_, int KSUB_>
 struct PairCfg {
   static constexpr int STAGES = STAGES_;
-  static constexpr uint32_t A_BYTES = 128 * BK * 2;  // this CTA's 128 rows
-  static constexpr uint32_t B_BYTES = 128 * BK * 2;  // this CTA's half of the 256 N rows
+  static constexpr int KSUB = KSUB_;
+  static constexpr uint32_t A_BYTES = KSUB * kSubBytes;  // this CTA's 128 rows
+  static constexpr uint32_t B_BYTES = KSUB * kSubBytes;  // this CTA's half of the 256 N rows
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
   // kEpiF32Tma: two 32 x 32 fp32 staging blocks (4 KB each) per epilogue warp.
@@ -48,7 +64,7 @@ struct PairCfg {
 
 template <int EPI, int STAGES, bool QUAD>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ KParams p) {
-  using C = PairCfg<STAGES>;
+  using C = PairCfg<STAGES, ksub_of<EPI>()>;
   constexpr int BN = 256;
   constexpr uint32_t kCtas = QUAD ? 4 : 2;
   extern __shared__ uint8_t smem_raw[];
@@ -119,33 +135,43 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         const int m0 = mb * 256 + static_cast<int>(pos) * 128;
         const int nb256 = QUAD ? 2 * nb + static_cast<int>(pq) : nb;
         const int n0 = nb256 * BN + static_cast<int>(pos) * 128;
-        int gg = g, kk = 0;  // group and K block of the next fill (chain mode walks the groups in order)
-        for (int kb = 0; kb < kb_per_tile; ++kb, ++kk) {
-          if (kk == p.k_blocks) {
-            kk = 0;
-            ++gg;
-          }
+        int gg = g, kk = 0;  // group and K block of the next load (chain mode walks the groups in order)
+        for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
             aborted = true;
             break;
           }
           const uint32_t full_lead = map_to_cta(smem_addr(full + stage), lead);
+          const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;  // K blocks in this stage
           ++fill;
           if (fill != p.inject) {
             if (pos == 0) {
-              mbar_arrive_expect_tx(full + stage, 2 * C::STAGE_BYTES);
+              mbar_arrive_expect_tx(full + stage, 2 * 2 * nsub * kSubBytes);  // both CTAs' A and B
               armed |= 1u << stage;
               parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
             }
-            if constexpr (QUAD) {
-              // 64 of this position's 128 M x K rows, to this CTA and its twin in the other pair.
-              const uint16_t mask = static_cast<uint16_t>((1u << pos) | (1u << (2 + pos)));
-              tma_load_2d_pair_multicast(sA + stage * C::A_BYTES + pq * (C::A_BYTES / 2), &p.map_a[gg], kk * BK,
-                                         m0 + static_cast<int>(pq) * 64, full_lead, mask);
-            } else {
-              tma_load_2d_pair(sA + stage * C::A_BYTES, &p.map_a[gg], kk * BK, m0, full_lead);
+            for (int u = 0; u < nsub; ++u) {
+              uint8_t* a_dst = sA + stage * C::A_BYTES + u * kSubBytes;
+              if constexpr (QUAD) {
+                // 64 of this position's 128 M x K rows, to this CTA and its twin in the other pair.
+                const uint16_t mask = static_cast<uint16_t>((1u << pos) | (1u << (2 + pos)));
+                tma_load_2d_pair_multicast(a_dst + pq * (kSubBytes / 2), &p.map_a[gg], kk * BK,
+                                           m0 + static_cast<int>(pq) * 64, full_lead, mask);
+              } else {
+                tma_load_2d_pair(a_dst, &p.map_a[gg], kk * BK, m0, full_lead);
+              }
+              tma_load_2d_pair(sB + stage * C::B_BYTES + u * kSubBytes, &p.map_b[gg], kk * BK, n0, full_lead);
+              if (++kk == p.k_blocks) {
+                kk = 0;
+                ++gg;
+              }
             }
-            tma_load_2d_pair(sB + stage * C::B_BYTES, &p.map_b[gg], kk * BK, n0, full_lead);
+          } else {
+            for (int u = 0; u < nsub; ++u)  // the withheld fill still advances the K position
+              if (++kk == p.k_blocks) {
+                kk = 0;
+                ++gg;
+              }
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -184,18 +210,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < kb_per_tile; ++kb) {
+        for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
             aborted = true;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES);
-          const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES);
+          const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;
+          for (int u = 0; u < nsub; ++u) {
+            const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES + u * kSubBytes);
+            const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES + u * kSubBytes);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
-                             (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+                               (kb | u | k) != 0 ? 1u : 0u);
+            }
           }
           tc_commit_pair_multicast(empty + stage, kStageMask);  // frees the stage once these MMAs have read it
           if (++stage == C::STAGES) {
@@ -304,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
 
 template <int EPI, int STAGES, bool QUAD>
 cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
-  using C = PairCfg<STAGES>;
+  using C = PairCfg<STAGES, ksub_of<EPI>()>;
   constexpr size_t kSmem = C::template smem<EPI>();
   constexpr unsigned kCtas = QUAD ? 4 : 2;
   auto kern = tc_gemm_pair_kernel<EPI, STAGES, QUAD>;
@@ -344,17 +373,17 @@ template <bool QUAD>
 cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
   switch (epi) {
     case kEpiGeluBf16:
-      return launch_impl<kEpiGeluBf16, 6, QUAD>(kp, s);
+      return launch_impl<kEpiGeluBf16, stages_of<kEpiGeluBf16>(), QUAD>(kp, s);
     case kEpiF32:
-      return launch_impl<kEpiF32, 6, QUAD>(kp, s);
+      return launch_impl<kEpiF32, stages_of<kEpiF32>(), QUAD>(kp, s);
     case kEpiBwdAct:
-      return launch_impl<kEpiBwdAct, 6, QUAD>(kp, s);
+      return launch_impl<kEpiBwdAct, stages_of<kEpiBwdAct>(), QUAD>(kp, s);
     case kEpiF32Tma:
-      return launch_impl<kEpiF32Tma, 6, QUAD>(kp, s);
+      return launch_impl<kEpiF32Tma, stages_of<kEpiF32Tma>(), QUAD>(kp, s);
     case kEpiGeluSaveP:
-      return launch_impl<kEpiGeluSaveP, 6, QUAD>(kp, s);
+      return launch_impl<kEpiGeluSaveP, stages_of<kEpiGeluSaveP>(), QUAD>(kp, s);
     case kEpiBf16:
-      return launch_impl<kEpiBf16, 6, QUAD>(kp, s);
+      return launch_impl<kEpiBf16, stages_of<kEpiBf16>(), QUAD>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }
