@@ -48,7 +48,7 @@ TRAFFIC_BYTES = {
 
 
 # The sources of the step's kernels and of their launch parameters.
-STEP_SOURCES = ["api.cu", "device.cuh", "elementwise.cu", "gemm_common.cuh", "gemm_pair.cu", "gemm_tc.cu"]
+STEP_SOURCES = ["api.cu", "device.cuh", "elementwise.cu", "gemm_common.cuh", "gemm_pair.cu", "gemm_tc.cu", "internal.h"]
 
 
 def source_hash() -> str:

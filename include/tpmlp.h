@@ -20,6 +20,11 @@
  *     aligned (TPMLP_ERR_ALIGN otherwise).
  *   - Every call that takes a stream only enqueues work on it and returns; the
  *     results are ready when that stream has reached the point of the call.
+ *     Kernels are launched with programmatic dependent launch: each one's
+ *     set-up overlaps the end of the previous kernel in the stream, and it
+ *     waits for that kernel to complete before it reads or writes global
+ *     memory, so stream order is kept (environment variable TPMLP_PDL=0
+ *     launches them plainly).
  *   - The return value is TPMLP_OK (0) or a negative tpmlp_status. On error
  *     nothing has been enqueued, and tpmlp_last_error() gives a message.
  *   - Kernels never trap. A device-side wait that runs past its time limit

@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // set-up done: wait for the kernel that wrote Q, K and V
+  pdl_launch_dependents();
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
 
   const int32_t row0 = b * p.seq;  // first token of the sequence
@@ -396,6 +398,8 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // set-up done: wait for the kernel that wrote Q, K and V
+  pdl_launch_dependents();
   const uint32_t tS = tmem, tO = tmem + 128;
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
   const int32_t row0 = b * p.seq;
@@ -691,16 +695,14 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kStrmSmem));
     if (e != cudaSuccess) return e;
-    attn_stream_kernel<<<grid, kStrmThreads, kStrmSmem, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(attn_stream_kernel, grid, dim3(kStrmThreads), kStrmSmem, s, p);
   }
   const int nkv = (a.seq + 127) / 128, nch = (a.seq + 63) / 64;
   const uint32_t smem = attn_smem_bytes(nkv, nch);
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(attn_smem_bytes(4, 8)));
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<<<grid, kAttnThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel, grid, dim3(kAttnThreads), smem, s, p);
 }
 
 cudaError_t launch_attention_f32(const float* qkv, int64_t T, int n, int Dn, int dh, int local_heads, int batch,

@@ -282,6 +282,8 @@ template <typename E, int THREADS, int C>
 __global__ void __launch_bounds__(THREADS) layer_norm_reg_kernel(const E* __restrict__ x, int64_t T, int D, float eps,
                                                                  E* __restrict__ y) {
   __shared__ float red[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const int nch = D >> 3;
   Raw8<E> nxt[C];
   int64_t t = blockIdx.x;
@@ -330,6 +332,8 @@ __global__ void __launch_bounds__(THREADS) layer_norm_bwd_reg_kernel(const float
                                                                      const E* __restrict__ dout, int64_t T, int D,
                                                                      float eps, float* __restrict__ dx) {
   __shared__ float red[64];
+  pdl_wait();
+  pdl_launch_dependents();
   const int nch = D >> 3;
   const int c = threadIdx.x;
   const bool on = c < nch;
@@ -423,8 +427,7 @@ int pow2_threads(int v) {
 template <typename E, int THREADS, int C>
 cudaError_t ln_reg(const E* x, int64_t T, int D, float eps, E* y, cudaStream_t s) {
   auto k = layer_norm_reg_kernel<E, THREADS, C>;
-  k<<<row_grid(k, THREADS, 0, T), THREADS, 0, s>>>(x, T, D, eps, y);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(row_grid(k, THREADS, 0, T)), dim3(THREADS), 0, s, x, T, D, eps, y);
 }
 
 // Forward: two chunks per thread where the row allows (so each thread has
@@ -462,8 +465,7 @@ template <typename E, int THREADS>
 cudaError_t lnb_reg(const float* G, int n, const E* x, const E* dout, int64_t T, int D, float eps, float* dx,
                     cudaStream_t s) {
   auto k = layer_norm_bwd_reg_kernel<E, THREADS>;
-  k<<<row_grid(k, THREADS, 0, T), THREADS, 0, s>>>(G, n, x, dout, T, D, eps, dx);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(row_grid(k, THREADS, 0, T)), dim3(THREADS), 0, s, G, n, x, dout, T, D, eps, dx);
 }
 
 // Backward tail: one chunk per thread up to D = 8192, else the shared-memory kernel.

@@ -91,6 +91,19 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint6
   return true;
 }
 
+// ------------------------------------------------------------------ dependent launch
+//
+// Kernels launched with programmatic stream serialisation may start while the
+// previous kernel of the stream is still running: they set up shared memory,
+// barriers and tensor memory, then wait here until that kernel has completed
+// and its writes are visible, before touching global memory. Without the
+// launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel of the stream start its own set-up.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

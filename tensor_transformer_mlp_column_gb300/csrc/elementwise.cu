@@ -78,6 +78,8 @@ template <int NMAX>
 __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __restrict__ Yp, int n, int64_t count,
                                                                const void* __restrict__ res, int res_kind,
                                                                OutSlices out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t slice = count / gridDim.y;
   const int64_t base4 = int64_t(blockIdx.y) * (slice / 4);
   float* __restrict__ Y = out.p[blockIdx.y];
@@ -115,6 +117,8 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
 // Any n and any slice length: the same order, shards taken from memory one by one.
 __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, const void* __restrict__ res,
                                      int res_kind, OutSlices out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int64_t slice = count / gridDim.y;
   const int64_t base = int64_t(blockIdx.y) * slice;
   float* __restrict__ Y = out.p[blockIdx.y];
@@ -132,6 +136,8 @@ __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_
 // Each thread moves four words per pass, all four loads issued first.
 template <typename W>
 __global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__ out) {
+  pdl_wait();
+  pdl_launch_dependents();
   const W* __restrict__ src = static_cast<const W*>(in.p[blockIdx.y]);
   W* __restrict__ dst = out + int64_t(blockIdx.y) * words;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -237,19 +243,14 @@ cudaError_t launch_reduce_scatter(const float* Yp, int n, int64_t count, const O
   const unsigned gy = static_cast<unsigned>(nslices);
   if (slice % 4 != 0) {  // slices would not be 16-byte aligned
     dim3 g(static_cast<unsigned>((ew_grid(count, 1) + nslices - 1) / nslices), gy);
-    allreduce_any_kernel<<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
-    return cudaGetLastError();
+    return launch_pdl(allreduce_any_kernel, g, dim3(kEwThreads), 0, s, Yp, n, count, res, res_kind, out);
   }
   dim3 g(static_cast<unsigned>((ew_grid(count, 4) + nslices - 1) / nslices), gy);
-  if (n <= 4)
-    allreduce_kernel<4><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
-  else if (n <= 8)
-    allreduce_kernel<8><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
-  else if (n <= 16)
-    allreduce_kernel<16><<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
-  else
-    allreduce_any_kernel<<<g, kEwThreads, 0, s>>>(Yp, n, count, res, res_kind, out);
-  return cudaGetLastError();
+  const dim3 b(kEwThreads);
+  if (n <= 4) return launch_pdl(allreduce_kernel<4>, g, b, 0, s, Yp, n, count, res, res_kind, out);
+  if (n <= 8) return launch_pdl(allreduce_kernel<8>, g, b, 0, s, Yp, n, count, res, res_kind, out);
+  if (n <= 16) return launch_pdl(allreduce_kernel<16>, g, b, 0, s, Yp, n, count, res, res_kind, out);
+  return launch_pdl(allreduce_any_kernel, g, b, 0, s, Yp, n, count, res, res_kind, out);
 }
 
 cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s, const void* res,
@@ -266,17 +267,17 @@ cudaError_t launch_all_gather(const InSlices& in, int nslices, int64_t slice_byt
   auto gx = [&](int64_t words) {
     return static_cast<unsigned>((ew_grid(words * nslices, 4) + nslices - 1) / nslices);
   };
+  const dim3 b(kEwThreads);
   if (slice_bytes % 16 == 0) {
     const int64_t w = slice_bytes / 16;
-    gather_slices_kernel<uint4><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint4*>(out));
-  } else if (slice_bytes % 4 == 0) {
-    const int64_t w = slice_bytes / 4;
-    gather_slices_kernel<uint32_t><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint32_t*>(out));
-  } else {
-    const int64_t w = slice_bytes / 2;
-    gather_slices_kernel<uint16_t><<<dim3(gx(w), gy), kEwThreads, 0, s>>>(in, w, static_cast<uint16_t*>(out));
+    return launch_pdl(gather_slices_kernel<uint4>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint4*>(out));
   }
-  return cudaGetLastError();
+  if (slice_bytes % 4 == 0) {
+    const int64_t w = slice_bytes / 4;
+    return launch_pdl(gather_slices_kernel<uint32_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint32_t*>(out));
+  }
+  const int64_t w = slice_bytes / 2;
+  return launch_pdl(gather_slices_kernel<uint16_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint16_t*>(out));
 }
 
 cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_table, int64_t D, int64_t F,

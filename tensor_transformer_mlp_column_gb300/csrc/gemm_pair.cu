@@ -113,6 +113,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   cluster_sync_all();  // barriers of every CTA initialised, TMEM allocated
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up done: from here on global memory is read and written, so wait for
+  // the previous kernel of the stream, and let the next one start its set-up.
+  pdl_wait();
+  pdl_launch_dependents();
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
   const uint32_t abort_addr = smem_addr(const_cast<int*>(abort_flag));
   auto raise_abort_in_cluster = [&]() {
@@ -339,17 +343,19 @@ cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   auto kern = tc_gemm_pair_kernel<EPI, STAGES, QUAD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kCtas;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // Persistent grid: as many clusters as can be resident at once (per device
   // and per instantiation, since the shared-memory size differs).
   static int max_clusters[64] = {0};
@@ -360,7 +366,9 @@ cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   if (!cached) {
     cfg.gridDim = dim3(kCtas * (num_sms() / kCtas), 1, 1);
     int n = 0;
+    cfg.numAttrs = 1;  // the query takes the cluster shape only
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    cfg.numAttrs = 2;
     if (e != cudaSuccess) return e;
     cached = n > 0 ? n : 1;
   }

@@ -82,6 +82,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // Set-up done: from here on global memory is read and written, so wait for
+  // the previous kernel of the stream, and let the next one start its set-up.
+  pdl_wait();
+  pdl_launch_dependents();
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
   const int kb_per_tile = p.chain ? p.groups * p.k_blocks : p.k_blocks;
 
@@ -230,7 +234,8 @@ cudaError_t launch_single(const KParams& kp, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(C::SMEM));
   if (e != cudaSuccess) return e;
   const int grid = kp.tiles < num_sms() ? kp.tiles : num_sms();
-  kern<<<grid, kThreads, C::SMEM, s>>>(kp);
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), C::SMEM, s, kp);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -302,6 +307,12 @@ int* status_word() {
 }  // namespace
 
 int* device_status_word() { return status_word(); }
+
+bool pdl_enabled() {
+  static int v = -1;
+  if (v < 0) v = env_int("TPMLP_PDL", 1) != 0 ? 1 : 0;
+  return v == 1;
+}
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns);

@@ -174,6 +174,25 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s);
 
 int num_sms();
 
+// Programmatic dependent launch (TPMLP_PDL=0 turns it off): the kernels that
+// start with pdl_wait() are launched with this, so their set-up overlaps the
+// tail of the previous kernel in the stream.
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // Records the calling thread's error message (what tpmlp_last_error returns)
 // and returns `code`.
 int set_error(int code, const char* fmt, ...);
