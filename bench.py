@@ -37,13 +37,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # one pass; command and figures in profiles/traffic_large_forward.md). Valid
 # only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
-TRAFFIC_SOURCE_HASH = "8f8f89620345b20b"
+TRAFFIC_SOURCE_HASH = "deae8c21f25373fd"
 TRAFFIC_BYTES = {
-    "gemm1_gelu(faithful)": 1_233_763_840,
-    "gemm2_partials": 2_951_160_832,
-    "allreduce": 2_400_492_800,
-    "gemm1_gelu(fused)": 1_232_971_776,
-    "gemm2_fused_sum": 2_774_459_392,
+    "gemm1_gelu(faithful)": 1_302_671_616,
+    "gemm2_partials": 3_016_257_536,
+    "allreduce": 2_401_393_408,
+    "gemm1_gelu(fused)": 1_267_046_400,
+    "gemm2_fused_sum": 4_184_780_800,
 }
 
 
