@@ -202,6 +202,33 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Split form of tmem_ld_32cols for software pipelining: tmem_ld_32cols_issue
+// starts the load, tmem_ld_wait waits for every load of the thread issued so
+// far. The registers pass through the wait as operands, so no use of them can
+// be scheduled before it.
+__device__ __forceinline__ void tmem_ld_32cols_issue(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 // ------------------------------------------------------------------ CTA pairs (cta_group::2)
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -235,6 +262,13 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Arrive on a barrier in any CTA of the cluster (cluster address).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// The same arrival without release semantics: for signals that order only
+// tensor-memory reads already completed by tcgen05.wait::ld, so the arrival
+// need not wait for the thread's outstanding global stores.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
@@ -331,6 +365,25 @@ __device__ __forceinline__ float gelu_fast(float x) {
   const float k1 = 0.044715f;
   const float u = k0 * x * fmaf(k1, x * x, 1.0f);
   return __fdividef(x, 1.0f + __expf(-2.0f * u));
+}
+
+// GeLU for a result that is rounded to bf16: x/2 (1 + tanh u) with the
+// hardware tanh approximation (tanh.approx.f32), one special-function
+// instruction instead of the exponential and the reciprocal of gelu_fast,
+// which halves the epilogue's special-function work. Its error, about
+// 2^-11 |x| / 2 in absolute terms, is below bf16 rounding of the result except
+// in the negative tail (x < -2), where the result itself is near zero.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_bf16_fast(float x) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  const float h = 0.5f * x;
+  const float u = k0 * x * fmaf(k1, x * x, 1.0f);
+  return fmaf(h, tanh_approx(u), h);
 }
 
 // GeLU and its derivative at x: with s = sigmoid(2u),

@@ -158,10 +158,10 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
     for (int j = 0; j < 4; ++j) {
       if (n0 + 8 * j + 8 <= p.N) {
         uint4 w;
-        w.x = pack_bf16x2(gelu_fast(v[8 * j + 0]), gelu_fast(v[8 * j + 1]));
-        w.y = pack_bf16x2(gelu_fast(v[8 * j + 2]), gelu_fast(v[8 * j + 3]));
-        w.z = pack_bf16x2(gelu_fast(v[8 * j + 4]), gelu_fast(v[8 * j + 5]));
-        w.w = pack_bf16x2(gelu_fast(v[8 * j + 6]), gelu_fast(v[8 * j + 7]));
+        w.x = pack_bf16x2(gelu_bf16_fast(v[8 * j + 0]), gelu_bf16_fast(v[8 * j + 1]));
+        w.y = pack_bf16x2(gelu_bf16_fast(v[8 * j + 2]), gelu_bf16_fast(v[8 * j + 3]));
+        w.z = pack_bf16x2(gelu_bf16_fast(v[8 * j + 4]), gelu_bf16_fast(v[8 * j + 5]));
+        w.w = pack_bf16x2(gelu_bf16_fast(v[8 * j + 6]), gelu_bf16_fast(v[8 * j + 7]));
         store16(out + 8 * j, w, p.stream_out);
         if constexpr (EPI == kEpiGeluSaveP) {
           float* P = static_cast<float*>(p.out2[g]) + m * p.ldo + n0 + 8 * j;

@@ -270,27 +270,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       const int64_t m = m_warp + lane;
       const bool row_ok = m < p.M;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        float v[32];
+      // The 256 columns in chunks of 32, software-pipelined: the tcgen05.ld
+      // of the next chunk (and its residual load) is in flight while the
+      // current chunk is converted and stored.
+      auto with_res = [&](int n0) {
+        return (EPI == kEpiF32 || EPI == kEpiF32Tma) && p.resid != nullptr && row_ok && n0 < p.N;
+      };
+      auto issue = [&](int c, uint32_t (&r)[32], uint4 (&res)[4]) {
         const int n0 = nb256 * BN + c;
-        uint4 res[4];
-        const bool with_res = (EPI == kEpiF32 || EPI == kEpiF32Tma) && p.resid != nullptr && row_ok && n0 < p.N;
-        if (with_res) load_residual(p, m, n0, res);
+        if (with_res(n0)) load_residual(p, m, n0, res);
         __syncwarp();
-        tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
-        if (with_res) add_residual(res, v);
-        if (c + 32 == BN) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
-        }
+        tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c), r);
+      };
+      auto finish = [&](int c, const uint32_t (&r)[32], const uint4 (&res)[4]) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        const int n0 = nb256 * BN + c;
+        if (with_res(n0)) add_residual(res, v);
         if constexpr (EPI == kEpiF32Tma) {
           // Stage the warp's 32 x 32 fp32 block in shared memory with the
           // 128-byte swizzle (16-byte chunk j of row r at slot j ^ (r % 8),
           // conflict-free for these row-per-lane writes), then one TMA store
           // writes it as whole 128-byte lines, clipped to M x N.
-          if (n0 >= p.N || m_warp >= p.M) continue;  // warp-uniform
+          if (n0 >= p.N || m_warp >= p.M) return;  // warp-uniform
           uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
           if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
           __syncwarp();
@@ -311,8 +314,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           }
           ++blocks_out;
         } else {
-          if (!row_ok || n0 >= p.N) continue;
+          if (!row_ok || n0 >= p.N) return;
           epilogue_store<EPI>(p, g, m, n0, v);
+        }
+      };
+      uint32_t ra[32], rb[32];
+      uint4 resa[4], resb[4];
+      issue(0, ra, resa);
+      tmem_ld_wait(ra);
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 64) {
+        issue(c + 32, rb, resb);
+        finish(c, ra, resa);
+        __syncwarp();
+        tmem_ld_wait(rb);
+        if (c + 64 == BN) {
+          // Every column of the accumulator is in registers: hand it back to
+          // the MMA issuer. The arrival orders only these completed TMEM reads,
+          // so it is relaxed and does not wait for this thread's stores.
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
+        } else {
+          issue(c + 64, ra, resa);
+        }
+        finish(c + 32, rb, resb);
+        if (c + 64 < BN) {
+          __syncwarp();
+          tmem_ld_wait(ra);
         }
       }
       if (++acc == 2) {

@@ -91,6 +91,33 @@ def test_gelu_extremes(tp):
 
 # ----------------------------------------------------------------- shard slicing
 
+@pytest.mark.parametrize("D,F,n", [(1024, 4096, 4), (128, 512, 2)], ids=["pair_kernel", "single_cta_kernel"])
+def test_gemm_epilogue_gelu_pointwise(tp, D, F, n):
+    """The GeLU of the bf16 GEMM epilogue, element by element: with X = I the
+    pre-activations P_i = X A_i are exactly A's bf16 entries, swept over
+    [-8, 8], so every H_i[t, f] must be GeLU(A[t, i F/n + f]) up to the bf16
+    rounding of the result (2^-9 relative) and the hardware tanh's error
+    (below 2^-11 |x| / 2 absolute)."""
+    T = D
+    X = torch.eye(D, dtype=torch.bfloat16)
+    g = torch.Generator().manual_seed(3)
+    A = ((torch.rand((D, F), generator=g) * 2 - 1) * 8).to(torch.bfloat16)
+    A[0, :16] = torch.tensor([0, 1, -1, 2, -2, 3, -3, 4, -4, 6, -6, 8, -8, 0.5, -0.5, 1.5], dtype=torch.bfloat16)
+    B = (torch.randn((F, D), generator=g) * 0.02).to(torch.bfloat16)
+    sh = tp.tpmlp_shard(A.cuda(), B.cuda(), n)
+    H = f64(tp.tpmlp_hidden(X.cuda(), sh))  # [n, T, F/n]
+    a = f64(A)
+    ref = oracle.gelu(a)
+    got = np.concatenate([H[i] for i in range(n)], axis=1)  # back to [T, F]
+    assert got.shape == (T, F)
+    bound = 2.0**-8 * np.abs(ref) + 2.0**-11 * np.abs(a) + 1e-6
+    worst = np.max(np.abs(got - ref) - bound)
+    assert worst <= 0, f"GeLU epilogue off by {worst:.3e} beyond the bound"
+    pos = a >= 0
+    assert np.max(np.abs(got - ref)[pos] / np.maximum(np.abs(ref[pos]), 1e-30)) <= 2.0**-8 + 2.0**-10
+    sh.free()
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("D,F,n", [(64, 256, 4), (24, 96, 3), (8, 8, 1), (136, 1152, 16)])
 def test_shard_slices_bit_exact(tp, dtype, D, F, n):
