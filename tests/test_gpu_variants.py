@@ -1,11 +1,13 @@
-"""The tensor-core GEMM variants that the environment selects (read once per
+"""Launch variants that the environment selects (read once per
 process, so each runs in a child process): TPMLP_TC_KERNEL=0 (single-CTA
 tiles everywhere) and =2 (CTA quads sharing the M x K operand through TMA
 multicast). Each child checks, against the float64 oracle with the bf16
 tolerances, every epilogue the default pair kernel is tested with: GeLU,
 fp32 partials and the fused sum (TMA stores), the backward's activation step,
 the saved pre-activation, the block's residual, the sequence-parallel slice
-outputs and attention's QKV projection with V written transposed."""
+outputs and attention's QKV projection with V written transposed. TPMLP_PDL=0
+(kernels launched without programmatic dependent launch) must reproduce the
+default's results bit for bit."""
 
 import os
 import subprocess
@@ -84,3 +86,59 @@ def test_gemm_variant_against_oracle(family):
     env = dict(os.environ, TPMLP_TC_KERNEL=family)
     r = subprocess.run([sys.executable, "-c", CHILD], env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+
+
+# Programmatic dependent launch on (the default) and off (TPMLP_PDL=0, also read
+# once per process): every call must give the same bits either way, since each
+# kernel waits for its predecessor before its first global access.
+PDL_CHILD = r'''
+import sys, torch
+import tensor_transformer_mlp_column_gb300 as tp
+from tpmlp_inputs import Workload, make_inputs, make_block_inputs, AttnWorkload, make_attn_inputs
+torch.cuda.set_device(0)
+out = {}
+for name, T, D, F, N in (("pair", 1000, 1024, 4096, 4), ("single", 96, 128, 512, 2)):
+    w = Workload(name, T, D, F, N, "bf16", 1.0, 0.02, 0.02, 1.0, True)
+    inp = {k: v.cuda() for k, v in make_inputs(w, seed=81).items()}
+    sh = tp.tpmlp_shard(inp["A"], inp["B"], w.N)
+    bi = {k: v.cuda() for k, v in make_block_inputs(w, seed=82, with_dout=True).items()}
+    shb = tp.tpmlp_shard(bi["A"], bi["B"], w.N)
+    for mode in ("faithful", "fused"):
+        k = f"{name}_{mode}_"
+        out[k + "Y"] = tp.tpmlp_forward(inp["X"], sh, mode)
+        dX, dA, dB = tp.tpmlp_backward(inp["X"], inp["dY"], sh, mode)
+        out[k + "dX"], out[k + "dA"], out[k + "dB"] = dX, torch.stack(list(dA)), torch.stack(list(dB))
+        out[k + "block"] = tp.tpmlp_block_forward(bi["x"], shb, mode)
+        out[k + "block_dx"] = tp.tpmlp_block_backward(bi["x"], bi["dout"], shb, mode)[0]
+        out[k + "sp"] = torch.cat(tp.tpmlp_forward_sp([c.clone() for c in torch.chunk(inp["X"], w.N)], sh, mode))
+aw = AttnWorkload("pa", 2, 256, 512, 8, 2, "bf16", 1.0, 0.03)
+ai = {k: v.cuda() for k, v in make_attn_inputs(aw, seed=83).items()}
+sha = tp.tpmlp_attn_shard(ai["Wq"], ai["Wk"], ai["Wv"], ai["Wo"], aw.heads, aw.N)
+for mode in ("faithful", "fused"):
+    out["attn_" + mode] = tp.tpmlp_attn_forward(ai["X"], aw.batch, sha, mode)
+torch.cuda.synchronize()
+tp.tpmlp_check_status()
+torch.save({k: v.cpu() for k, v in out.items()}, sys.argv[1])
+print("ok")
+'''
+
+
+def test_dependent_launch_off_gives_identical_bits(tmp_path):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    results = {}
+    for flag in ("1", "0"):
+        path = str(tmp_path / f"pdl{flag}.pt")
+        env = dict(os.environ, TPMLP_PDL=flag)
+        r = subprocess.run([sys.executable, "-c", PDL_CHILD, path], env=env, cwd=ROOT, capture_output=True,
+                           text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+        results[flag] = torch.load(path)
+    assert results["1"].keys() == results["0"].keys()
+    for k in results["1"]:
+        assert torch.equal(results["1"][k], results["0"][k]), f"{k} differs with dependent launch off"
