@@ -365,12 +365,13 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   uint64_t* k_empty = bars + 3;  // [2]
   uint64_t* v_full = bars + 5;
   uint64_t* s_full = bars + 6;
-  uint64_t* s_free = bars + 7;   // one arrival per softmax warp: S read, P written, O rescaled
+  uint64_t* s_free = bars + 7;   // one arrival per softmax warp: P written, O rescaled
   uint64_t* o_done = bars + 8;
   uint64_t* x_bar = bars + 9;    // one arrival per softmax warp: the halves' partial maxima (sums) written
   uint64_t* drain = bars + 10;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* s_read = bars + 11;  // one arrival per softmax warp: its S columns are in registers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
 
   const int nkv = (p.seq + 127) / 128;
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
@@ -387,6 +388,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     mbar_init(v_full, 1);
     mbar_init(s_full, 1);
     mbar_init(s_free, kStrmSoftmaxWarps);
+    mbar_init(s_read, kStrmSoftmaxWarps);
     mbar_init(o_done, 1);
     mbar_init(x_bar, kStrmSoftmaxWarps);
     mbar_init(drain, 1);
@@ -427,7 +429,9 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
         if (j < nkv) {
           const int slot = j & 1;
           ok = wait_bounded(k_full + slot, (j >> 1) & 1, guard, kSiteProducer);
-          if (ok && j > 0) ok = wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);  // S of block j-1 read
+          // S_j overwrites S_{j-1} once every softmax warp holds its columns,
+          // so this product overlaps the softmax of block j-1.
+          if (ok && j > 0) ok = wait_bounded(s_read, (j - 1) & 1, guard, kSiteMmaAcc);
           if (!ok) break;
           tc_fence_after_sync();
           const uint64_t dk = smem_desc_sw128(smem_addr(sK + slot * kStrmKBytes));
@@ -435,12 +439,10 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
           for (int k = 0; k < 4; ++k) tc_mma_bf16(tS, dq + 2 * k, dk + 2 * k, kIdS, k > 0 ? 1u : 0u);
           tc_commit(s_full);
           tc_commit(k_empty + slot);
-        } else {
-          ok = wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);  // the last block's P written
-          if (!ok) break;
         }
-        if (j > 0) {  // O (+)= P_{j-1} V_{j-1}
-          ok = wait_bounded(v_full, (j - 1) & 1, guard, kSiteProducer);
+        if (j > 0) {  // O (+)= P_{j-1} V_{j-1}, once P_{j-1} is written and O rescaled
+          ok = wait_bounded(v_full, (j - 1) & 1, guard, kSiteProducer) &&
+               wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);
           if (!ok) break;
           tc_fence_after_sync();
 #pragma unroll
@@ -491,6 +493,9 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
           v[32 + i] = __uint_as_float(r1[i]);
         }
       }
+      tc_fence_before_sync();  // S may be overwritten by the next block's product now
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_read);
       const int kbase = j * 128 + half * 64;  // key of column 0 of this half
       const bool full = kbase + 64 <= p.seq;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
