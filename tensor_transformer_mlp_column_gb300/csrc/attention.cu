@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / p.local_heads, hl = gh % p.local_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  constexpr uint32_t kCols = 256;  // S: columns 0..127, O: 128..191
+  constexpr uint32_t kCols = 256;  // S: columns 0..127; O_0, O_1 (the two key halves): 128..191, 192..255
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
             const uint64_t dv = smem_desc_sw128(smem_addr(sVt + c * kVtChunkBytes));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              tc_mma_bf16(tO, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || c > 0 || k > 0) ? 1u : 0u);
+              tc_mma_bf16(tO + 64u * c, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || k > 0) ? 1u : 0u);
           }
           tc_commit(o_done);
           if (j < nkv) {  // V^T of block j into the slot once that product has read it
@@ -472,10 +472,16 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     }
   } else {
     // ---------------- softmax warps
+    // Warp (quarter, half) owns query rows 32*quarter.. and the 64 keys of
+    // its half of every block, with a running maximum, a row sum and an
+    // output accumulator O_half of its own, so the two warps of a row never
+    // wait for each other inside the loop; their partial results are merged
+    // once at the end.
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float m_run = -INFINITY, l_half = 0.f;
+    const uint32_t tOh = tO + lane_off + 64u * half;  // this warp's rows of O_half
+    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       ok = __all_sync(0xffffffffu, ok && wait_bounded(s_full, j & 1, guard, kSiteMmaFull));
@@ -507,18 +513,14 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
         for (int i = 0; i < 64; ++i)
           if (kbase + i < p.seq) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
       }
-      red_max[half * 128 + row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(x_bar);
-      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, j & 1, guard, kSiteEpilogue));
-      if (!ok) break;
+      const float m_blk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       // The running maximum moves only when the block's exceeds it by more
       // than 8 in log2 units: until then the weights stay <= 2^8 (well inside
       // fp32 and bf16 range) and O needs no rescale; the final division by l
-      // is the same either way.
-      const float m_blk = fmaxf(red_max[row], red_max[128 + row]);
-      const float m_new = (m_blk - m_run) * p.scale_log2 > 8.0f ? m_blk : m_run;  // m_blk on the first block
-      const float alpha = ex2_approx((m_run - m_new) * p.scale_log2);  // 0 on the first block, 1 if unmoved
+      // is the same either way. A half without keys so far keeps -inf and
+      // weight 0 (alpha 1, nothing to rescale).
+      const float m_new = (m_blk - m_run) * p.scale_log2 > 8.0f ? m_blk : m_run;  // m_blk on its first keys
+      const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx((m_run - m_new) * p.scale_log2);
       const float mb = m_new * p.scale_log2;
       uint32_t w[32];
       float s2[2] = {0.f, 0.f};
@@ -541,7 +543,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
           w[i / 2] = pack2_bf16(e0, e1);
         }
       }
-      l_half = l_half * alpha + (s2[0] + s2[1]);
+      l_run = l_run * alpha + (s2[0] + s2[1]);
       if (j > 0) {  // the previous P V has read P and finished writing O
         ok = __all_sync(0xffffffffu, wait_bounded(o_done, (j - 1) & 1, guard, kSiteMmaAcc));
         if (!ok) break;
@@ -552,12 +554,15 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       for (int u = 0; u < 8; ++u)
         *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
             make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's 32 columns of O
-        float o[32];
-        tmem_ld_32cols(tO + lane_off + half * 32, o);
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's rows of O_half
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 32) {
+          float o[32];
+          tmem_ld_32cols(tOh + c, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        tmem_st_32cols(tO + lane_off + half * 32, o);
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st_32cols(tOh + c, o);
+        }
       }
       m_run = m_new;
       fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
@@ -565,28 +570,38 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
     }
-    // ---- O / l -> bf16
+    // ---- merge the halves: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), f_h = 2^((m_h - m) s), m = max m_h
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_done, (nkv - 1) & 1, guard, kSiteEpilogue));
     if (ok) {
-      red_sum[half * 128 + row] = l_half;
+      red_max[half * 128 + row] = m_run;
+      red_sum[half * 128 + row] = l_run;
       __syncwarp();
       if (lane == 0) mbar_arrive(x_bar);
-      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, nkv & 1, guard, kSiteEpilogue));
+      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, 0, guard, kSiteEpilogue));
     }
     if (ok) {
       tc_fence_after_sync();
-      float o[32];
-      tmem_ld_32cols(tO + lane_off + half * 32, o);
+      float o0[32], o1[32];
+      tmem_ld_32cols(tO + lane_off + half * 32, o0);       // O_0, this warp's 32 output columns
+      tmem_ld_32cols(tO + lane_off + 64 + half * 32, o1);  // O_1, the same columns
       const int qi = qt * 128 + row;
       if (qi < p.seq) {
-        const float inv = 1.0f / (red_sum[row] + red_sum[128 + row]);
+        const float m0 = red_max[row], m1 = red_max[128 + row];
+        const float m = fmaxf(m0, m1);  // finite: key 0 lies in half 0 of block 0
+        const float f0 = ex2_approx((m0 - m) * p.scale_log2);
+        const float f1 = m1 == -INFINITY ? 0.0f : ex2_approx((m1 - m) * p.scale_log2);
+        const float inv = 1.0f / (f0 * red_sum[row] + f1 * red_sum[128 + row]);
+        const float g0 = f0 * inv, g1 = f1 * inv;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + (static_cast<int64_t>(row0) + qi) * p.Dn +
                              hl * 64 + half * 32;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          reinterpret_cast<uint4*>(dst)[u] = make_uint4(
-              pack2_bf16(o[8 * u] * inv, o[8 * u + 1] * inv), pack2_bf16(o[8 * u + 2] * inv, o[8 * u + 3] * inv),
-              pack2_bf16(o[8 * u + 4] * inv, o[8 * u + 5] * inv), pack2_bf16(o[8 * u + 6] * inv, o[8 * u + 7] * inv));
+        for (int u = 0; u < 4; ++u) {
+          float y[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) y[e] = fmaf(o0[8 * u + e], g0, o1[8 * u + e] * g1);
+          reinterpret_cast<uint4*>(dst)[u] =
+              make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]), pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7]));
+        }
       }
     }
   }
