@@ -33,6 +33,7 @@ struct KParams {
   int group_m;     // tile order: bands of group_m tile rows, rows fastest inside a band (1 = columns fastest)
   int shared;      // kSharedNone / kSharedA / kSharedB: an operand that every group reads
   int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
+  int load_hint;   // pair kernel: L2 policy kinds (l2_policy) of the M x K operand's loads (bits 0-1) and the N x K one's (2-3)
   const __nv_bfloat16* resid;  // kEpiF32 / kEpiF32Tma: residual [M][ldo] added to the accumulator, or null
   int64_t slice_rows;          // kEpiF32, chain: output row m goes to row m % slice_rows of out[m / slice_rows]
   int vt_col0;                 // kEpiBf16 with aux_ht: columns >= vt_col0 go transposed to aux_ht (row pitch ldt)

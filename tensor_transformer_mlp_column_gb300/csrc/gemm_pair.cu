@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       uint32_t phase = 0;
       uint32_t armed = 0, parity_bits = 0;
       int fill = 0;
+      const uint64_t pol_a = l2_policy(p.load_hint & 3), pol_b = l2_policy((p.load_hint >> 2) & 3);
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
@@ -162,9 +163,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
                 tma_load_2d_pair_multicast(a_dst + pq * (kSubBytes / 2), &p.map_a[gg], kk * BK,
                                            m0 + static_cast<int>(pq) * 64, full_lead, mask);
               } else {
-                tma_load_2d_pair(a_dst, &p.map_a[gg], kk * BK, m0, full_lead);
+                tma_load_2d_pair_hint(a_dst, &p.map_a[gg], kk * BK, m0, full_lead, pol_a);
               }
-              tma_load_2d_pair(sB + stage * C::B_BYTES + u * kSubBytes, &p.map_b[gg], kk * BK, n0, full_lead);
+              tma_load_2d_pair_hint(sB + stage * C::B_BYTES + u * kSubBytes, &p.map_b[gg], kk * BK, n0, full_lead,
+                                    pol_b);
               if (++kk == p.k_blocks) {
                 kk = 0;
                 ++gg;

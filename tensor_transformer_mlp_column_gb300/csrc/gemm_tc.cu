@@ -414,6 +414,10 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.group_m = env_int("TPMLP_GROUP_M", g.group_m);
   kp.shared = g.shared;
   kp.stream_out = env_int("TPMLP_STREAM_OUT", g.stream_out);
+  // Operand tiles are read by several CTAs (the tiles of a band share them):
+  // loaded with the evict-last L2 priority so that the output stream does
+  // not push them out first (TPMLP_LOAD_HINT=0 loads them with normal priority).
+  kp.load_hint = env_int("TPMLP_LOAD_HINT", 1 | (1 << 2));
   kp.resid = static_cast<const __nv_bfloat16*>(g.resid);
   if (kp.resid && g.epi != kEpiF32) return cudaErrorInvalidValue;
   kp.slice_rows = g.slice_rows;
