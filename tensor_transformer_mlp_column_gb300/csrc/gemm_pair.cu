@@ -27,19 +27,18 @@ namespace tpmlp {
 
 namespace {
 
-// A stage holds KSUB consecutive 64-column K blocks (each a 128-row tile of
-// 128-byte swizzled rows): two for the epilogues that need no output staging
-// (three stages of 64 KB: half the barrier round trips per MMA), one for the
-// TMA-store epilogue (six stages of 32 KB beside its 32 KB of staging) -
-// whichever measured faster.
+// A stage holds KSUB = 2 consecutive 64-column K blocks (each a 128-row tile
+// of 128-byte swizzled rows): three stages of 64 KB, half the barrier round
+// trips per MMA of one-block stages; the TMA-store epilogue's 32 KB of output
+// staging still fits beside them.
 constexpr uint32_t kSubBytes = 128 * BK * 2;
 template <int EPI>
 constexpr int ksub_of() {
-  return EPI == kEpiF32Tma ? 1 : 2;
+  return 2;
 }
 template <int EPI>
 constexpr int stages_of() {
-  return EPI == kEpiF32Tma ? 6 : 3;
+  return 3;
 }
 
 template <int STAGES_, int KSUB_>
