@@ -259,14 +259,10 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// Arrive on a barrier in any CTA of the cluster (cluster address).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// The same arrival without release semantics: for signals that order only
-// tensor-memory reads already completed by tcgen05.wait::ld, so the arrival
-// need not wait for the thread's outstanding global stores.
+// Arrival on a barrier of another CTA of the cluster (cluster address), without release
+// semantics: for signals that order only tensor-memory reads already
+// completed by tcgen05.wait::ld, so the arrival need not wait for the
+// thread's outstanding global stores.
 __device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
@@ -275,8 +271,6 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
 }
 
-// TMA tile load into this CTA's shared memory whose completion is counted on
-// a barrier that may live in the peer CTA (cluster address).
 // L2 eviction priority for a load, as a cache policy operand:
 // 0 normal, 1 evict-last (keep: other CTAs read the same tile soon), 2 evict-first.
 __device__ __forceinline__ uint64_t l2_policy(int kind) {
@@ -290,22 +284,15 @@ __device__ __forceinline__ uint64_t l2_policy(int kind) {
   return pol;
 }
 
-// tma_load_2d_pair with an L2 cache policy (l2_policy) for the loaded lines.
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// a barrier that may live in the peer CTA (cluster address), with an L2 cache
+// policy (l2_policy) for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
                                                       uint32_t bar_cluster_addr, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
       "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                                 uint32_t bar_cluster_addr) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
       : "memory");
 }
 
