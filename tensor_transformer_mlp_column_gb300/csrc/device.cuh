@@ -53,6 +53,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// The same test with a limit (ns) on how long the thread may be suspended
+// inside the instruction while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return done != 0;
+}
+constexpr uint32_t kWaitSuspendNs = 20000;  // long waits sleep in the instruction instead of looping (0: its own limit)
+
 // Shared state of one CTA's bounded waits.
 struct WaitGuard {
   volatile int* abort_flag;  // shared memory: set once any wait of the CTA gives up
@@ -69,7 +84,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (kWaitSuspendNs ? mbar_try_wait_for(a, parity, kWaitSuspendNs) : mbar_try_wait(a, parity)) return true;
     if ((it & 31u) == 0) {
       if (*g.abort_flag) return false;
       if (global_timer_ns() - t0 > g.limit_ns) {
