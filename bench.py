@@ -37,13 +37,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # one pass; command and figures in profiles/traffic_large_forward.md). Valid
 # only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
-TRAFFIC_SOURCE_HASH = "37ac878e3f5058b9"
+TRAFFIC_SOURCE_HASH = "803cd23f158d3eed"
 TRAFFIC_BYTES = {
-    "gemm1_gelu(faithful)": 1_231_062_528,
-    "gemm2_partials": 2_984_125_952,
-    "allreduce": 2_401_472_768,
-    "gemm1_gelu(fused)": 1_229_968_640,
-    "gemm2_fused_sum": 2_761_753_344,
+    "gemm1_gelu(faithful)": 1_234_637_056,
+    "gemm2_partials": 3_000_253_952,
+    "allreduce": 2_401_188_864,
+    "gemm1_gelu(fused)": 1_240_460_544,
+    "gemm2_fused_sum": 2_762_115_072,
 }
 
 
