@@ -87,6 +87,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (sm_100 and later): one instruction for two lanes'
+// worth of fused multiply-add or add.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(a), "f"(b));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t d, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(d));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 and later).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -525,14 +546,20 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       uint32_t w[32];
       float s2[2] = {0.f, 0.f};
       if (full) {
+        // Exponent arguments and the row sum on packed fp32 pairs (half the
+        // FMA-pipe instructions); the two lanes of a pair are the even and
+        // odd columns, so the sums are the same two partial sums as below.
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nmb2 = f2_pack(-mb, -mb);
+        uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float e0 = ex2_approx(fmaf(v[i], p.scale_log2, -mb));
-          const float e1 = ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb));
-          s2[0] += e0;
-          s2[1] += e1;
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), sc2, nmb2), x0, x1);
+          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+          acc2 = f2_add(acc2, f2_pack(e0, e1));
           w[i / 2] = pack2_bf16(e0, e1);
         }
+        f2_unpack(acc2, s2[0], s2[1]);
       } else {
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
