@@ -273,6 +273,48 @@ def test_large_forward_sampled_rows(tp):
     tp.tpmlp_check_status()
 
 
+def _random_shapes(count, seed):
+    """Seeded (T, D, F, N) draws over the bf16 path's constraints (D and F/N
+    multiples of 8), small and pair-sized alike, ragged in every dimension."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        n = int(rng.choice([1, 2, 3, 4, 5, 8, 16]))
+        fs = 8 * int(rng.integers(1, 129))   # 8 .. 1024
+        d = 8 * int(rng.integers(1, 193))    # 8 .. 1536
+        t = int(rng.integers(1, 2501))
+        if n * fs > 8192:
+            continue
+        out.append((t, d, n * fs, n))
+    return out
+
+
+RANDOM_SHAPES = _random_shapes(12, 2026)
+
+
+@pytest.mark.parametrize("shape", RANDOM_SHAPES, ids=lambda s: "T%dD%dF%dN%d" % s)
+def test_random_shapes_forward_backward(tp, shape):
+    """Forward (both modes) on 48 sampled token rows plus the last one, and the
+    backward's dX on the same rows, against the float64 oracle."""
+    T, D, F, N = shape
+    w = Workload("rand", T, D, F, N, "bf16", 1.0, 0.05, 0.05, 1.0, True)
+    inp = make_inputs(w, seed=T + D)
+    rows = sorted(set(sample_indices(T, min(T, 48), seed=7)) | {T - 1})
+    ref = {k: f64(v) for k, v in inp.items()}
+    shards_ref = oracle.shard_mlp(ref["A"], ref["B"], N)
+    Y_ref = oracle.tp_mlp_rows(ref["X"], shards_ref, rows)
+    dX_ref = oracle.tp_mlp_backward_dx_rows(ref["X"], ref["dY"], shards_ref, rows)
+    d = on_gpu(inp)
+    sh = tp.tpmlp_shard(d["A"], d["B"], N)
+    idx = torch.tensor(rows, device="cuda")
+    for mode in ("faithful", "fused"):
+        check(f64(tp.tpmlp_forward(d["X"], sh, mode).index_select(0, idx)), Y_ref, "bf16", f"Y {mode} {shape}")
+        dX, _, _ = tp.tpmlp_backward(d["X"], d["dY"], sh, mode)
+        check(f64(dX.index_select(0, idx)), dX_ref, "bf16", f"dX {mode} {shape}")
+    tp.tpmlp_check_status()
+    sh.free()
+
+
 # ----------------------------------------------------------------- backward
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
