@@ -29,11 +29,17 @@ __device__ int g_status = 0;
 
 namespace {
 
+// A stage holds KSUB consecutive 64-column K blocks: two for 128-column
+// tiles (three stages of 64 KB, half the barrier round trips per MMA), one
+// for 256-column tiles (four stages of 48 KB).
 template <int BN>
 struct Cfg {
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
-  static constexpr uint32_t A_BYTES = BM * BK * 2;
-  static constexpr uint32_t B_BYTES = BN * BK * 2;
+  static constexpr int KSUB = BN == 128 ? 2 : 1;
+  static constexpr int STAGES = BN == 256 ? 4 : 3;
+  static constexpr uint32_t A_SUB = BM * BK * 2;  // one K block of the M x K operand
+  static constexpr uint32_t B_SUB = BN * BK * 2;  // one K block of the N x K operand
+  static constexpr uint32_t A_BYTES = KSUB * A_SUB;
+  static constexpr uint32_t B_BYTES = KSUB * B_SUB;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators
   static constexpr size_t SMEM = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + 256 /*barriers*/;
@@ -97,29 +103,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       uint32_t issued = 0, parity_bits = 0;
       int fill = 0;
       bool ok = true;
+      const uint64_t pol_a = l2_policy(p.load_hint & 3), pol_b = l2_policy((p.load_hint >> 2) & 3);
       for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
-        int gg = g, kk = 0;  // group and K block of the next fill (chain mode walks the groups in order)
-        for (int kb = 0; kb < kb_per_tile; ++kb, ++kk) {
-          if (kk == p.k_blocks) {
-            kk = 0;
-            ++gg;
-          }
+        int gg = g, kk = 0;  // group and K block of the next load (chain mode walks the groups in order)
+        for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
             ok = false;
             break;
           }
+          const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;  // K blocks in this stage
           ++fill;
           if (fill != p.inject) {
-            mbar_arrive_expect_tx(full + stage, C::STAGE_BYTES);
-            // The M x K operand's maps have 128- or 64-row boxes (the latter
-            // when the quad kernel is in use); the stage holds 128 rows.
-            for (int r = 0; r < BM; r += p.a_box)
-              tma_load_2d(sA + stage * C::A_BYTES + r * 128, &p.map_a[gg], kk * BK, mb * BM + r, full + stage);
-            tma_load_2d(sB + stage * C::B_BYTES, &p.map_b[gg], kk * BK, nb * BN, full + stage);
+            mbar_arrive_expect_tx(full + stage, nsub * (C::A_SUB + C::B_SUB));
+            for (int u = 0; u < nsub; ++u) {
+              // The M x K operand's maps have 128- or 64-row boxes (the latter
+              // when the quad kernel is in use); a K block holds 128 rows.
+              for (int r = 0; r < BM; r += p.a_box)
+                tma_load_2d_hint(sA + stage * C::A_BYTES + u * C::A_SUB + r * 128, &p.map_a[gg], kk * BK, mb * BM + r,
+                                 full + stage, pol_a);
+              tma_load_2d_hint(sB + stage * C::B_BYTES + u * C::B_SUB, &p.map_b[gg], kk * BK, nb * BN, full + stage,
+                               pol_b);
+              if (++kk == p.k_blocks) {
+                kk = 0;
+                ++gg;
+              }
+            }
             issued |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+          } else {
+            for (int u = 0; u < nsub; ++u)  // the withheld fill still advances the K position
+              if (++kk == p.k_blocks) {
+                kk = 0;
+                ++gg;
+              }
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -149,18 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < kb_per_tile; ++kb) {
+        for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES);
-          const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES);
+          const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;
+          for (int u = 0; u < nsub; ++u) {
+            const uint32_t a0 = smem_addr(sA + stage * C::A_BYTES + u * C::A_SUB);
+            const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES + u * C::B_SUB);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
-                        (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+                          (kb | u | k) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(empty + stage);  // frees the stage once these MMAs have read it
           if (++stage == C::STAGES) {
@@ -207,8 +228,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tmem_ld_32cols(t_row + static_cast<uint32_t>(c), v);
         if (with_res) add_residual(res, v);
         if (c + 32 == BN) {
+          // The accumulator may be overwritten now; the arrival orders only
+          // these completed TMEM reads, so it is relaxed.
           tc_fence_before_sync();
-          mbar_arrive(acc_empty + acc);  // accumulator may be overwritten now
+          mbar_arrive_relaxed(acc_empty + acc);
         }
         if (!row_ok || n0 >= p.N) continue;
         epilogue_store<EPI>(p, g, m, n0, v);

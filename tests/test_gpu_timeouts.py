@@ -33,7 +33,9 @@ def tp():
     return tp
 
 
-@pytest.mark.parametrize("case", [("pair_kernel", 4096, 1024, 4096, 4), ("single_cta_kernel", 256, 256, 1024, 4)],
+# Each CTA of both cases issues at least three stage fills (K = D in blocks of
+# 64, two blocks per stage), so the withheld third fill is reached.
+@pytest.mark.parametrize("case", [("pair_kernel", 4096, 1024, 4096, 4), ("single_cta_kernel", 256, 512, 1024, 4)],
                          ids=lambda c: c[0])
 def test_withheld_fill_times_out_and_library_recovers(tp, case):
     name, T, D, F, n = case
