@@ -37,13 +37,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # one pass; command and figures in profiles/traffic_large_forward.md). Valid
 # only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
-TRAFFIC_SOURCE_HASH = "6dd7229c0a893d31"
+TRAFFIC_SOURCE_HASH = "7376e14e7b78a752"
 TRAFFIC_BYTES = {
-    "gemm1_gelu(faithful)": 1_219_691_264,
-    "gemm2_partials": 2_927_765_248,
-    "allreduce": 2_400_924_672,
-    "gemm1_gelu(fused)": 1_215_876_352,
-    "gemm2_fused_sum": 2_761_106_176,
+    "gemm1_gelu(faithful)": 1_245_079_552,
+    "gemm2_partials": 2_992_263_680,
+    "allreduce": 2_401_096_960,
+    "gemm1_gelu(fused)": 1_243_064_064,
+    "gemm2_fused_sum": 2_761_955_328,
 }
 
 

@@ -23,6 +23,8 @@
 // are drained, and both CTAs of each pair free their TMEM.
 #include "gemm_common.cuh"
 
+#include <atomic>
+
 namespace tpmlp {
 
 namespace {
@@ -388,11 +390,11 @@ cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   cfg.numAttrs = 2;
   // Persistent grid: as many clusters as can be resident at once (per device
   // and per instantiation, since the shared-memory size differs).
-  static int max_clusters[64] = {0};
+  static std::atomic<int> max_clusters[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  int& cached = max_clusters[dev];
+  int cached = max_clusters[dev].load(std::memory_order_relaxed);
   if (!cached) {
     cfg.gridDim = dim3(kCtas * (num_sms() / kCtas), 1, 1);
     int n = 0;
@@ -401,6 +403,7 @@ cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
     cfg.numAttrs = 2;
     if (e != cudaSuccess) return e;
     cached = n > 0 ? n : 1;
+    max_clusters[dev].store(cached, std::memory_order_relaxed);
   }
   const int clusters = kp.tiles < cached ? kp.tiles : cached;
   cfg.gridDim = dim3(kCtas * clusters, 1, 1);

@@ -18,6 +18,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -306,25 +307,28 @@ int env_int(const char* name, int dflt) {
 // (pairs sharing the M x K operand by multicast), 1 = CTA pairs, 0 = single
 // CTAs only. TPMLP_TC_KERNEL overrides the default for comparisons.
 int kernel_family() {
-  static int v = -1;
-  if (v < 0) {
-    v = env_int("TPMLP_TC_KERNEL", 1);
-    if (v < 0 || v > 2) v = 1;
-  }
+  static const int v = [] {
+    const int f = env_int("TPMLP_TC_KERNEL", 1);
+    return f < 0 || f > 2 ? 1 : f;
+  }();
   return v;
 }
 
 // Device address of g_status on the current device.
 int* status_word() {
-  static int* cached[64] = {nullptr};
+  static std::atomic<int*> cached[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
+  int* w = cached[dev].load(std::memory_order_relaxed);
+  if (!w) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_status) == cudaSuccess) cached[dev] = static_cast<int*>(ptr);
+    if (cudaGetSymbolAddress(&ptr, g_status) == cudaSuccess) {
+      w = static_cast<int*>(ptr);
+      cached[dev].store(w, std::memory_order_relaxed);
+    }
   }
-  return cached[dev];
+  return w;
 }
 
 }  // namespace
@@ -332,9 +336,8 @@ int* status_word() {
 int* device_status_word() { return status_word(); }
 
 bool pdl_enabled() {
-  static int v = -1;
-  if (v < 0) v = env_int("TPMLP_PDL", 1) != 0 ? 1 : 0;
-  return v == 1;
+  static const bool v = env_int("TPMLP_PDL", 1) != 0;
+  return v;
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {
@@ -367,16 +370,16 @@ int tc_box_rows_b(int N) {
 // of box_cols x box_rows elements, 128-byte swizzle.
 static bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows, int64_t cols,
                       int64_t pitch_bytes, int box_cols, int box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !fn)
-      return false;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch_bytes)};
   const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
@@ -459,16 +462,18 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
 }
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (!n) {
     int v = 0;
     cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = v > 0 ? v : 1;
+    n = v > 0 ? v : 1;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace tpmlp

@@ -66,3 +66,45 @@ def test_calls_run_on_the_given_stream(tp):
         assert finished, f"{name}: waited for the default stream"
         assert torch.equal(out, ref), f"{name}: differs on the side stream"
     tp.tpmlp_check_status()
+
+
+def test_concurrent_host_threads(tp):
+    """Calls from several host threads, each with its own stream, workspace and
+    shards, interleave freely: every thread's results equal the ones computed
+    alone (the library's host state is per thread or set once per process)."""
+    import threading
+
+    shapes = [(2048, 1024, 4096, 4), (1000, 512, 2048, 8), (300, 256, 1024, 2)]
+    jobs = []
+    for i, (T, D, F, N) in enumerate(shapes):
+        inp = {k: v.cuda() for k, v in make_inputs(Workload(f"thr{i}", T, D, F, N, "bf16", 1.0, 0.03, 0.03),
+                                                    seed=90 + i).items()}
+        sh = tp.tpmlp_shard(inp["A"], inp["B"], N)
+        ref = {m: tp.tpmlp_forward(inp["X"], sh, m).clone() for m in ("faithful", "fused")}
+        jobs.append((inp, sh, ref))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(job):
+        inp, sh, ref = job
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(20):
+                    for m in ("faithful", "fused"):
+                        Y = tp.tpmlp_forward(inp["X"], sh, m, stream=s)
+                        s.synchronize()
+                        if not torch.equal(Y, ref[m]):
+                            errors.append(f"{m} differs in a concurrent thread")
+                            return
+        except Exception as e:  # reported below, on the main thread
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=run, args=(j,)) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    assert not any(t.is_alive() for t in threads)
+    tp.tpmlp_check_status()
