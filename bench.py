@@ -67,6 +67,8 @@ def traffic_of(kernel: str):
     if source_hash() != TRAFFIC_SOURCE_HASH:
         return None
     return TRAFFIC_BYTES.get(kernel)
+
+
 METRIC = "TP-MLP fwd TFLOP/s on 1 GB300 (% BF16 peak); partial-sum reduce GB/s (% HBM)"
 
 
@@ -129,25 +131,31 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        t0, t1 = getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30)
-        for ts, ln in self.lines:
-            if not (t0 <= ts <= t1 + 0.15):  # samples taken during the timed region
-                continue
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarize_clocks(self.lines, getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30))
+
+
+def summarize_clocks(lines, t0: float, t1: float) -> dict:
+    """Median and maximum SM clock and the throttle reasons seen in the
+    nvidia-smi samples (time, csv line of ClockSampler.FIELDS) taken during
+    the timed region [t0, t1] (plus one sampling period)."""
+    sm, smax, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for ts, ln in lines:
+        if not (t0 <= ts <= t1 + 0.15):
+            continue
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for nm, v in zip(names, parts[5:9]):
+            if v.lower() == "active":
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
