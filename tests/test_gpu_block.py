@@ -246,3 +246,43 @@ def test_block_fwd_bwd_workload_sampled(tp):
               f"dA_{i} cols")
         check(f64(dB[i].index_select(0, cidx)), oracle.grad_B_rows(xn_full, dout_full, A_i, cols), "bf16",
               f"dB_{i} rows")
+
+
+def _random_block_shapes(count, seed):
+    """Seeded (T, D, F, N) for the bf16 block: D and F/N multiples of 8, D up
+    to the register layer norm's 8192-wide backward rows, T ragged."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        n = int(rng.choice([1, 2, 4, 8]))
+        fs = 8 * int(rng.integers(1, 97))
+        d = 8 * int(rng.integers(1, 161))
+        t = int(rng.integers(1, 1801))
+        if n * fs <= 6144:
+            out.append((t, d, n * fs, n))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_block_shapes(8, 77), ids=lambda s: "T%dD%dF%dN%d" % s)
+def test_block_random_shapes(tp, shape):
+    """The block forward (out and out - x) and backward dx on sampled rows, both
+    modes, on seeded random shapes, against the float64 oracle."""
+    T, D, F, N = shape
+    w = Workload("rb", T, D, F, N, "bf16", 1.0, 0.05, 0.05, 1.0, True)
+    inp = make_block_inputs(w, seed=T + 3 * D, with_dout=True)
+    x, dout = f64(inp["x"]), f64(inp["dout"])
+    rows = sorted(set(sample_indices(T, min(T, 40), seed=5)) | {T - 1})
+    shards_ref = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), N)
+    out_ref = oracle.block_mlp_rows(x, shards_ref, rows, EPS)
+    dx_ref = oracle.block_mlp_backward_dx_rows(x, dout, shards_ref, rows, EPS)
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], N)
+    idx = torch.tensor(rows, device="cuda")
+    for mode in ("faithful", "fused"):
+        out = f64(tp.tpmlp_block_forward(d["x"], sh, mode, EPS).index_select(0, idx))
+        check(out, out_ref, "bf16", f"out {mode} {shape}")
+        check(out - x[rows], out_ref - x[rows], "bf16", f"out - x {mode} {shape}")
+        dx = f64(tp.tpmlp_block_backward(d["x"], d["dout"], sh, mode, EPS)[0].index_select(0, idx))
+        check(dx, dx_ref, "bf16", f"dx {mode} {shape}")
+    tp.tpmlp_check_status()
+    sh.free()

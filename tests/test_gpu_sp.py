@@ -195,3 +195,43 @@ def test_sp_fwd_bwd_workload_matches_unsplit(tp):
         for i in range(n):
             assert torch.equal(dA[i], dA_u[i]) and torch.equal(dB[i], dB_u[i])
         del dXs, dA, dB, dX, dA_u, dB_u
+
+
+def _random_sp_shapes(count, seed):
+    """Seeded (T, D, F, N) with T a multiple of N (the rank slices), D and F/N
+    multiples of 8, slices of any height (not only multiples of 32)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        n = int(rng.choice([2, 3, 4, 8]))
+        fs = 8 * int(rng.integers(1, 97))
+        d = 8 * int(rng.integers(1, 161))
+        t = n * int(rng.integers(1, 400))
+        if n * fs <= 6144:
+            out.append((t, d, n * fs, n))
+    return out
+
+
+@pytest.mark.parametrize("shape", _random_sp_shapes(8, 91), ids=lambda s: "T%dD%dF%dN%d" % s)
+def test_sp_random_shapes(tp, shape):
+    """Sequence-parallel forward and backward (dX) on seeded random shapes: every
+    rank slice bitwise equal to the unsplit call's rows, and sampled rows
+    against the float64 oracle, both modes."""
+    T, D, F, n = shape
+    w = Workload("rs", T, D, F, n, "bf16", 1.0, 0.05, 0.05, 1.0, True)
+    inp = make_inputs(w, seed=T + 5 * D)
+    rows = sorted(set(sample_indices(T, min(T, 40), seed=9)) | {T - 1})
+    shards_ref = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), n)
+    Y_ref = oracle.tp_mlp_rows(f64(inp["X"]), shards_ref, rows)
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], n)
+    Xs, dYs = slices_of(d["X"], n), slices_of(d["dY"], n)
+    idx = torch.tensor(rows, device="cuda")
+    for mode in ("faithful", "fused"):
+        Y = torch.cat(tp.tpmlp_forward_sp(Xs, sh, mode))
+        assert torch.equal(Y, tp.tpmlp_forward(d["X"], sh, mode)), f"{mode} {shape}: slices differ from the unsplit rows"
+        check(f64(Y.index_select(0, idx)), Y_ref, "bf16", f"Y {mode} {shape}")
+        dX = torch.cat(tp.tpmlp_backward_sp(Xs, dYs, sh, mode)[0])
+        assert torch.equal(dX, tp.tpmlp_backward(d["X"], d["dY"], sh, mode)[0]), f"dX {mode} {shape}"
+    tp.tpmlp_check_status()
+    sh.free()
