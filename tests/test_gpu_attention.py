@@ -71,7 +71,25 @@ SMALL_F32 = [
     ("seq512", 2, 512, 64, 1, 1),
     ("seq700", 1, 700, 64, 2, 2),
 ]
-CASES = [c + ("bf16",) for c in SMALL_BF16] + [c + ("f32",) for c in SMALL_F32]
+
+
+def _random_bf16_cases(count, seed):
+    """Seeded (name, batch, seq, D, heads, n) for the bf16 path: head size 64,
+    seq any multiple of 8, heads a multiple of the rank count."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        n = int(rng.choice([1, 2, 4, 8]))
+        heads = n * int(rng.integers(1, 5))
+        seq = 8 * int(rng.integers(1, 161))   # 8 .. 1280
+        batch = int(rng.integers(1, 5))
+        if batch * seq <= 3000:
+            out.append((f"random{len(out)}", batch, seq, 64 * heads, heads, n))
+    return out
+
+
+CASES = ([c + ("bf16",) for c in SMALL_BF16] + [c + ("f32",) for c in SMALL_F32] +
+         [c + ("bf16",) for c in _random_bf16_cases(6, 61)])
 
 
 def oracle_parts(inp, w):
