@@ -27,6 +27,7 @@ struct tpmlp_shards {
   // operand of a tensor-core product.
   std::vector<CUtensorMap> map_At;  // A_i^T [Fs, D]: X A_i        (N = Fs, K = D)
   std::vector<CUtensorMap> map_Bt;  // B_i^T [D, Fs]: H_i B_i      (N = D,  K = Fs)
+  std::vector<CUtensorMap> map_Bt64;  // the same in 64-row boxes (narrow tiles of a small shard-ordered sum)
   std::vector<CUtensorMap> map_B;   // B_i   [Fs, D]: dY B_i^T     (N = Fs, K = D)
   std::vector<CUtensorMap> map_A;   // A_i   [D, Fs]: dP_i A_i^T   (N = D,  K = Fs)
 };
@@ -204,6 +205,7 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
       if (rc) return rc;
       g.map_a[i] = &mh[i];
       g.map_b[i] = &sh->map_Bt[i];
+      if (chain) g.map_b_narrow[i] = &sh->map_Bt64[i];
       if (slices) {  // rank slices: one output (and output map) per slice of T/n rows
         g.out[i] = slices->p[i];
         if ((rc = out_map(&mo[i], g.out[i], T / sh->n, D, D, "Y slice"))) return rc;
@@ -461,12 +463,14 @@ int tpmlp_shard(const void* A, const void* B, int64_t D, int64_t F, int n, tpmlp
   if (dt == TPMLP_BF16) {
     sh->map_At.resize(n);
     sh->map_Bt.resize(n);
+    sh->map_Bt64.resize(n);
     sh->map_B.resize(n);
     sh->map_A.resize(n);
     for (int i = 0; i < n; ++i) {
       const ShardDesc& d = sh->desc[i];
       rc = map_or_fail(&sh->map_At[i], d.At, Fs, D, D, tc_box_rows_b(static_cast<int>(Fs)), "A_i^T");
       if (!rc) rc = map_or_fail(&sh->map_Bt[i], d.Bt, D, Fs, Fs, tc_box_rows_b(static_cast<int>(D)), "B_i^T");
+      if (!rc) rc = map_or_fail(&sh->map_Bt64[i], d.Bt, D, Fs, Fs, 64, "B_i^T");
       if (!rc) rc = map_or_fail(&sh->map_B[i], d.B, Fs, D, D, tc_box_rows_b(static_cast<int>(Fs)), "B_i");
       if (!rc) rc = map_or_fail(&sh->map_A[i], d.A, D, Fs, Fs, tc_box_rows_b(static_cast<int>(D)), "A_i");
       if (rc) {

@@ -2,7 +2,8 @@
 // each product, the single-CTA tcgen05 kernel for small products, the TMA map
 // helpers, and the device status word with its self test.
 //
-// Single-CTA kernel: one CTA per SM loops over output tiles of 128 x BN:
+// Single-CTA kernel: one CTA per SM loops over output tiles of 128 x BN
+// (BN = 64, 128 or 256):
 //   warp 0, lane 0 : TMA producer — fills a STAGES-deep ring of shared-memory
 //                    stages (A 128 x 64, B BN x 64, 128-byte swizzle)
 //   warp 1         : allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN,
@@ -31,12 +32,13 @@ __device__ int g_status = 0;
 namespace {
 
 // A stage holds KSUB consecutive 64-column K blocks: two for 128-column
-// tiles (three stages of 64 KB, half the barrier round trips per MMA), one
-// for 256-column tiles (four stages of 48 KB).
+// tiles (three stages of 64 KB, half the barrier round trips per MMA) and for
+// 64-column tiles (four stages of 48 KB), one for 256-column tiles (four
+// stages of 48 KB).
 template <int BN>
 struct Cfg {
-  static constexpr int KSUB = BN == 128 ? 2 : 1;
-  static constexpr int STAGES = BN == 256 ? 4 : 3;
+  static constexpr int KSUB = BN <= 128 ? 2 : 1;
+  static constexpr int STAGES = BN == 128 ? 3 : 4;
   static constexpr uint32_t A_SUB = BM * BK * 2;  // one K block of the M x K operand
   static constexpr uint32_t B_SUB = BN * BK * 2;  // one K block of the N x K operand
   static constexpr uint32_t A_BYTES = KSUB * A_SUB;
@@ -420,8 +422,21 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   const int pair_tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256) * (g.chain ? 1 : g.groups);
   const bool pair = family >= 1 && pair_tiles >= num_sms() / 4;
   const bool quad = pair && family == 2;
-  const int BN = pair ? 256 : tc_box_rows_b(g.N);
+  int BN = pair ? 256 : tc_box_rows_b(g.N);
+  // A single-CTA product that is read from L2 at the SM's load rate (128 x 128
+  // tiles load 32 KB per 64-deep K block, 256 MMA cycles of work) moves to
+  // 128 x 64 tiles (24 KB per 128 MMA cycles) when their twice as many tiles
+  // still fit in one round over the SMs: a quarter less to load per SM, on
+  // twice as many SMs. Needs the 64-row maps of the N x K operand.
+  if (!pair && BN == 128 && g.map_b_narrow[0] != nullptr && env_int("TPMLP_NARROW", 1) != 0) {
+    const int64_t units = int64_t((g.M + BM - 1) / BM) * (g.chain ? 1 : g.groups);
+    const int64_t t128 = units * ((g.N + 127) / 128), t64 = units * ((g.N + 63) / 64);
+    const int64_t sms = num_sms();
+    if ((t64 + sms - 1) / sms <= (t128 + sms - 1) / sms) BN = 64;
+  }
   const int TM = pair ? 256 : BM;
+  if (BN == 64)
+    for (int i = 0; i < g.groups; ++i) kp.map_b[i] = *g.map_b_narrow[i];
   kp.ldo = g.ldo;
   kp.ldt = g.ldt;
   kp.M = g.M;
@@ -458,6 +473,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
                          env_int("TPMLP_TMA_STORE", 1) != 0;
     return launch_pair(kp, tma_out ? kEpiF32Tma : g.epi, quad ? 1 : 0, s);
   }
+  if (BN == 64) return launch_single_epi<64>(kp, g.epi, s);
   return BN == 256 ? launch_single_epi<256>(kp, g.epi, s) : launch_single_epi<128>(kp, g.epi, s);
 }
 

@@ -42,6 +42,7 @@ def test_clock_summary_reports_hardware_slowdown():
 
 
 def test_traffic_only_for_the_measured_sources(monkeypatch):
+    monkeypatch.setattr(bench, "TRAFFIC_SOURCE_HASH", bench.source_hash())
     assert bench.traffic_of("gemm2_partials") == bench.TRAFFIC_BYTES["gemm2_partials"]
     monkeypatch.setattr(bench, "TRAFFIC_SOURCE_HASH", "0" * 16)
     assert bench.traffic_of("gemm2_partials") is None

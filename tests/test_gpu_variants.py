@@ -7,7 +7,8 @@ fp32 partials and the fused sum (TMA stores), the backward's activation step,
 the saved pre-activation, the block's residual, the sequence-parallel slice
 outputs and attention's QKV projection with V written transposed. TPMLP_PDL=0
 (kernels launched without programmatic dependent launch) must reproduce the
-default's results bit for bit."""
+default's results bit for bit. TPMLP_NARROW=0 (no 128 x 64 single-CTA tiles for
+a small shard-ordered sum) must match both the oracle and the default."""
 
 import os
 import subprocess
@@ -142,3 +143,71 @@ def test_dependent_launch_off_gives_identical_bits(tmp_path):
     assert results["1"].keys() == results["0"].keys()
     for k in results["1"]:
         assert torch.equal(results["1"][k], results["0"][k]), f"{k} differs with dependent launch off"
+
+
+# Narrow single-CTA tiles (128 x 64) for a shard-ordered sum with few output
+# tiles, on by default and off with TPMLP_NARROW=0 (read once per process):
+# both must match the oracle, and each other to within fp32 rounding, since an
+# output element is summed over the same K blocks in the same order either way.
+NARROW_CHILD = r'''
+import sys, numpy as np, torch
+import oracle
+import tensor_transformer_mlp_column_gb300 as tp
+from tpmlp_inputs import Workload, make_inputs, make_block_inputs
+
+def check(got, ref, what):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    fro = np.linalg.norm(got - ref) / np.linalg.norm(ref); mx = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
+    assert fro <= 5e-3 and mx <= 2e-2, (what, fro, mx)
+
+f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+torch.cuda.set_device(0)
+out = {}
+# 8 x 16 and 8 x 15 (ragged rows and columns) tiles of 128 x 64, a single round.
+for name, T, D, F, N in (("seq128", 1024, 1024, 4096, 4), ("ragged", 1000, 960, 1920, 2)):
+    w = Workload(name, T, D, F, N, "bf16", 1.0, 0.02, 0.02)
+    inp = make_inputs(w, seed=91)
+    shards = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), N)
+    rows = list(range(0, T, 13))
+    idx = torch.tensor(rows, device="cuda")
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], N)
+    Y = tp.tpmlp_forward(d["X"], sh, "fused")
+    check(f64(Y.index_select(0, idx)), oracle.tp_mlp_rows(f64(inp["X"]), shards, rows), name + " fused")
+    out[name + "_Y"] = Y
+    bi = make_block_inputs(w, seed=92)
+    shb = tp.tpmlp_shard(bi["A"].cuda(), bi["B"].cuda(), N)
+    blk = tp.tpmlp_block_forward(bi["x"].cuda(), shb, "fused")
+    check(f64(blk.index_select(0, idx)),
+          oracle.block_mlp_rows(f64(bi["x"]), oracle.shard_mlp(f64(bi["A"]), f64(bi["B"]), N), rows), name + " block")
+    out[name + "_block"] = blk
+    if T % N == 0:
+        out[name + "_sp"] = torch.cat(tp.tpmlp_forward_sp([c.clone() for c in torch.chunk(d["X"], N)], sh, "fused"))
+        assert torch.equal(out[name + "_sp"], Y), name + " sequence-parallel slices"
+torch.cuda.synchronize()
+tp.tpmlp_check_status()
+torch.save({k: v.cpu() for k, v in out.items()}, sys.argv[1])
+print("ok")
+'''
+
+
+def test_narrow_single_cta_tiles_against_oracle_and_wide(tmp_path):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    results = {}
+    for flag in ("1", "0"):
+        path = str(tmp_path / f"narrow{flag}.pt")
+        env = dict(os.environ, TPMLP_NARROW=flag)
+        r = subprocess.run([sys.executable, "-c", NARROW_CHILD, path], env=env, cwd=ROOT, capture_output=True,
+                           text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+        results[flag] = torch.load(path)
+    assert results["1"].keys() == results["0"].keys()
+    for k in results["1"]:
+        a, b = results["1"][k].double(), results["0"][k].double()
+        assert (a - b).abs().max() <= 1e-5 * b.abs().max(), f"{k}: narrow and wide tiles differ"
