@@ -308,33 +308,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 
 // ------------------------------------------------------------------ streaming form (any seq)
 //
-// One CTA of 8 softmax warps + 1 control warp per (128-query tile, head,
-// sequence), 99 KB of shared memory and 256 TMEM columns, so two CTAs share an
-// SM and one's loads and products overlap the other's softmax. Keys go in
-// blocks of 128 with a running maximum m and sum l per query row:
-//   control thread: TMA loads (Q once; K through a 2-slot ring; V^T of one
-//     block), S_j = Q K_j^T into TMEM columns 0..127, and P_{j-1} V_{j-1}
-//     accumulated into O (TMEM columns 128..191) once the softmax has written
-//     P_{j-1}; every wait bounded.
+// One CTA of 8 softmax warps, an MMA warp and a load warp per (128-query tile,
+// head, sequence), 99 KB of shared memory and 256 TMEM columns, so two CTAs
+// share an SM and one's loads and products overlap the other's softmax. Keys
+// go in blocks of 128 with a running maximum m and sum l per query row:
+//   load thread: Q once, then K_j and V_j^T (16 KB each) through a ring of
+//     three slots in the order the products read them (K_0, then K_j, V_{j-1}
+//     for j = 1.., then the last V), each slot refilled as soon as the product
+//     that read it has finished, so a load is issued about a block ahead.
+//   MMA thread: S_j = Q K_j^T into TMEM columns 0..127 once every softmax warp
+//     holds S_{j-1} in registers, then P_{j-1} V_{j-1} accumulated into O
+//     (TMEM columns 128..255) once the softmax has written P_{j-1}; every
+//     wait bounded.
 //   softmax warp w: TMEM lanes 32 (w % 4) (its query rows) and key half w / 4
-//     of the block. Block maximum (the two halves meet in shared memory), new
-//     running maximum m' (moved only when the block's maximum exceeds m by
-//     more than 2^8 in weight), a = 2^((m - m') log2(e)/sqrt(d_h)),
+//     of the block, with a running maximum, row sum and output accumulator
+//     O_half of its own: new running maximum m' (moved only when the block's
+//     maximum exceeds m by more than 2^8 in weight), a = 2^((m - m') log2(e)/sqrt(d_h)),
 //     p = 2^((s - m') log2(e)/sqrt(d_h)) written as bf16 into the swizzled P
 //     operand once the previous P V has finished, l <- a l + sum p, and
-//     O <- a O in TMEM when the maximum moved.
+//     O_half <- a O_half in TMEM when the maximum moved.
 // (A one-CTA-per-SM form with every buffer doubled and 16 softmax warps was
 // measured slower: 217 vs 186 us at seq 4096; two independent CTAs per SM
 // overlap better than 16 warps meeting at a barrier every block.)
-// At the end O / l is rounded to bf16. The same result as the exact kernel up
-// to rounding (the weights of earlier blocks are rescaled in fp32).
+// At the end the two halves of a row merge and O / l is rounded to bf16. The
+// same result as the exact kernel up to rounding (the weights of earlier
+// blocks are rescaled in fp32).
 
 constexpr int kStrmSoftmaxWarps = 8;
-constexpr int kStrmThreads = (kStrmSoftmaxWarps + 1) * 32;
-constexpr uint32_t kStrmKBytes = 128 * 128;             // 128 keys x 64 bf16
-constexpr uint32_t kStrmVtBytes = 2 * kVtChunkBytes;    // V^T of 128 keys
-constexpr uint32_t kStrmPBytes = 2 * kPChunkBytes;      // P of 128 keys
-constexpr uint32_t kStrmSmem = 1024 + kQBytes + 2 * kStrmKBytes + kStrmVtBytes + kStrmPBytes + 2 * 2 * 128 * 4 + 128;
+constexpr int kStrmThreads = (kStrmSoftmaxWarps + 2) * 32;  // + the MMA warp and the load warp
+constexpr uint32_t kStrmSlotBytes = 128 * 128;              // K of 128 keys (128 x 64 bf16) or their V^T (64 x 128)
+constexpr int kStrmSlots = 3;
+constexpr uint32_t kStrmPBytes = 2 * kPChunkBytes;  // P of 128 keys
+constexpr uint32_t kStrmSmem = 1024 + kQBytes + kStrmSlots * kStrmSlotBytes + kStrmPBytes + 2 * 2 * 128 * 4 + 128;
+static_assert(2 * kVtChunkBytes == kStrmSlotBytes, "V^T of a key block fills one ring slot");
 
 // 32 TMEM columns of this warp's lanes without waiting: the registers are valid
 // only after tmem_wait_ld(), so several loads can be in flight at once.
@@ -375,38 +381,36 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sK = sQ + kQBytes;  // two slots
-  uint8_t* sVt = sK + 2 * kStrmKBytes;
-  uint8_t* sP = sVt + kStrmVtBytes;
+  uint8_t* sRing = sQ + kQBytes;  // kStrmSlots slots of one K or V^T block
+  uint8_t* sP = sRing + kStrmSlots * kStrmSlotBytes;
   float* red_max = reinterpret_cast<float*>(sP + kStrmPBytes);  // [2][128]
-  float* red_sum = red_max + 256;                                // [2][128]
+  float* red_sum = red_max + 256;                               // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 256);
   uint64_t* bar_q = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;
-  uint64_t* s_full = bars + 6;
-  uint64_t* s_free = bars + 7;   // one arrival per softmax warp: P written, O rescaled
-  uint64_t* o_done = bars + 8;
-  uint64_t* x_bar = bars + 9;    // one arrival per softmax warp: the halves' partial maxima (sums) written
-  uint64_t* drain = bars + 10;
-  uint64_t* s_read = bars + 11;  // one arrival per softmax warp: its S columns are in registers
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* ring_full = bars + 1;                 // [kStrmSlots]
+  uint64_t* ring_empty = bars + 1 + kStrmSlots;   // [kStrmSlots]: the product that read the slot has finished
+  uint64_t* s_full = bars + 1 + 2 * kStrmSlots;
+  uint64_t* s_free = s_full + 1;  // one arrival per softmax warp: P written, O rescaled
+  uint64_t* o_done = s_full + 2;
+  uint64_t* x_bar = s_full + 3;   // one arrival per softmax warp: the halves' partial maxima (sums) written
+  uint64_t* drain = s_full + 4;
+  uint64_t* s_read = s_full + 5;  // one arrival per softmax warp: its S columns are in registers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 6);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
 
   const int nkv = (p.seq + 127) / 128;
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / p.local_heads, hl = gh % p.local_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr uint32_t kCols = 256;  // S: columns 0..127; O_0, O_1 (the two key halves): 128..191, 192..255
+  constexpr int kMmaWarp = kStrmSoftmaxWarps, kLoadWarp = kStrmSoftmaxWarps + 1;
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(k_full, 1);
-    mbar_init(k_full + 1, 1);
-    mbar_init(k_empty, 1);
-    mbar_init(k_empty + 1, 1);
-    mbar_init(v_full, 1);
+    for (int i = 0; i < kStrmSlots; ++i) {
+      mbar_init(ring_full + i, 1);
+      mbar_init(ring_empty + i, 1);
+    }
     mbar_init(s_full, 1);
     mbar_init(s_free, kStrmSoftmaxWarps);
     mbar_init(s_read, kStrmSoftmaxWarps);
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kStrmSoftmaxWarps) tmem_alloc(tmem_slot, kCols);
+  if (warp == kMmaWarp) tmem_alloc(tmem_slot, kCols);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -427,67 +431,74 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
   const int32_t row0 = b * p.seq;
 
-  if (warp == kStrmSoftmaxWarps) {
+  if (warp == kLoadWarp) {
     if (lane == 0) {
-      // ---------------- control: loads and products
+      // ---------------- loads: Q, then the ring in the order the products read it
       const CUtensorMap* mq = &p.map_qkv[shard];
       const CUtensorMap* mv = &p.map_vt[shard];
       const int kx = p.Dn + hl * 64;
       mbar_arrive_expect_tx(bar_q, kQBytes);
       tma_load_2d(sQ, mq, hl * 64, row0 + qt * 128, bar_q);
-      for (int j = 0; j < 2 && j < nkv; ++j) {
-        mbar_arrive_expect_tx(k_full + j, kStrmKBytes);
-        tma_load_2d(sK + j * kStrmKBytes, mq, kx, row0 + j * 128, k_full + j);
-      }
-      mbar_arrive_expect_tx(v_full, kStrmVtBytes);
-      tma_load_2d(sVt, mv, row0, hl * 64, v_full);
-      tma_load_2d(sVt + kVtChunkBytes, mv, row0 + 64, hl * 64, v_full);
+      int n = 0;  // ring position of the next load
+      auto put = [&](bool is_v, int blk) {
+        const int slot = n % kStrmSlots;
+        if (!wait_bounded(ring_empty + slot, ((n / kStrmSlots) & 1) ^ 1u, guard, kSiteProducer)) return false;
+        uint8_t* dst = sRing + slot * kStrmSlotBytes;
+        mbar_arrive_expect_tx(ring_full + slot, kStrmSlotBytes);
+        if (is_v) {
+          tma_load_2d(dst, mv, row0 + blk * 128, hl * 64, ring_full + slot);
+          tma_load_2d(dst + kVtChunkBytes, mv, row0 + blk * 128 + 64, hl * 64, ring_full + slot);
+        } else {
+          tma_load_2d(dst, mq, kx, row0 + blk * 128, ring_full + slot);
+        }
+        ++n;
+        return true;
+      };
+      bool ok = put(false, 0);
+      for (int j = 1; ok && j < nkv; ++j) ok = put(false, j) && put(true, j - 1);
+      if (ok) put(true, nkv - 1);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      // ---------------- products
       bool ok = wait_bounded(bar_q, 0, guard, kSiteProducer);
       const uint64_t dq = smem_desc_sw128(smem_addr(sQ));
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
+      int n = 0;  // ring position of the next operand
       for (int j = 0; ok && j <= nkv; ++j) {
         if (j < nkv) {
-          const int slot = j & 1;
-          ok = wait_bounded(k_full + slot, (j >> 1) & 1, guard, kSiteProducer);
           // S_j overwrites S_{j-1} once every softmax warp holds its columns,
           // so this product overlaps the softmax of block j-1.
+          const int slot = n % kStrmSlots;
+          ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull);
           if (ok && j > 0) ok = wait_bounded(s_read, (j - 1) & 1, guard, kSiteMmaAcc);
           if (!ok) break;
+          ++n;
           tc_fence_after_sync();
-          const uint64_t dk = smem_desc_sw128(smem_addr(sK + slot * kStrmKBytes));
+          const uint64_t dk = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes));
 #pragma unroll
           for (int k = 0; k < 4; ++k) tc_mma_bf16(tS, dq + 2 * k, dk + 2 * k, kIdS, k > 0 ? 1u : 0u);
           tc_commit(s_full);
-          tc_commit(k_empty + slot);
+          tc_commit(ring_empty + slot);
         }
         if (j > 0) {  // O (+)= P_{j-1} V_{j-1}, once P_{j-1} is written and O rescaled
-          ok = wait_bounded(v_full, (j - 1) & 1, guard, kSiteProducer) &&
+          const int slot = n % kStrmSlots;
+          ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull) &&
                wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);
           if (!ok) break;
+          ++n;
           tc_fence_after_sync();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             const uint64_t dp = smem_desc_sw128(smem_addr(sP + c * kPChunkBytes));
-            const uint64_t dv = smem_desc_sw128(smem_addr(sVt + c * kVtChunkBytes));
+            const uint64_t dv = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes + c * kVtChunkBytes));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc_mma_bf16(tO + 64u * c, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || k > 0) ? 1u : 0u);
           }
           tc_commit(o_done);
-          if (j < nkv) {  // V^T of block j into the slot once that product has read it
-            ok = wait_bounded(o_done, (j - 1) & 1, guard, kSiteMmaAcc);
-            if (!ok) break;
-            mbar_arrive_expect_tx(v_full, kStrmVtBytes);
-            tma_load_2d(sVt, mv, row0 + j * 128, hl * 64, v_full);
-            tma_load_2d(sVt + kVtChunkBytes, mv, row0 + j * 128 + 64, hl * 64, v_full);
-          }
-        }
-        if (j + 2 < nkv) {  // K of block j+2 into block j's slot once S_j has read it
-          ok = wait_bounded(k_empty + (j & 1), (j >> 1) & 1, guard, kSiteProducer);
-          if (!ok) break;
-          mbar_arrive_expect_tx(k_full + (j & 1), kStrmKBytes);
-          tma_load_2d(sK + (j & 1) * kStrmKBytes, mq, kx, row0 + (j + 2) * 128, k_full + (j & 1));
+          tc_commit(ring_empty + slot);
         }
       }
     }
