@@ -55,14 +55,14 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t round_up8(int64_t x) { return (x + 7) / 8 * 8; }
 size_t esize(tpmlp_dtype dt) { return dt == TPMLP_BF16 ? 2 : 4; }
 
+// Read once per process (thread-safe static initialisation).
 uint64_t wait_limit_ns() {
-  static uint64_t v = 0;
-  if (!v) {
+  static const uint64_t v = [] {
     const char* s = getenv("TPMLP_WAIT_LIMIT_MS");
     long ms = s ? atol(s) : 0;
     if (ms <= 0 || ms > 600000) ms = 4000;
-    v = static_cast<uint64_t>(ms) * 1000000ull;
-  }
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
   return v;
 }
 

@@ -146,7 +146,8 @@ def test_dependent_launch_off_gives_identical_bits(tmp_path):
 
 
 # Narrow single-CTA tiles (128 x 64) for a shard-ordered sum with few output
-# tiles, on by default and off with TPMLP_NARROW=0 (read once per process):
+# tiles, on by default and off with TPMLP_NARROW=0 (each setting in a child
+# process of its own):
 # both must match the oracle, and each other to within fp32 rounding, since an
 # output element is summed over the same K blocks in the same order either way.
 NARROW_CHILD = r'''
