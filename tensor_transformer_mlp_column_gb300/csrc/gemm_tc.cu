@@ -428,7 +428,9 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   // 128 x 64 tiles (24 KB per 128 MMA cycles) when their twice as many tiles
   // still fit in one round over the SMs: a quarter less to load per SM, on
   // twice as many SMs. Needs the 64-row maps of the N x K operand.
-  if (!pair && BN == 128 && g.map_b_narrow[0] != nullptr && env_int("TPMLP_NARROW", 1) != 0) {
+  bool narrow_maps = g.groups > 0;
+  for (int i = 0; i < g.groups; ++i) narrow_maps = narrow_maps && g.map_b_narrow[i] != nullptr;
+  if (!pair && BN == 128 && narrow_maps && env_int("TPMLP_NARROW", 1) != 0) {
     const int64_t units = int64_t((g.M + BM - 1) / BM) * (g.chain ? 1 : g.groups);
     const int64_t t128 = units * ((g.N + 127) / 128), t64 = units * ((g.N + 63) / 64);
     const int64_t sms = num_sms();

@@ -40,7 +40,8 @@ enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
 struct TcGemm {
   const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
   const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
-  const CUtensorMap* map_b_narrow[kMaxGroups];  // optional: the same operands in 64-row boxes (narrow single-CTA tiles)
+  const CUtensorMap* map_b_narrow[kMaxGroups];  // optional: the same operands in 64-row boxes (narrow single-CTA
+                                                // tiles; used only when every group has one)
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
   void* out2[kMaxGroups];                // kEpiGeluSaveP only: fp32 pre-activation, row stride ldo
   const CUtensorMap* map_out[kMaxGroups];  // optional fp32 output maps (make_output_map_f32) for TMA stores
