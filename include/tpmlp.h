@@ -85,7 +85,8 @@ const char* tpmlp_last_error(void);
 
 /* Waits for `stream`, then reads and clears the current device's status word.
  * Returns TPMLP_OK, TPMLP_ERR_TIMEOUT if a kernel gave up on a wait since the
- * last check, or TPMLP_ERR_CUDA if the stream reports an error. */
+ * last check, or TPMLP_ERR_CUDA if the stream reports an error or a kernel
+ * found its dynamic shared memory misaligned (it then did no work). */
 int tpmlp_check_status(tpmlp_stream_t stream);
 
 /* gelu(x), elementwise: GeLU(x) = 1/2 x (1 + tanh u), u = sqrt(2/pi)(x + 0.044715 x^3)

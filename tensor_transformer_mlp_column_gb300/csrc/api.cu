@@ -383,6 +383,8 @@ const char* tpmlp_last_error(void) { return g_msg; }
 int tpmlp_check_status(tpmlp_stream_t stream) {
   int v = 0;
   TRY_CUDA(read_and_clear_status(&v, stream));
+  if (v == kSiteSmemAlign)
+    return fail(TPMLP_ERR_CUDA, "a kernel found its dynamic shared memory misaligned and did no work");
   if (v) return fail(TPMLP_ERR_TIMEOUT, "a device-side wait ran out of time (site %d)", v);
   return TPMLP_OK;
 }

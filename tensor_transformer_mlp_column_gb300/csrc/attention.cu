@@ -309,24 +309,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 // ------------------------------------------------------------------ streaming form (any seq)
 //
 // One CTA of 8 softmax warps, an MMA warp and a load warp per (128-query tile,
-// head, sequence), 99 KB of shared memory and 256 TMEM columns, so two CTAs
+// head, sequence), 112 KB of shared memory and 256 TMEM columns, so two CTAs
 // share an SM and one's loads and products overlap the other's softmax. Keys
 // go in blocks of 128 with a running maximum m and sum l per query row:
 //   load thread: Q once, then K_j and V_j^T (16 KB each) through a ring of
-//     three slots in the order the products read them (K_0, then K_j, V_{j-1}
+//     two slots in the order the products read them (K_0, then K_j, V_{j-1}
 //     for j = 1.., then the last V), each slot refilled as soon as the product
-//     that read it has finished, so a load is issued about a block ahead.
+//     that read it has finished.
 //   MMA thread: S_j = Q K_j^T into TMEM columns 0..127 once every softmax warp
 //     holds S_{j-1} in registers, then P_{j-1} V_{j-1} accumulated into O
 //     (TMEM columns 128..255) once the softmax has written P_{j-1}; every
-//     wait bounded.
+//     wait bounded. P has two buffers, block j using buffer j % 2, so the
+//     softmax writes P_j as soon as P_{j-2} V_{j-2} has finished and waits
+//     for P_{j-1} V_{j-1} only before it rescales O.
 //   softmax warp w: TMEM lanes 32 (w % 4) (its query rows) and key half w / 4
 //     of the block, with a running maximum, row sum and output accumulator
 //     O_half of its own: new running maximum m' (moved only when the block's
 //     maximum exceeds m by more than 2^8 in weight), a = 2^((m - m') log2(e)/sqrt(d_h)),
 //     p = 2^((s - m') log2(e)/sqrt(d_h)) written as bf16 into the swizzled P
-//     operand once the previous P V has finished, l <- a l + sum p, and
-//     O_half <- a O_half in TMEM when the maximum moved.
+//     operand, l <- a l + sum p, and O_half <- a O_half in TMEM when the
+//     maximum moved.
 // (A one-CTA-per-SM form with every buffer doubled and 16 softmax warps was
 // measured slower: 217 vs 186 us at seq 4096; two independent CTAs per SM
 // overlap better than 16 warps meeting at a barrier every block.)
@@ -337,9 +339,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 constexpr int kStrmSoftmaxWarps = 8;
 constexpr int kStrmThreads = (kStrmSoftmaxWarps + 2) * 32;  // + the MMA warp and the load warp
 constexpr uint32_t kStrmSlotBytes = 128 * 128;              // K of 128 keys (128 x 64 bf16) or their V^T (64 x 128)
-constexpr int kStrmSlots = 3;
-constexpr uint32_t kStrmPBytes = 2 * kPChunkBytes;  // P of 128 keys
-constexpr uint32_t kStrmSmem = 1024 + kQBytes + kStrmSlots * kStrmSlotBytes + kStrmPBytes + 2 * 2 * 128 * 4 + 128;
+constexpr int kStrmSlots = 2;
+constexpr uint32_t kStrmPBufBytes = 2 * kPChunkBytes;  // P of 128 keys
+constexpr uint32_t kStrmPBytes = 2 * kStrmPBufBytes;   // two P buffers, blocks alternating
+// No alignment slack: the dynamic shared memory is declared 1024-aligned (and
+// checked), so two CTAs fit an SM with both P buffers.
+constexpr uint32_t kStrmSmem = kQBytes + kStrmSlots * kStrmSlotBytes + kStrmPBytes + 128;
 static_assert(2 * kVtChunkBytes == kStrmSlotBytes, "V^T of a key block fills one ring slot");
 
 // 32 TMEM columns of this warp's lanes without waiting: the registers are valid
@@ -378,25 +383,30 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const float (&v)[
 }
 
 __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_addr(smem_raw) & 1023u) {  // the 128-byte-swizzled operands need 1024-byte alignment
+    if (threadIdx.x == 0) atomicExch(p.status, kSiteSmemAlign);
+    return;  // CTA-uniform, before any barrier or TMEM allocation
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sQ = smem;
   uint8_t* sRing = sQ + kQBytes;  // kStrmSlots slots of one K or V^T block
-  uint8_t* sP = sRing + kStrmSlots * kStrmSlotBytes;
-  float* red_max = reinterpret_cast<float*>(sP + kStrmPBytes);  // [2][128]
-  float* red_sum = red_max + 256;                               // [2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_sum + 256);
+  uint8_t* sP = sRing + kStrmSlots * kStrmSlotBytes;  // two buffers of kStrmPBufBytes
+  // The halves' final maxima and sums, in ring slot 0 (free once the last product is done).
+  float* red_max = reinterpret_cast<float*>(sRing);  // [2][128]
+  float* red_sum = red_max + 256;                    // [2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kStrmPBytes);
   uint64_t* bar_q = bars + 0;
   uint64_t* ring_full = bars + 1;                 // [kStrmSlots]
   uint64_t* ring_empty = bars + 1 + kStrmSlots;   // [kStrmSlots]: the product that read the slot has finished
   uint64_t* s_full = bars + 1 + 2 * kStrmSlots;
   uint64_t* s_free = s_full + 1;  // one arrival per softmax warp: P written, O rescaled
-  uint64_t* o_done = s_full + 2;
-  uint64_t* x_bar = s_full + 3;   // one arrival per softmax warp: the halves' partial maxima (sums) written
-  uint64_t* drain = s_full + 4;
-  uint64_t* s_read = s_full + 5;  // one arrival per softmax warp: its S columns are in registers
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 6);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 7);
+  uint64_t* x_bar = s_full + 2;   // one arrival per softmax warp: the halves' partial maxima (sums) written
+  uint64_t* drain = s_full + 3;
+  uint64_t* s_read = s_full + 4;  // one arrival per softmax warp: its S columns are in registers
+  uint64_t* o_done = s_full + 5;  // [2]: P_k V_k done, k even / odd (phase k / 2 of o_done[k % 2])
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 7);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
 
   const int nkv = (p.seq + 127) / 128;
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
@@ -415,6 +425,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     mbar_init(s_free, kStrmSoftmaxWarps);
     mbar_init(s_read, kStrmSoftmaxWarps);
     mbar_init(o_done, 1);
+    mbar_init(o_done + 1, 1);
     mbar_init(x_bar, kStrmSoftmaxWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -491,13 +502,13 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
           tc_fence_after_sync();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            const uint64_t dp = smem_desc_sw128(smem_addr(sP + c * kPChunkBytes));
+            const uint64_t dp = smem_desc_sw128(smem_addr(sP + ((j - 1) & 1) * kStrmPBufBytes + c * kPChunkBytes));
             const uint64_t dv = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes + c * kVtChunkBytes));
 #pragma unroll
             for (int k = 0; k < 4; ++k)
               tc_mma_bf16(tO + 64u * c, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || k > 0) ? 1u : 0u);
           }
-          tc_commit(o_done);
+          tc_commit(o_done + ((j - 1) & 1));
           tc_commit(ring_empty + slot);
         }
       }
@@ -582,17 +593,20 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
         }
       }
       l_run = l_run * alpha + (s2[0] + s2[1]);
-      if (j > 0) {  // the previous P V has read P and finished writing O
-        ok = __all_sync(0xffffffffu, wait_bounded(o_done, (j - 1) & 1, guard, kSiteMmaAcc));
+      if (j > 1) {  // P buffer j % 2 was last read by P_{j-2} V_{j-2}
+        ok = __all_sync(0xffffffffu, wait_bounded(o_done + (j & 1), ((j >> 1) - 1) & 1, guard, kSiteMmaAcc));
         if (!ok) break;
-        tc_fence_after_sync();
       }
-      uint8_t* prow = sP + half * kPChunkBytes + row * 128;
+      uint8_t* prow = sP + (j & 1) * kStrmPBufBytes + half * kPChunkBytes + row * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
             make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's rows of O_half
+        // once P_{j-1} V_{j-1} has finished writing O
+        ok = __all_sync(0xffffffffu, wait_bounded(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, guard, kSiteMmaAcc));
+        if (!ok) break;
+        tc_fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 64; c += 32) {
           float o[32];
@@ -609,7 +623,8 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       if (lane == 0) mbar_arrive(s_free);
     }
     // ---- merge the halves: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), f_h = 2^((m_h - m) s), m = max m_h
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(o_done, (nkv - 1) & 1, guard, kSiteEpilogue));
+    if (ok)
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, guard, kSiteEpilogue));
     if (ok) {
       red_max[half * 128 + row] = m_run;
       red_sum[half * 128 + row] = l_run;

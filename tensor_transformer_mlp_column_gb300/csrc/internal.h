@@ -10,13 +10,15 @@ namespace tpmlp {
 
 constexpr int kMaxGroups = 16;  // shards per tensor-core launch (TPMLP_MAX_SHARDS)
 
-// Status codes of the bounded waits (stored in the device status word).
+// Status codes of the device-side checks (stored in the device status word):
+// the bounded waits, and the shared-memory alignment check.
 enum WaitSite : int {
   kSiteProducer = 1,
   kSiteMmaFull = 2,
   kSiteMmaAcc = 3,
   kSiteEpilogue = 4,
   kSiteSelftest = 5,
+  kSiteSmemAlign = 6,  // a kernel found its dynamic shared memory misaligned and returned without work
 };
 
 // Output treatment of the tensor-core GEMM.
