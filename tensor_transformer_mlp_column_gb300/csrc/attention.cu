@@ -400,13 +400,18 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   uint64_t* ring_full = bars + 1;                 // [kStrmSlots]
   uint64_t* ring_empty = bars + 1 + kStrmSlots;   // [kStrmSlots]: the product that read the slot has finished
   uint64_t* s_full = bars + 1 + 2 * kStrmSlots;
-  uint64_t* s_free = s_full + 1;  // one arrival per softmax warp: P written, O rescaled
-  uint64_t* x_bar = s_full + 2;   // one arrival per softmax warp: the halves' partial maxima (sums) written
-  uint64_t* drain = s_full + 3;
-  uint64_t* s_read = s_full + 4;  // one arrival per softmax warp: its S columns are in registers
-  uint64_t* o_done = s_full + 5;  // [2]: P_k V_k done, k even / odd (phase k / 2 of o_done[k % 2])
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 7);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 8);
+  // [2]: one arrival per softmax warp once P_k is written and O rescaled, k
+  // even / odd (phase k / 2 of s_free[k % 2]). Two barriers because a warp
+  // may finish block k+1 (it waits only for P_{k-1} V_{k-1}) before the MMA
+  // thread has waited for block k: one barrier could then be two phases
+  // ahead of that wait.
+  uint64_t* s_free = s_full + 1;
+  uint64_t* x_bar = s_full + 3;   // one arrival per softmax warp: the halves' partial maxima (sums) written
+  uint64_t* drain = s_full + 4;
+  uint64_t* s_read = s_full + 5;  // one arrival per softmax warp: its S columns are in registers
+  uint64_t* o_done = s_full + 6;  // [2]: P_k V_k done, k even / odd (phase k / 2 of o_done[k % 2])
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
 
   const int nkv = (p.seq + 127) / 128;
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
@@ -423,6 +428,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, kStrmSoftmaxWarps);
+    mbar_init(s_free + 1, kStrmSoftmaxWarps);
     mbar_init(s_read, kStrmSoftmaxWarps);
     mbar_init(o_done, 1);
     mbar_init(o_done + 1, 1);
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
         if (j > 0) {  // O (+)= P_{j-1} V_{j-1}, once P_{j-1} is written and O rescaled
           const int slot = n % kStrmSlots;
           ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull) &&
-               wait_bounded(s_free, (j - 1) & 1, guard, kSiteMmaAcc);
+               wait_bounded(s_free + ((j - 1) & 1), ((j - 1) >> 1) & 1, guard, kSiteMmaAcc);
           if (!ok) break;
           ++n;
           tc_fence_after_sync();
@@ -620,7 +626,7 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
       fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_free);
+      if (lane == 0) mbar_arrive(s_free + (j & 1));
     }
     // ---- merge the halves: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), f_h = 2^((m_h - m) s), m = max m_h
     if (ok)
