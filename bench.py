@@ -33,9 +33,10 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 # DRAM bytes (read + write) per launch of each kernel of the step on the large
-# workload, from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum,
-# one pass; command and figures in profiles/traffic_large_forward.md). Valid
-# only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
+# workload, from one ncu capture of dram__bytes_read.sum + dram__bytes_write.sum
+# (one kernel per capture on a reduced token count, scaled to the full launch
+# by the tokens it processes; the capture commands are kept with the profiles).
+# Valid only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
 TRAFFIC_SOURCE_HASH = "11c3a9176eab212d"
 TRAFFIC_BYTES = {
@@ -553,11 +554,11 @@ def bench_backward(args, local_rank, peaks):
         alg = 8.0 * w.T * w.D * w.F / (ms * 1e-3) / 1e12
         if saved:  # no recompute: all 8*T*D*F FLOP are algorithmic
             out[f"saved_P_{mode}"] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
-                                      "frac_bf16": round(alg / peaks["bf16_tflops_sustained"], 4)}
+                                      "frac_bf16": round(alg / peaks["bf16_tflops"], 4)}
         else:
             out[mode] = {"ms": round(ms, 3), "TFLOP/s": round(alg, 1),
                          "TFLOP/s_incl_recompute": round(alg * 10 / 8, 1),
-                         "frac_bf16_incl_recompute": round(alg * 10 / 8 / peaks["bf16_tflops_sustained"], 4)}
+                         "frac_bf16_incl_recompute": round(alg * 10 / 8 / peaks["bf16_tflops"], 4)}
         del ws
     sh.free()
     return out
@@ -758,7 +759,7 @@ def bench_attention(args, local_rank, peaks):
             gms = _time_graph_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, mode, Y, ws), dev, 50)
             tf = w.fwd_flops() / (ms * 1e-3) / 1e12
             res[mode] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                         "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4),
+                         "frac_bf16": round(tf / peaks["bf16_tflops"], 4),
                          "graph_ms": round(gms, 4), "graph_TFLOP/s": round(w.fwd_flops() / (gms * 1e-3) / 1e12, 1)}
         tp.tpmlp_check_status(stream)
         sh.free()
@@ -775,7 +776,7 @@ def bench_attention(args, local_rank, peaks):
         ms = _time_ms(lambda: tp.tpmlp_attn_forward(d["X"], w.batch, sh, "fused", Y, ws), dev, stream, 20, 3)
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         out[name] = {"batch": w.batch, "seq": w.seq, "fused": {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                     "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4)}}
+                     "frac_bf16": round(tf / peaks["bf16_tflops"], 4)}}
         tp.tpmlp_check_status(stream)
         sh.free()
     # heads time against seq: least squares on (1, seq, seq^2)
@@ -882,34 +883,40 @@ def main():
         else:
             tf = flops_of[k] / (ms * 1e-3) / 1e12
             kernel_report[k] = {"ms": round(ms, 4), "TFLOP/s": round(tf, 1),
-                                "frac_bf16": round(tf / peaks["bf16_tflops_sustained"], 4)}
+                                "frac_bf16": round(tf / peaks["bf16_tflops"], 4)}
     step_ms_sum = sum(avg.values())
-    dominant = max(avg, key=lambda k: avg[k])
+    dominant = max((k for k in avg if k != "allreduce"), key=lambda k: avg[k])
     default_workload = args.workload == "large" and not args.T and not args.N
-    traffic = traffic_of(dominant) if default_workload else None
-    if dominant == "allreduce":
-        ach = reduce_bytes / (avg[dominant] * 1e-3) / 1e9
-        roof = {"kernel": dominant, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "algorithmic_bytes": reduce_bytes, "peak_source": peaks["source"]}
-    else:
-        ach = flops_of[dominant] / (avg[dominant] * 1e-3) / 1e12
-        pk = peaks["bf16_tflops_sustained"]
-        roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
-                "frac": round(ach / pk, 4), "traffic": traffic,
-                "algorithmic_flops": flops_of[dominant],
-                # operands read once and results written once
-                "algorithmic_bytes": (2.0 * (T * D + D * F + T * F) if dominant.startswith("gemm1") else
-                                      2.0 * (T * F + F * D) + 4.0 * T * D * (N if dominant == "gemm2_partials" else 1)),
-                "peak_source": peaks["source"] + " (sustained bf16, kernel timed inside a long step)"}
+    # The timed region lasts res["total_ms"]: well under the seconds-long loop
+    # that settles the sustained (power-capped) rate, so the kernels are held
+    # against the burst peak; a region of several seconds takes the sustained one.
+    long_region = res["total_ms"] >= 2000.0
+    pk = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    pk_kind = (f"sustained bf16 (timed region {res['total_ms'] / 1e3:.2f} s)" if long_region else
+               f"burst bf16 (timed region {res['total_ms'] / 1e3:.2f} s, under the seconds-long sustained loop)")
+    ach = flops_of[dominant] / (avg[dominant] * 1e-3) / 1e12
     red_gbs = reduce_bytes / (avg["allreduce"] * 1e-3) / 1e9
+    roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": pk, "unit": "TFLOP/s",
+            "frac": round(ach / pk, 4), "traffic": traffic_of(dominant) if default_workload else None,
+            "algorithmic_flops": flops_of[dominant],
+            # operands read once and results written once
+            "algorithmic_bytes": (2.0 * (T * D + D * F + T * F) if dominant.startswith("gemm1") else
+                                  2.0 * (T * F + F * D) + 4.0 * T * D * (N if dominant == "gemm2_partials" else 1)),
+            "peak_source": f"{peaks['source']}: {pk_kind}",
+            # the second target: the faithful simulated all-reduce against HBM
+            "reduce": {"kernel": "allreduce", "bound": "hbm", "achieved": round(red_gbs, 1),
+                       "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(red_gbs / peaks["hbm_gbs"], 4),
+                       "traffic": traffic_of("allreduce") if default_workload else None,
+                       "algorithmic_bytes": reduce_bytes,
+                       "peak_source": f"{peaks['source']}: copy bandwidth"},
+            "modes": {}}
     value = job_throughput(world, step_flops, ms_step)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded normal inputs, A,B ~ N(0, 0.02), X ~ N(0, 1))", "config": config,
-        "frac_bf16_peak": round(value / world / peaks["bf16_tflops_sustained"], 4),
+        "frac_bf16_peak": round(value / world / pk, 4),
         "reduce": {"GB/s": round(red_gbs, 1), "peak": peaks["hbm_gbs"],
                    "frac_hbm": round(red_gbs / peaks["hbm_gbs"], 4), "bytes": reduce_bytes},
         "modes": {
@@ -928,7 +935,8 @@ def main():
         ms = line["modes"][m]["ms"]
         tf = w.fwd_flops() / (ms * 1e-3) / 1e12
         line["modes"][m]["TFLOP/s"] = round(tf, 1)
-        line["modes"][m]["frac_bf16"] = round(tf / peaks["bf16_tflops_sustained"], 4)
+        line["modes"][m]["frac_bf16"] = round(tf / pk, 4)
+        roof["modes"][m] = dict(line["modes"][m])
     if not args.no_backward and world == 1 and not args.T and not args.N:
         line["backward"] = bench_backward(args, local_rank, peaks)
         line["other_workloads"] = bench_small_workloads(local_rank)

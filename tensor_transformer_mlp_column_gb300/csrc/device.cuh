@@ -327,18 +327,6 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorM
       : "memory");
 }
 
-// The same load multicast to every CTA of `mask` (each receives the box at
-// the same shared-memory offset); the completion for each destination CTA is
-// counted on the barrier at bar's offset in that destination's pair-even CTA.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                                           uint32_t bar_cluster_addr, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(mask)
-      : "memory");
-}
-
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),

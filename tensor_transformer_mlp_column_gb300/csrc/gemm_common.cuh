@@ -29,7 +29,6 @@ struct KParams {
   uint64_t wait_ns;
   int* status;     // device status word (bounded waits record their site here)
   int inject;      // test hook: > 0 withholds that fill (1-based) in every CTA
-  int a_box;       // rows of the M x K operand's TMA box (128, or 64 when quads split it)
   int group_m;     // tile order: bands of group_m tile rows, rows fastest inside a band (1 = columns fastest)
   int shared;      // kSharedNone / kSharedA / kSharedB: an operand that every group reads
   int stream_out;  // 1: epilogue stores bypass L2 retention (evict-first)
@@ -49,8 +48,7 @@ struct KParams {
 //   shared B (every group reads the same N x K operand): rows = the groups'
 //     M blocks stacked, cols = N blocks;
 //   otherwise each group's grid in turn (chain mode: the one output grid).
-// "Blocks" are the kernel's tile units (for the CTA-quad kernel an N block is
-// a pair of 256-column blocks).
+// "Blocks" are the kernel's tile units.
 __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
   int rows_total, cols, base = 0;
   if (p.chain || p.shared == kSharedNone) {
@@ -226,10 +224,8 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
   }
 }
 
-// Launches the CTA-pair kernel (quad = 0) or the CTA-quad kernel (quad = 1,
-// two pairs sharing the M x K operand through TMA multicast) with epilogue
-// `epi`; kp's tile units must match (256-row M blocks; 256-column N blocks,
-// or pairs of them for the quad kernel).
-cudaError_t launch_pair(const KParams& kp, int epi, int quad, cudaStream_t s);
+// Launches the CTA-pair kernel with epilogue `epi`; kp's tile units must
+// match (256-row M blocks, 256-column N blocks).
+cudaError_t launch_pair(const KParams& kp, int epi, cudaStream_t s);
 
 }  // namespace tpmlp

@@ -1,26 +1,21 @@
 // gemm_pair.cu — tcgen05 cta_group::2 GEMM: a CTA pair (cluster of 2 CTAs on
-// two SMs) computes one 256 x 256 tile; optionally two pairs form a quad
-// (cluster of 4) that computes two 256 x 256 tiles side by side in N and
-// shares the M x K operand through TMA multicast.
+// two SMs) computes one 256 x 256 tile.
 //
 // Per k-block each CTA brings in its 128 rows of the M x K operand and its
 // 128 of the 256 rows of the N x K operand (the pair MMA reads both CTAs'
-// shared memory). In a quad, the two CTAs at the same position of the two
-// pairs need the same 128 M x K rows: each loads 64 of them once and
-// multicasts them to both, so a CTA fetches 24 KB per k-block instead of 32 KB
-// and L2 serves 25 % fewer bytes per MMA.
+// shared memory); every CTA loads only into its own shared memory.
 //   every CTA, warp 0 lane 0 : TMA producer; the pair's bytes are counted on
 //                              the full barrier of the pair's even CTA, which
 //                              its producer arms with both CTAs' bytes
 //   even CTA, warp 1 lane 0  : MMA issuer (M=256, N=256, K=16 per
 //                              instruction) into one of two TMEM accumulators;
-//                              commits free each stage in every CTA that shares
-//                              it and publish each accumulator in the pair
+//                              commits free each stage in both CTAs and
+//                              publish each accumulator in the pair
 //   every CTA, warps 2..5    : epilogue of the CTA's own 128 rows; release the
 //                              accumulator on the pair's even CTA
-// Every wait is bounded; on a timeout the CTA raises the abort flag of every
-// CTA of its cluster, all roles leave their loops, copies in flight and MMAs
-// are drained, and both CTAs of each pair free their TMEM.
+// Every wait is bounded; on a timeout the CTA raises the abort flag of the
+// other CTA of its pair, all roles leave their loops, copies in flight and
+// MMAs are drained, and both CTAs free their TMEM.
 #include "gemm_common.cuh"
 
 #include <atomic>
@@ -63,11 +58,11 @@ struct PairCfg {
   }
 };
 
-template <int EPI, int STAGES, bool QUAD>
+template <int EPI, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_constant__ KParams p) {
   using C = PairCfg<STAGES, ksub_of<EPI>()>;
   constexpr int BN = 256;
-  constexpr uint32_t kCtas = QUAD ? 4 : 2;
+  constexpr uint32_t kCtas = 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -85,15 +80,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const uint32_t pos = rank & 1u;   // position in the pair: 0 = even CTA, issues the pair's MMAs
-  const uint32_t pq = rank >> 1;    // which pair of the quad (always 0 for a lone pair)
-  const uint32_t lead = rank & ~1u; // the pair's even CTA
+  const uint32_t lead = 0;          // the pair's even CTA
   const int cluster = static_cast<int>(cluster_id_x());
   const int nclusters = static_cast<int>(cluster_count_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full + s, 1);                    // even CTA: its producer's arrive (+ the pair's bytes)
-      mbar_init(empty + s, QUAD ? 2u : 1u);      // one commit from each pair whose MMAs read the stage
+      mbar_init(empty + s, 1);                   // the pair's commit once its MMAs have read the stage
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full + b, 1);   // one commit per tile
@@ -139,8 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
         const int m0 = mb * 256 + static_cast<int>(pos) * 128;
-        const int nb256 = QUAD ? 2 * nb + static_cast<int>(pq) : nb;
-        const int n0 = nb256 * BN + static_cast<int>(pos) * 128;
+        const int n0 = nb * BN + static_cast<int>(pos) * 128;
         int gg = g, kk = 0;  // group and K block of the next load (chain mode walks the groups in order)
         for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
@@ -157,15 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
               parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
             }
             for (int u = 0; u < nsub; ++u) {
-              uint8_t* a_dst = sA + stage * C::A_BYTES + u * kSubBytes;
-              if constexpr (QUAD) {
-                // 64 of this position's 128 M x K rows, to this CTA and its twin in the other pair.
-                const uint16_t mask = static_cast<uint16_t>((1u << pos) | (1u << (2 + pos)));
-                tma_load_2d_pair_multicast(a_dst + pq * (kSubBytes / 2), &p.map_a[gg], kk * BK,
-                                           m0 + static_cast<int>(pq) * 64, full_lead, mask);
-              } else {
-                tma_load_2d_pair_hint(a_dst, &p.map_a[gg], kk * BK, m0, full_lead, pol_a);
-              }
+              tma_load_2d_pair_hint(sA + stage * C::A_BYTES + u * kSubBytes, &p.map_a[gg], kk * BK, m0, full_lead,
+                                    pol_a);
               tma_load_2d_pair_hint(sB + stage * C::B_BYTES + u * kSubBytes, &p.map_b[gg], kk * BK, n0, full_lead,
                                     pol_b);
               if (++kk == p.k_blocks) {
@@ -204,8 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     if (lane == 0 && pos == 0) {
       // ---------------- MMA issuer (even CTA of each pair)
       constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
-      constexpr uint16_t kStageMask = QUAD ? 0xF : 0x3;  // CTAs whose shared memory holds this pair's stages
-      const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead);
+      constexpr uint16_t kPairMask = 0x3;  // both CTAs: each holds half of every stage and of every accumulator
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -233,14 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
                                (kb | u | k) != 0 ? 1u : 0u);
             }
           }
-          tc_commit_pair_multicast(empty + stage, kStageMask);  // frees the stage once these MMAs have read it
+          tc_commit_pair_multicast(empty + stage, kPairMask);  // frees the stage once these MMAs have read it
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (aborted) break;
-        tc_commit_pair_multicast(acc_full + acc, pair_mask);  // accumulator complete in both CTAs of the pair
+        tc_commit_pair_multicast(acc_full + acc, kPairMask);  // accumulator complete in both CTAs of the pair
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
@@ -268,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         break;
       }
       tc_fence_after_sync();
-      const int nb256 = QUAD ? 2 * nb + static_cast<int>(pq) : nb;
       const int64_t m_warp = int64_t(mb) * 256 + int64_t(pos) * 128 + quarter * 32;  // row of lane 0
       const int64_t m = m_warp + lane;
       const bool row_ok = m < p.M;
@@ -280,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         return (EPI == kEpiF32 || EPI == kEpiF32Tma) && p.resid != nullptr && row_ok && n0 < p.N;
       };
       auto issue = [&](int c, uint32_t (&r)[32], uint4 (&res)[4]) {
-        const int n0 = nb256 * BN + c;
+        const int n0 = nb * BN + c;
         if (with_res(n0)) load_residual(p, m, n0, res);
         __syncwarp();
         tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c), r);
@@ -289,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        const int n0 = nb256 * BN + c;
+        const int n0 = nb * BN + c;
         if (with_res(n0)) add_residual(res, v);
         if constexpr (EPI == kEpiF32Tma) {
           // Stage the warp's 32 x 32 fp32 block in shared memory with the
@@ -367,12 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   }
 }
 
-template <int EPI, int STAGES, bool QUAD>
+template <int EPI, int STAGES>
 cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   using C = PairCfg<STAGES, ksub_of<EPI>()>;
   constexpr size_t kSmem = C::template smem<EPI>();
-  constexpr unsigned kCtas = QUAD ? 4 : 2;
-  auto kern = tc_gemm_pair_kernel<EPI, STAGES, QUAD>;
+  constexpr unsigned kCtas = 2;
+  auto kern = tc_gemm_pair_kernel<EPI, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[2];
@@ -410,21 +394,20 @@ cudaError_t launch_impl(const KParams& kp, cudaStream_t s) {
   return cudaLaunchKernelEx(&cfg, kern, kp);
 }
 
-template <bool QUAD>
 cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
   switch (epi) {
     case kEpiGeluBf16:
-      return launch_impl<kEpiGeluBf16, stages_of<kEpiGeluBf16>(), QUAD>(kp, s);
+      return launch_impl<kEpiGeluBf16, stages_of<kEpiGeluBf16>()>(kp, s);
     case kEpiF32:
-      return launch_impl<kEpiF32, stages_of<kEpiF32>(), QUAD>(kp, s);
+      return launch_impl<kEpiF32, stages_of<kEpiF32>()>(kp, s);
     case kEpiBwdAct:
-      return launch_impl<kEpiBwdAct, stages_of<kEpiBwdAct>(), QUAD>(kp, s);
+      return launch_impl<kEpiBwdAct, stages_of<kEpiBwdAct>()>(kp, s);
     case kEpiF32Tma:
-      return launch_impl<kEpiF32Tma, stages_of<kEpiF32Tma>(), QUAD>(kp, s);
+      return launch_impl<kEpiF32Tma, stages_of<kEpiF32Tma>()>(kp, s);
     case kEpiGeluSaveP:
-      return launch_impl<kEpiGeluSaveP, stages_of<kEpiGeluSaveP>(), QUAD>(kp, s);
+      return launch_impl<kEpiGeluSaveP, stages_of<kEpiGeluSaveP>()>(kp, s);
     case kEpiBf16:
-      return launch_impl<kEpiBf16, stages_of<kEpiBf16>(), QUAD>(kp, s);
+      return launch_impl<kEpiBf16, stages_of<kEpiBf16>()>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }
@@ -432,8 +415,6 @@ cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_pair(const KParams& kp, int epi, int quad, cudaStream_t s) {
-  return quad ? launch_epi<true>(kp, epi, s) : launch_epi<false>(kp, epi, s);
-}
+cudaError_t launch_pair(const KParams& kp, int epi, cudaStream_t s) { return launch_epi(kp, epi, s); }
 
 }  // namespace tpmlp

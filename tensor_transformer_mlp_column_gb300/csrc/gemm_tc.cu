@@ -121,11 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (fill != p.inject) {
             mbar_arrive_expect_tx(full + stage, nsub * (C::A_SUB + C::B_SUB));
             for (int u = 0; u < nsub; ++u) {
-              // The M x K operand's maps have 128- or 64-row boxes (the latter
-              // when the quad kernel is in use); a K block holds 128 rows.
-              for (int r = 0; r < BM; r += p.a_box)
-                tma_load_2d_hint(sA + stage * C::A_BYTES + u * C::A_SUB + r * 128, &p.map_a[gg], kk * BK, mb * BM + r,
-                                 full + stage, pol_a);
+              tma_load_2d_hint(sA + stage * C::A_BYTES + u * C::A_SUB, &p.map_a[gg], kk * BK, mb * BM, full + stage,
+                               pol_a);
               tma_load_2d_hint(sB + stage * C::B_BYTES + u * C::B_SUB, &p.map_b[gg], kk * BK, nb * BN, full + stage,
                                pol_b);
               if (++kk == p.k_blocks) {
@@ -305,13 +302,13 @@ int env_int(const char* name, int dflt) {
   return e && *e ? atoi(e) : dflt;
 }
 
-// Kernel family for the bf16 products, read once per process: 2 = CTA quads
-// (pairs sharing the M x K operand by multicast), 1 = CTA pairs, 0 = single
-// CTAs only. TPMLP_TC_KERNEL overrides the default for comparisons.
+// Kernel family for the bf16 products, read once per process: 1 = CTA pairs
+// for products with enough 256 x 256 tiles, 0 = single CTAs only.
+// TPMLP_TC_KERNEL overrides the default for comparisons.
 int kernel_family() {
   static const int v = [] {
     const int f = env_int("TPMLP_TC_KERNEL", 1);
-    return f < 0 || f > 2 ? 1 : f;
+    return f < 0 || f > 1 ? 1 : f;
   }();
   return v;
 }
@@ -358,11 +355,11 @@ cudaError_t read_and_clear_status(int* value, cudaStream_t s) {
   return cudaStreamSynchronize(s);
 }
 
-// Box heights of the operand maps: the M x K operand in 128-row boxes (64 when
-// quads split it between the two pairs); the N x K operand in 128-row boxes
-// (each CTA of a pair loads half of the 256 N rows), or BN rows for the
-// single-CTA kernel when it is the only family in use.
-int tc_box_rows_a() { return kernel_family() == 2 ? 64 : 128; }
+// Box heights of the operand maps: the M x K operand in 128-row boxes; the
+// N x K operand in 128-row boxes (each CTA of a pair loads half of the 256 N
+// rows), or BN rows for the single-CTA kernel when it is the only family in
+// use.
+int tc_box_rows_a() { return 128; }
 int tc_box_rows_b(int N) {
   if (kernel_family() >= 1) return 128;
   return N <= 128 ? 128 : 256;
@@ -414,14 +411,13 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.aux_dpt[i] = g.aux_dpt[i];
     if (g.map_out[i]) kp.map_out[i] = *g.map_out[i];
   }
-  // CTA pairs (or quads) with 256 x 256 tiles, unless the product has too few
+  // CTA pairs with 256 x 256 tiles, unless the product has too few
   // of those tiles to occupy a quarter of the SMs: then single CTAs with
   // 128 x 128 tiles (the N x K boxes that pair mode encodes) spread it over
   // four times as many SMs.
   const int family = kernel_family();
   const int pair_tiles = ((g.M + 255) / 256) * ((g.N + 255) / 256) * (g.chain ? 1 : g.groups);
   const bool pair = family >= 1 && pair_tiles >= num_sms() / 4;
-  const bool quad = pair && family == 2;
   int BN = pair ? 256 : tc_box_rows_b(g.N);
   // A single-CTA product that is read from L2 at the SM's load rate (128 x 128
   // tiles load 32 KB per 64-deep K block, 256 MMA cycles of work) moves to
@@ -447,13 +443,11 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   kp.chain = g.chain;
   kp.m_blocks = (g.M + TM - 1) / TM;
   kp.n_blocks = (g.N + BN - 1) / BN;
-  if (quad) kp.n_blocks = (kp.n_blocks + 1) / 2;  // a quad's N unit is two 256-column blocks
   kp.k_blocks = (g.K + BK - 1) / BK;
   kp.tiles = kp.m_blocks * kp.n_blocks * (g.chain ? 1 : g.groups);
   kp.wait_ns = wait_ns;
   kp.status = status_word();
   kp.inject = g.inject;
-  kp.a_box = tc_box_rows_a();
   kp.group_m = env_int("TPMLP_GROUP_M", g.group_m);
   kp.shared = g.shared;
   kp.stream_out = env_int("TPMLP_STREAM_OUT", g.stream_out);
@@ -473,7 +467,7 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     // (with rank slices only when no warp's 32 rows straddle two slices)
     const bool tma_out = g.epi == kEpiF32 && g.map_out[0] != nullptr && g.slice_rows % 32 == 0 &&
                          env_int("TPMLP_TMA_STORE", 1) != 0;
-    return launch_pair(kp, tma_out ? kEpiF32Tma : g.epi, quad ? 1 : 0, s);
+    return launch_pair(kp, tma_out ? kEpiF32Tma : g.epi, s);
   }
   if (BN == 64) return launch_single_epi<64>(kp, g.epi, s);
   return BN == 256 ? launch_single_epi<256>(kp, g.epi, s) : launch_single_epi<128>(kp, g.epi, s);

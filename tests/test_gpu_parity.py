@@ -349,28 +349,64 @@ def test_backward_tiny_fp32_workload(tp):
         check(f64(dB[i]), dB_ref[i], "f32", f"dB_{i}")
 
 
-def test_fwd_bwd_workload_sampled(tp):
-    # T=8192, D=8192, F=32768, N=8 at full size: sampled rows of Y and dX,
-    # sampled columns of every dA_i and rows of every dB_i.
-    w = WORKLOADS["fwd_bwd"]
-    inp = make_inputs(w, seed=0)
+def _check_sampled_fwd_bwd(tp, w, inp, rows, cols, what):
+    """Both modes of tpmlp_forward and tpmlp_backward at the workload's full
+    size, against the float64 oracle on sampled token rows of Y and dX,
+    sampled columns of every dA_i and the same rows of every dB_i. The oracle
+    values are computed once; the GPU outputs of each mode are compared with
+    them separately."""
     X, dY = f64(inp["X"]), f64(inp["dY"])
     shards_ref = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), w.N)
-    rows = sample_indices(w.T, 64, seed=5)
-    cols = sample_indices(w.Fs, 16, seed=6)
+    Y_ref = oracle.tp_mlp_rows(X, shards_ref, rows)
+    dX_ref = oracle.tp_mlp_backward_dx_rows(X, dY, shards_ref, rows)
+    dA_ref = [oracle.grad_A_cols(X, dY, A_i, B_i, cols) for A_i, B_i in shards_ref]
+    dB_ref = [oracle.grad_B_rows(X, dY, A_i, cols) for A_i, _ in shards_ref]
     d = on_gpu(inp)
     sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
     idx = torch.tensor(rows, device="cuda")
     cidx = torch.tensor(cols, device="cuda")
-    Y = tp.tpmlp_forward(d["X"], sh, "fused")
-    check(f64(Y.index_select(0, idx)), oracle.tp_mlp_rows(X, shards_ref, rows), "bf16", "Y rows")
-    del Y
-    dX, dA, dB = tp.tpmlp_backward(d["X"], d["dY"], sh, "faithful")
-    tp.tpmlp_check_status()
-    check(f64(dX.index_select(0, idx)), oracle.tp_mlp_backward_dx_rows(X, dY, shards_ref, rows), "bf16", "dX rows")
-    for i, (A_i, B_i) in enumerate(shards_ref):
-        check(f64(dA[i].index_select(1, cidx)), oracle.grad_A_cols(X, dY, A_i, B_i, cols), "bf16", f"dA_{i} cols")
-        check(f64(dB[i].index_select(0, cidx)), oracle.grad_B_rows(X, dY, A_i, cols), "bf16", f"dB_{i} rows")
+    for mode in ("faithful", "fused"):
+        Y = tp.tpmlp_forward(d["X"], sh, mode)
+        check(f64(Y.index_select(0, idx)), Y_ref, "bf16", f"{what} Y rows {mode}")
+        del Y
+        dX, dA, dB = tp.tpmlp_backward(d["X"], d["dY"], sh, mode)
+        tp.tpmlp_check_status()
+        check(f64(dX.index_select(0, idx)), dX_ref, "bf16", f"{what} dX rows {mode}")
+        for i in range(w.N):
+            check(f64(dA[i].index_select(1, cidx)), dA_ref[i], "bf16", f"{what} dA_{i} cols {mode}")
+            check(f64(dB[i].index_select(0, cidx)), dB_ref[i], "bf16", f"{what} dB_{i} rows {mode}")
+        del dX, dA, dB
+    sh.free()
+
+
+def test_fwd_bwd_workload_sampled(tp):
+    # T=8192, D=8192, F=32768, N=8 at full size, in the bench's launch
+    # configuration, both modes of the forward and of the backward: 64 sampled
+    # rows of Y and dX, 16 sampled columns of every dA_i and rows of every dB_i.
+    # The fused products chain K over all eight shards (F = 32768: 512 K blocks
+    # of 64 per output tile).
+    w = WORKLOADS["fwd_bwd"]
+    inp = make_inputs(w, seed=0)
+    rows = sample_indices(w.T, 64, seed=5)
+    cols = sample_indices(w.Fs, 16, seed=6)
+    _check_sampled_fwd_bwd(tp, w, inp, rows, cols, "fwd_bwd")
+
+
+# Shapes whose shard-ordered sums chain K over 512 blocks of 64 (F = 32768, as
+# in the fwd+bwd workload) at a fraction of its size: one with enough 256 x 256
+# output tiles for the CTA-pair kernel, one small enough for the single-CTA
+# kernel's narrow tiles.
+LONG_CHAIN = [("pair_kernel", 2048, 1280, 32768, 8), ("single_cta_kernel", 384, 512, 32768, 8)]
+
+
+@pytest.mark.parametrize("case", LONG_CHAIN, ids=[c[0] for c in LONG_CHAIN])
+def test_long_shard_chain_sampled(tp, case):
+    name, T, D, F, N = case
+    w = Workload(name, T, D, F, N, "bf16", 1.0, 0.01, 0.01, 1.0, True)
+    inp = make_inputs(w, seed=T + 3)
+    rows = sorted(set(sample_indices(T, 48, seed=8)) | {0, T - 1})
+    cols = sorted(set(sample_indices(w.Fs, 24, seed=9)) | {0, w.Fs - 1})
+    _check_sampled_fwd_bwd(tp, w, inp, rows, cols, name)
 
 
 # ----------------------------------------------------------------- bounded waits

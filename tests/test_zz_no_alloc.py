@@ -6,7 +6,9 @@ fixed 64 MiB scratch array instead of a caller workspace.
 Checked through the C ABI against tpmlp_forward (which takes a workspace), on
 two calls in a row with different inputs, so the second call runs on scratch
 that still holds the first call's data. Same tolerances as the other parity
-tests. This file is collected last on purpose.
+tests. The second call must also leave the device's free memory exactly as it
+found it (the first call may still load kernel code). This file is collected
+last on purpose.
 """
 
 import ctypes
@@ -57,9 +59,14 @@ def test_noalloc_forward_matches_forward_twice(tp, dtype, mode):
     first = {k: v.cuda() for k, v in make_inputs(w, seed=31).items()}
     second_X = make_inputs(w, seed=32)["X"].cuda()
     sh = tp.tpmlp_shard(first["A"], first["B"], w.N)
-    for X in (first["X"], second_X):  # two calls in a row on the shared scratch
+    for call, X in enumerate((first["X"], second_X)):  # two calls in a row on the shared scratch
         Y = torch.full((w.T, w.D), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         assert _call_noalloc(tp, X, sh, Y, mode) == tp.TPMLP_OK, tp.tpmlp_last_error()
+        torch.cuda.synchronize()
+        if call == 1:  # nothing allocated or freed on the device by the call itself
+            assert torch.cuda.mem_get_info()[0] == free_before
         ref = tp.tpmlp_forward(X, sh, "fused" if mode else "faithful")
         torch.cuda.synchronize()
         assert torch.isfinite(Y).all()
