@@ -383,6 +383,24 @@ int tpmlp_attn_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn
 int tpmlp_attn_forward(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards* shards, void* Y,
                        tpmlp_mode mode, void* workspace, size_t workspace_bytes, tpmlp_stream_t stream);
 
+/* Per-step timing, switched on by TPMLP_TRACE=1 in the environment (read once
+ * per process; the method the pages use to find where a layer's time goes,
+ * [P1] section 5, "profile in segments"). While it is on, every step of a call
+ * that launches device work (gemm1_gelu, gemm2_partials, allreduce,
+ * gemm2_fused_sum, bwd_dual_P_dH, bwd_dB, bwd_dA, bwd_dX_partials, layer_norm,
+ * attn_core, ...) is bracketed by two CUDA events on the call's stream. Steps
+ * enqueued on a stream that is capturing a CUDA graph are not recorded.
+ * tpmlp_trace_read waits for every recorded step to finish, then writes one
+ * line per step, "<name> <milliseconds>\n", in the order the steps were
+ * enqueued (across all threads), into buf (bytes long, NUL-terminated), sets
+ * *records (may be NULL) to the number of lines written and forgets the
+ * steps. Returns TPMLP_OK; TPMLP_ERR_WORKSPACE if buf could not hold every
+ * line (the rest are dropped) or if more than 65536 steps were enqueued since
+ * the last read; TPMLP_ERR_ARG if buf is NULL while bytes > 0. With tracing off
+ * it writes an empty string. tpmlp_trace_enabled returns 1 if tracing is on. */
+int tpmlp_trace_read(char* buf, size_t bytes, int* records);
+int tpmlp_trace_enabled(void);
+
 /* Test hook for the time limits: launches one block that waits on a device
  * barrier nobody ever completes, with the library's bounded wait and a limit
  * of limit_ms milliseconds (1..10000). The block then stops and records

@@ -79,6 +79,8 @@ SIGNATURES = {
     "tpmlp_forward_sp": (_I, [ctypes.POINTER(_P), _I64, _P, ctypes.POINTER(_P), _I, _P, _SZ, _P]),
     "tpmlp_backward_sp": (_I, [ctypes.POINTER(_P), ctypes.POINTER(_P), _I64, _P, ctypes.POINTER(_P),
                                ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
+    "tpmlp_trace_read": (_I, [ctypes.c_char_p, _SZ, ctypes.POINTER(_I)]),
+    "tpmlp_trace_enabled": (_I, []),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -524,3 +526,22 @@ def tpmlp_selftest_gemm_withheld_fill(X: torch.Tensor, shards: Shards, H: torch.
 
 def tpmlp_selftest_wait_timeout(limit_ms: int, stream=None) -> None:
     _check(lib().tpmlp_selftest_wait_timeout(limit_ms, _stream(stream)), "tpmlp_selftest_wait_timeout")
+
+
+def tpmlp_trace_enabled() -> bool:
+    """True when the library records per-step times (TPMLP_TRACE=1 when it was loaded)."""
+    return bool(lib().tpmlp_trace_enabled())
+
+
+def tpmlp_trace_read(max_bytes: int = 1 << 20):
+    """Waits for the steps recorded since the last read and returns them as
+    [(step name, device milliseconds)] in the order they were enqueued; [] when
+    tracing is off."""
+    buf = ctypes.create_string_buffer(max_bytes)
+    count = ctypes.c_int(0)
+    _check(lib().tpmlp_trace_read(buf, max_bytes, ctypes.byref(count)), "tpmlp_trace_read")
+    out = []
+    for line in buf.value.decode().splitlines():
+        name, ms = line.rsplit(" ", 1)
+        out.append((name, float(ms)))
+    return out

@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libtpmlp.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "simt.cu", "elementwise.cu", "block.cu", "attention.cu", "attn_api.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "gemm_dual.cu", "simt.cu", "elementwise.cu", "block.cu", "attention.cu", "attn_api.cu", "noalloc.cu", "trace.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "trace.h"
 
 using namespace tpmlp;
 
@@ -50,9 +51,15 @@ int fail(int code, const char* fmt, ...) {
     if (e_ != cudaSuccess) return fail(TPMLP_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
   } while (0)
 
+// TRY_CUDA of a launch that TPMLP_TRACE=1 times as the step `phase` (trace.cu).
+#define TRACED(phase, stream, expr)     \
+  do {                                  \
+    TraceScope trace_scope_(phase, stream); \
+    TRY_CUDA(expr);                     \
+  } while (0)
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-int64_t round_up8(int64_t x) { return (x + 7) / 8 * 8; }
 size_t esize(tpmlp_dtype dt) { return dt == TPMLP_BF16 ? 2 : 4; }
 
 // Read once per process (thread-safe static initialisation).
@@ -91,9 +98,25 @@ int check_handle_device(const tpmlp_shards* sh) {
 
 // Workspace plan: byte offsets of every scratch buffer, 256-byte aligned.
 struct WsPlan {
-  size_t H = 0, Yp = 0, Xt = 0, dYt = 0, P = 0, dH = 0, Ht = 0, dP = 0, dPt = 0, dXp = 0;
+  size_t H = 0, Yp = 0, P = 0, dH = 0, dP = 0, dXp = 0;
   size_t total = 0;
 };
+
+// Whether the bf16 recomputing backward runs its first step in the dual
+// kernel (gemm_dual.cu: P_i and dH_i in tensor memory, P never written): for
+// products with enough 256 x 256 tiles to keep CTA pairs busy, as the other
+// tensor-core products decide (TPMLP_BWD_DUAL=0 computes P_i into the
+// workspace with one product and applies the activation in the epilogue of
+// the dH_i product instead, for comparisons; read once per process).
+bool use_dual_backward(int64_t T, const tpmlp_shards* sh) {
+  static const bool on = [] {
+    const char* e = getenv("TPMLP_BWD_DUAL");
+    return !(e && *e && atoi(e) == 0);
+  }();
+  if (!on || sh->dt != TPMLP_BF16 || !tc_pairs_enabled()) return false;
+  const int64_t tiles = ((T + 255) / 256) * ((sh->Fs + 255) / 256) * sh->n;
+  return tiles >= num_sms() / 4;
+}
 
 WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int backward) {
   WsPlan w;
@@ -103,22 +126,19 @@ WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int ba
     off = round_up(off + bytes, 256);
     return at;
   };
-  const size_t n = sh->n, D = sh->D, Fs = sh->Fs, t = T, tp = round_up8(T), es = esize(sh->dt);
+  const size_t n = sh->n, D = sh->D, Fs = sh->Fs, t = T, es = esize(sh->dt);
   if (!backward) {
     w.H = take(n * t * Fs * es);
     if (mode == TPMLP_FAITHFUL) w.Yp = take(n * t * D * 4);
   } else {
-    if (backward == 1) w.P = take(n * t * Fs * 4);  // backward == 2: the caller's saved P
-    if (sh->dt == TPMLP_F32) {  // bf16 applies the activation in the dH epilogue instead
+    // backward == 2: the caller's saved P; the dual kernel keeps P in tensor memory.
+    if (backward == 1 && !use_dual_backward(T, sh)) w.P = take(n * t * Fs * 4);
+    if (sh->dt == TPMLP_F32) {  // bf16 applies the activation in a product's epilogue instead
       w.H = take(n * t * Fs * 4);
       w.dH = take(n * t * Fs * 4);
-    }
-    if (sh->dt == TPMLP_BF16) {
-      w.Xt = take(D * tp * 2);
-      w.dYt = take(D * tp * 2);
-      w.Ht = take(n * Fs * tp * 2);
+    } else {
+      w.H = take(n * t * Fs * 2);
       w.dP = take(n * t * Fs * 2);
-      w.dPt = take(n * Fs * tp * 2);
     }
     if (mode == TPMLP_FAITHFUL) w.dXp = take(n * t * D * 4);
   }
@@ -137,6 +157,20 @@ int map_or_fail(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, in
     return fail(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the map of %s [%lld x %lld]", what,
                 static_cast<long long>(rows), static_cast<long long>(cols));
   return TPMLP_OK;
+}
+
+// Map of a row-major bf16 [rows][cols] tensor read as an MN-major operand of
+// a product that contracts over its rows: a 3-D map (one TMA box per 128
+// columns) where cols is a multiple of 64, else a 2-D one in 64 x 64 boxes.
+// Adds the matching TcMajor bits (kMnA/kMnA3d, or kMnB/kMnB3d with is_b) to *major.
+int mn_map_or_fail(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t pitch, bool is_b,
+                   int* major, const char* what) {
+  *major |= is_b ? kMnB : kMnA;
+  if (cols % 64 == 0 && make_operand_map_mn3d(m, base, rows, cols, pitch)) {
+    *major |= is_b ? kMnB3d : kMnA3d;
+    return TPMLP_OK;
+  }
+  return map_or_fail(m, base, rows, cols, pitch, 64, what);
 }
 
 int out_map(CUtensorMap* m, void* base, int64_t rows, int64_t cols, int64_t pitch, const char* what) {
@@ -175,7 +209,7 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
     g.group_m = 16;       // bands of 16 M blocks: fewest DRAM re-reads of the shards' A_i^T measured
     g.stream_out = 1;
     g.inject = inject;
-    TRY_CUDA(launch_tc_gemm(g, wait_ns ? wait_ns : wait_limit_ns(), s));
+    TRACED(P_out ? "gemm1_gelu_save_p" : "gemm1_gelu", s, launch_tc_gemm(g, wait_ns ? wait_ns : wait_limit_ns(), s));
     return TPMLP_OK;
   }
   for (int i = 0; i < sh->n; ++i) {
@@ -226,7 +260,7 @@ int run_second(const void* H, int64_t T, const tpmlp_shards* sh, void* out, int 
     g.group_m = 8;
     g.stream_out = 1;
     g.resid = chain ? resid : nullptr;
-    TRY_CUDA(launch_tc_gemm(g, wait_limit_ns(), s));
+    TRACED(chain ? "gemm2_fused_sum" : "gemm2_partials", s, launch_tc_gemm(g, wait_limit_ns(), s));
     return TPMLP_OK;
   }
   // fp32: one product per shard (and, with rank slices, per slice of T/n rows).
@@ -335,7 +369,7 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
   if (mode == TPMLP_FUSED) return run_second(H, T, sh, Y, 1, stream);
   float* Yp = at<float>(ws, w.Yp);
   if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
-  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
+  TRACED("allreduce", stream, launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
   return TPMLP_OK;
 }
 
@@ -344,16 +378,16 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
 int finish_dx(const float* dXp, int n, int64_t T, const tpmlp_shards* sh, void* dX, const LnTail* tail,
               const OutSlices* slices, cudaStream_t s) {
   if (slices) {  // the rank slices were written by the product (fused) or come from the partials
-    if (dXp) TRY_CUDA(launch_reduce_scatter(dXp, n, T * sh->D, *slices, n, s));
+    if (dXp) TRACED("bwd_dx_reduce_scatter", s, launch_reduce_scatter(dXp, n, T * sh->D, *slices, n, s));
     return TPMLP_OK;
   }
   if (tail) {
     const float* G = dXp ? dXp : static_cast<const float*>(dX);
-    TRY_CUDA(launch_layer_norm_bwd(G, dXp ? n : 1, tail->x, tail->dout, T, static_cast<int>(sh->D), tail->eps,
+    TRACED("bwd_layer_norm_tail", s, launch_layer_norm_bwd(G, dXp ? n : 1, tail->x, tail->dout, T, static_cast<int>(sh->D), tail->eps,
                                    sh->dt == TPMLP_BF16, tail->dx, s));
     return TPMLP_OK;
   }
-  if (dXp) TRY_CUDA(launch_allreduce(dXp, n, T * sh->D, static_cast<float*>(dX), s));
+  if (dXp) TRACED("bwd_dx_allreduce", s, launch_allreduce(dXp, n, T * sh->D, static_cast<float*>(dX), s));
   return TPMLP_OK;
 }
 
@@ -397,7 +431,7 @@ int tpmlp_gelu(const void* x, void* y, int64_t n, tpmlp_dtype dt, tpmlp_stream_t
   if (!aligned16(x) || !aligned16(y)) return fail(TPMLP_ERR_ALIGN, "x and y must be 16-byte aligned");
   int rc = check_device(nullptr);
   if (rc) return rc;
-  TRY_CUDA(launch_gelu(x, y, n, dt == TPMLP_BF16, stream));
+  TRACED("gelu", stream, launch_gelu(x, y, n, dt == TPMLP_BF16, stream));
   return TPMLP_OK;
 }
 
@@ -555,7 +589,7 @@ int tpmlp_allreduce(const void* Yp, int n, int64_t count, void* Y, tpmlp_stream_
   if (!aligned16(Yp) || !aligned16(Y)) return fail(TPMLP_ERR_ALIGN, "Yp and Y must be 16-byte aligned");
   int rc = check_device(nullptr);
   if (rc) return rc;
-  TRY_CUDA(launch_allreduce(static_cast<const float*>(Yp), n, count, static_cast<float*>(Y), stream));
+  TRACED("allreduce", stream, launch_allreduce(static_cast<const float*>(Yp), n, count, static_cast<float*>(Y), stream));
   return TPMLP_OK;
 }
 
@@ -666,93 +700,121 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
     return finish_dx(dXp, n, T, sh, dX, tail, dx_slices, s);
   }
 
-  // bf16: tensor-core products on K-major operands.
-  const int64_t Tp = round_up8(T);
-  void* Xt = at<char>(ws, w.Xt);
-  void* dYt = at<char>(ws, w.dYt);
-  uint16_t* Ht = at<uint16_t>(ws, w.Ht);
+  // bf16: tensor-core products. X, dY, H_i and dP_i are read in place: K-major
+  // where the product contracts over their columns, MN-major (64 x 64 boxes)
+  // where it contracts over their rows (the token index T).
+  uint16_t* H = at<uint16_t>(ws, w.H);
   uint16_t* dP = at<uint16_t>(ws, w.dP);
-  uint16_t* dPt = at<uint16_t>(ws, w.dPt);
-  TRY_CUDA(launch_transpose_u16(X, T, D, D, Xt, Tp, s));    // X^T  [D, Tp]
-  TRY_CUDA(launch_transpose_u16(dY, T, D, D, dYt, Tp, s));  // dY^T [D, Tp]
-
-  CUtensorMap mX, mdY, mXt, mdYt;
+  CUtensorMap mX, mdY, mXmn, mdYmn;
+  int major_dB = 0, major_dA = 0;  // TcMajor bits of the dB_i and dA_i products
   if ((rc = map_or_fail(&mX, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
   if ((rc = map_or_fail(&mdY, dY, T, D, D, tc_box_rows_a(), "dY"))) return rc;
-  if ((rc = map_or_fail(&mXt, Xt, D, T, Tp, tc_box_rows_a(), "X^T"))) return rc;
-  if ((rc = map_or_fail(&mdYt, dYt, D, T, Tp, tc_box_rows_b(static_cast<int>(D)), "dY^T"))) return rc;
-  std::vector<CUtensorMap> mHt(n), mdPt(n), mdP(n);
+  if ((rc = mn_map_or_fail(&mXmn, X, T, D, D, false, &major_dA, "X (MN-major)"))) return rc;
+  if ((rc = mn_map_or_fail(&mdYmn, dY, T, D, D, true, &major_dB, "dY (MN-major)"))) return rc;
+  std::vector<CUtensorMap> mHmn(n), mdPmn(n), mdP(n);
   for (int i = 0; i < n; ++i) {
-    if ((rc = map_or_fail(&mHt[i], Ht + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp, tc_box_rows_a(), "H_i^T"))) return rc;
-    if ((rc = map_or_fail(&mdPt[i], dPt + static_cast<size_t>(i) * Fs * Tp, Fs, T, Tp,
-                          tc_box_rows_b(static_cast<int>(Fs)), "dP_i^T")))
-      return rc;
-    if ((rc = map_or_fail(&mdP[i], dP + static_cast<size_t>(i) * T * Fs, T, Fs, Fs, tc_box_rows_a(), "dP_i"))) return rc;
+    uint16_t* Hi = H + static_cast<size_t>(i) * T * Fs;
+    uint16_t* dPi = dP + static_cast<size_t>(i) * T * Fs;
+    int mh = 0, mdp = 0;
+    if ((rc = mn_map_or_fail(&mHmn[i], Hi, T, Fs, Fs, false, &mh, "H_i (MN-major)"))) return rc;
+    if ((rc = mn_map_or_fail(&mdPmn[i], dPi, T, Fs, Fs, true, &mdp, "dP_i (MN-major)"))) return rc;
+    if ((rc = map_or_fail(&mdP[i], dPi, T, Fs, Fs, tc_box_rows_a(), "dP_i"))) return rc;
+    if (i == 0) {  // the same width for every shard, so the same map form
+      major_dB |= mh;
+      major_dA |= mdp;
+    }
   }
   const uint64_t wl = wait_limit_ns();
+  if (!P_saved && use_dual_backward(T, sh)) {
+    // P_i = X A_i and dH_i = dY B_i^T in tensor memory; H_i and dP_i = dH_i *
+    // GeLU'(P_i) from the epilogue.
+    DualBwd d{};
+    d.map_x = &mX;
+    d.map_dy = &mdY;
+    for (int i = 0; i < n; ++i) {
+      d.map_at[i] = &sh->map_At[i];
+      d.map_b[i] = &sh->map_B[i];
+      d.h[i] = H + static_cast<size_t>(i) * T * Fs;
+      d.dp[i] = dP + static_cast<size_t>(i) * T * Fs;
+    }
+    d.ldo = Fs;
+    d.M = static_cast<int>(T);
+    d.N = static_cast<int>(Fs);
+    d.K = static_cast<int>(D);
+    d.groups = n;
+    d.group_m = 16;  // X and dY feed every shard
+    d.load_hint = 1 | (1 << 2);
+    TRACED("bwd_dual_P_dH", s, launch_dual_bwd(d, wl, s));
+  } else {
+    TcGemm g{};
+    g.groups = n;
+    std::vector<CUtensorMap> mo(n);
+    // P_i = X A_i (recompute), fp32, unless the caller saved it.
+    for (int i = 0; i < n; ++i) {
+      g.map_a[i] = &mX;
+      g.map_b[i] = &sh->map_At[i];
+      g.out[i] = P + static_cast<size_t>(i) * T * Fs;
+      if ((rc = out_map(&mo[i], g.out[i], T, Fs, Fs, "P_i"))) return rc;
+      g.map_out[i] = &mo[i];
+    }
+    g.ldo = Fs;
+    g.M = static_cast<int>(T);
+    g.N = static_cast<int>(Fs);
+    g.K = static_cast<int>(D);
+    g.epi = kEpiF32;
+    g.shared = kSharedA;  // X (then dY) feeds every shard
+    g.group_m = 16;
+    g.stream_out = 0;     // P is read back right away by the dH product's epilogue
+    if (!P_saved) TRACED("bwd_recompute_P", s, launch_tc_gemm(g, wl, s));
+    // dH_i = dY B_i^T with the activation step in its epilogue: dP_i = dH_i *
+    // GeLU'(P_i) and H_i = GeLU(P_i), bf16 row-major.
+    for (int i = 0; i < n; ++i) {
+      g.map_a[i] = &mdY;
+      g.map_b[i] = &sh->map_B[i];
+      g.out[i] = dP + static_cast<size_t>(i) * T * Fs;
+      g.out2[i] = H + static_cast<size_t>(i) * T * Fs;
+      g.aux_p[i] = P + static_cast<size_t>(i) * T * Fs;
+      g.map_out[i] = nullptr;
+    }
+    g.epi = kEpiBwdAct;
+    TRACED("bwd_dH_act", s, launch_tc_gemm(g, wl, s));
+  }
   TcGemm g{};
   g.groups = n;
+  g.epi = kEpiF32;
   std::vector<CUtensorMap> mo(n);  // fp32 output maps of the current product (copied at each launch)
-  // P_i = X A_i (recompute), fp32.
+  // dB_i = H_i^T dY: [Fs, D], K = T; both operands MN-major.
   for (int i = 0; i < n; ++i) {
-    g.map_a[i] = &mX;
-    g.map_b[i] = &sh->map_At[i];
-    g.out[i] = P + static_cast<size_t>(i) * T * Fs;
-    if ((rc = out_map(&mo[i], g.out[i], T, Fs, Fs, "P_i"))) return rc;
-    g.map_out[i] = &mo[i];
-  }
-  g.ldo = Fs;
-  g.M = static_cast<int>(T);
-  g.N = static_cast<int>(Fs);
-  g.K = static_cast<int>(D);
-  g.epi = kEpiF32;
-  g.shared = kSharedA;  // X (then dY) feeds every shard
-  g.group_m = 16;
-  g.stream_out = 0;     // P is read back right away by the dH product's epilogue
-  if (!P_saved) TRY_CUDA(launch_tc_gemm(g, wl, s));
-  // dH_i = dY B_i^T with the activation step in its epilogue: dP_i = dH_i *
-  // GeLU'(P_i) and the transposes H_i^T = GeLU(P_i)^T and dP_i^T, all bf16.
-  for (int i = 0; i < n; ++i) {
-    g.map_a[i] = &mdY;
-    g.map_b[i] = &sh->map_B[i];
-    g.out[i] = dP + static_cast<size_t>(i) * T * Fs;
-    g.aux_p[i] = P + static_cast<size_t>(i) * T * Fs;
-    g.aux_ht[i] = Ht + static_cast<size_t>(i) * Fs * Tp;
-    g.aux_dpt[i] = dPt + static_cast<size_t>(i) * Fs * Tp;
-  }
-  g.ldt = Tp;
-  g.epi = kEpiBwdAct;
-  TRY_CUDA(launch_tc_gemm(g, wl, s));
-  g.epi = kEpiF32;
-  // dB_i = H_i^T dY: [Fs, D], K = T.
-  for (int i = 0; i < n; ++i) {
-    g.map_a[i] = &mHt[i];
-    g.map_b[i] = &mdYt;
+    g.map_a[i] = &mHmn[i];
+    g.map_b[i] = &mdYmn;
     g.out[i] = dB[i];
     if ((rc = out_map(&mo[i], g.out[i], Fs, D, D, "dB_i"))) return rc;
+    g.map_out[i] = &mo[i];
   }
   g.ldo = D;
   g.M = static_cast<int>(Fs);
   g.N = static_cast<int>(D);
   g.K = static_cast<int>(T);
-  g.shared = kSharedB;  // dY^T feeds every shard
+  g.mn_major = major_dB;
+  g.shared = kSharedB;  // dY feeds every shard
   g.group_m = 16;
   g.stream_out = 1;
-  TRY_CUDA(launch_tc_gemm(g, wl, s));
-  // dA_i = X^T dP_i: [D, Fs], K = T.
+  TRACED("bwd_dB", s, launch_tc_gemm(g, wl, s));
+  // dA_i = X^T dP_i: [D, Fs], K = T; both operands MN-major.
   for (int i = 0; i < n; ++i) {
-    g.map_a[i] = &mXt;
-    g.map_b[i] = &mdPt[i];
+    g.map_a[i] = &mXmn;
+    g.map_b[i] = &mdPmn[i];
     g.out[i] = dA[i];
     if ((rc = out_map(&mo[i], g.out[i], D, Fs, Fs, "dA_i"))) return rc;
   }
   g.ldo = Fs;
   g.M = static_cast<int>(D);
   g.N = static_cast<int>(Fs);
-  g.shared = kSharedA;  // X^T feeds every shard
+  g.mn_major = major_dA;
+  g.shared = kSharedA;  // X feeds every shard
   g.group_m = 16;
-  TRY_CUDA(launch_tc_gemm(g, wl, s));
-  // dX = sum_i dP_i A_i^T: [T, D], K = Fs.
+  TRACED("bwd_dA", s, launch_tc_gemm(g, wl, s));
+  // dX = sum_i dP_i A_i^T: [T, D], K = Fs; K-major operands.
   for (int i = 0; i < n; ++i) {
     g.map_a[i] = &mdP[i];
     g.map_b[i] = &sh->map_A[i];
@@ -769,10 +831,11 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
   g.M = static_cast<int>(T);
   g.N = static_cast<int>(D);
   g.K = static_cast<int>(Fs);
+  g.mn_major = 0;
   g.chain = dXp ? 0 : 1;
   g.shared = kSharedNone;
   g.group_m = 8;
-  TRY_CUDA(launch_tc_gemm(g, wl, s));
+  TRACED(dXp ? "bwd_dX_partials" : "bwd_dX_fused_sum", s, launch_tc_gemm(g, wl, s));
   return finish_dx(dXp, n, T, sh, dX, tail, dx_slices, s);
 }
 
@@ -789,7 +852,7 @@ int tpmlp_layer_norm(const void* x, int64_t T, int64_t D, tpmlp_dtype dt, float 
   if (!x || !y) return fail(TPMLP_ERR_ARG, "x and y must not be NULL");
   if (!aligned16(x) || !aligned16(y)) return fail(TPMLP_ERR_ALIGN, "x and y must be 16-byte aligned");
   if ((rc = check_device(nullptr))) return rc;
-  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(D), eps, dt == TPMLP_BF16, y, stream));
+  TRACED("layer_norm", stream, launch_layer_norm(x, T, static_cast<int>(D), eps, dt == TPMLP_BF16, y, stream));
   return TPMLP_OK;
 }
 
@@ -816,13 +879,13 @@ int tpmlp_block_forward(const void* x, int64_t T, const tpmlp_shards* sh, float 
   const bool bf16 = sh->dt == TPMLP_BF16;
   void* xnb = xn ? xn : at<char>(ws, b.xn);
   void* inner = at<char>(ws, b.inner);
-  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(sh->D), eps, bf16, xnb, stream));
+  TRACED("layer_norm", stream, launch_layer_norm(x, T, static_cast<int>(sh->D), eps, bf16, xnb, stream));
   void* H = at<char>(inner, b.w.H);
   if ((rc = run_hidden(xnb, T, sh, H, stream))) return rc;
   if (mode == TPMLP_FUSED) return run_second(H, T, sh, out, 1, stream, x);
   float* Yp = at<float>(inner, b.w.Yp);
   if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
-  TRY_CUDA(launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(out), stream, x, bf16 ? 2 : 1));
+  TRACED("allreduce_residual", stream, launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(out), stream, x, bf16 ? 2 : 1));
   return TPMLP_OK;
 }
 
@@ -843,7 +906,7 @@ int tpmlp_block_backward(const void* x, const void* dout, int64_t T, const tpmlp
   if (ws_bytes < b.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, b.total);
   if ((rc = check_handle_device(sh))) return rc;
   void* xn = at<char>(ws, b.xn);
-  TRY_CUDA(launch_layer_norm(x, T, static_cast<int>(sh->D), eps, sh->dt == TPMLP_BF16, xn, stream));
+  TRACED("layer_norm", stream, launch_layer_norm(x, T, static_cast<int>(sh->D), eps, sh->dt == TPMLP_BF16, xn, stream));
   const LnTail tail{x, dout, eps, static_cast<float*>(dx)};
   void* dxn = mode == TPMLP_FUSED ? at<char>(ws, b.dxn) : dx;  // FAITHFUL: the partials feed the tail directly
   return backward_impl(xn, dout, nullptr, T, sh, dxn, dA, dB, mode, at<char>(ws, b.inner), b.w.total, stream, &tail);
@@ -862,7 +925,7 @@ int tpmlp_all_gather(const void* const* slices, int n, int64_t slice_bytes, void
   if ((rc = check_device(nullptr))) return rc;
   InSlices in{};
   for (int j = 0; j < n; ++j) in.p[j] = slices[j];
-  TRY_CUDA(launch_all_gather(in, n, slice_bytes, out, stream));
+  TRACED("all_gather", stream, launch_all_gather(in, n, slice_bytes, out, stream));
   return TPMLP_OK;
 }
 
@@ -879,7 +942,7 @@ int tpmlp_reduce_scatter(const void* Yp, int n, int64_t count, void* const* Y_sl
   if ((rc = check_device(nullptr))) return rc;
   OutSlices out{};
   for (int j = 0; j < n; ++j) out.p[j] = static_cast<float*>(Y_slices[j]);
-  TRY_CUDA(launch_reduce_scatter(static_cast<const float*>(Yp), n, count, out, n, stream));
+  TRACED("reduce_scatter", stream, launch_reduce_scatter(static_cast<const float*>(Yp), n, count, out, n, stream));
   return TPMLP_OK;
 }
 
@@ -915,13 +978,13 @@ int tpmlp_forward_sp(const void* const* X_slices, int64_t T, const tpmlp_shards*
   }
   void* X = at<char>(ws, p.x);
   void* inner = at<char>(ws, p.inner);
-  TRY_CUDA(launch_all_gather(in, n, Ts * D * static_cast<int64_t>(esize(sh->dt)), X, stream));
+  TRACED("all_gather", stream, launch_all_gather(in, n, Ts * D * static_cast<int64_t>(esize(sh->dt)), X, stream));
   void* H = at<char>(inner, p.w.H);
   if ((rc = run_hidden(X, T, sh, H, stream))) return rc;
   if (mode == TPMLP_FUSED) return run_second(H, T, sh, nullptr, 1, stream, nullptr, &out);
   float* Yp = at<float>(inner, p.w.Yp);
   if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
-  TRY_CUDA(launch_reduce_scatter(Yp, n, T * D, out, n, stream));
+  TRACED("reduce_scatter", stream, launch_reduce_scatter(Yp, n, T * D, out, n, stream));
   return TPMLP_OK;
 }
 
@@ -946,9 +1009,9 @@ int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices,
   const int64_t slice_bytes = (T / n) * sh->D * static_cast<int64_t>(esize(sh->dt));
   InSlices in{};
   for (int j = 0; j < n; ++j) in.p[j] = X_slices[j];
-  TRY_CUDA(launch_all_gather(in, n, slice_bytes, at<char>(ws, p.x), stream));
+  TRACED("all_gather", stream, launch_all_gather(in, n, slice_bytes, at<char>(ws, p.x), stream));
   for (int j = 0; j < n; ++j) in.p[j] = dY_slices[j];
-  TRY_CUDA(launch_all_gather(in, n, slice_bytes, at<char>(ws, p.dy), stream));
+  TRACED("all_gather", stream, launch_all_gather(in, n, slice_bytes, at<char>(ws, p.dy), stream));
   OutSlices out{};
   for (int j = 0; j < n; ++j) out.p[j] = static_cast<float*>(dX_slices[j]);
   // dX itself is never written: the partials are reduce-scattered (FAITHFUL) or

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "trace.h"
 
 using namespace tpmlp;
 
@@ -33,6 +34,13 @@ namespace {
   do {                                                                                                  \
     cudaError_t e_ = (expr);                                                                            \
     if (e_ != cudaSuccess) return set_error(TPMLP_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));   \
+  } while (0)
+
+// ATTN_TRY of a launch that TPMLP_TRACE=1 times as the step `phase` (trace.cu).
+#define ATTN_TRACED(phase, stream, expr)    \
+  do {                                      \
+    TraceScope trace_scope_(phase, stream); \
+    ATTN_TRY(expr);                         \
   } while (0)
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,7 +155,7 @@ int run_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards
   g.epi = kEpiBf16;
   g.shared = kSharedA;
   g.group_m = 16;
-  ATTN_TRY(launch_tc_gemm(g, attn_wait_ns(), s));
+  ATTN_TRACED("attn_qkv", s, launch_tc_gemm(g, attn_wait_ns(), s));
   std::vector<CUtensorMap> mq(n), mv(n);
   AttnLaunch a{};
   for (int i = 0; i < n; ++i) {
@@ -167,7 +175,7 @@ int run_heads(const void* X, int64_t batch, int64_t seq, const tpmlp_attn_shards
   a.wait_ns = attn_wait_ns();
   a.status = device_status_word();
   if (!a.status) return set_error(TPMLP_ERR_CUDA, "the device status word is not available");
-  ATTN_TRY(launch_attention_tc(a, s));
+  ATTN_TRACED("attn_core", s, launch_attention_tc(a, s));
   return TPMLP_OK;
 }
 
@@ -342,9 +350,9 @@ int tpmlp_attn_forward(const void* X, int64_t batch, int64_t seq, const tpmlp_at
     g.epi = kEpiF32;
     g.group_m = 8;
     g.stream_out = 1;
-    ATTN_TRY(launch_tc_gemm(g, attn_wait_ns(), s));
+    ATTN_TRACED("attn_out_proj", s, launch_tc_gemm(g, attn_wait_ns(), s));
   }
-  if (Yp) ATTN_TRY(launch_allreduce(Yp, n, T * D, static_cast<float*>(Y), s));
+  if (Yp) ATTN_TRACED("allreduce", s, launch_allreduce(Yp, n, T * D, static_cast<float*>(Y), s));
   return TPMLP_OK;
 }
 

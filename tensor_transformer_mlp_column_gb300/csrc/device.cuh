@@ -151,6 +151,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// 3-D form of tma_load_2d_hint: box at (x, y, z).
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                                 uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // 2-D tiled bulk tensor store from this CTA's shared memory; the box at
 // (x, y) is clipped to the tensor's bounds. Completion is tracked per thread
 // with bulk groups.
@@ -327,6 +337,16 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorM
       : "memory");
 }
 
+// 3-D form of tma_load_2d_pair_hint: box at (x, y, z).
+__device__ __forceinline__ void tma_load_3d_pair_hint(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                                      int32_t z, uint32_t bar_cluster_addr, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster_addr), "l"(policy)
+      : "memory");
+}
+
 // TMEM allocation shared by the CTA pair: one warp of EACH CTA executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
@@ -375,14 +395,45 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B (both
-// K-major), fp32 accumulator, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Shared-memory matrix descriptor for an MN-major bf16 tile (M or N
+// contiguous) with 128-byte swizzling, as TMA writes it from a row-major
+// [K][MN] tensor in boxes of 64 MN elements x 64 K rows: each K row of a box
+// is one 128-byte line (64 consecutive MN elements), 8 K rows form a
+// 1024-byte swizzle atom. The stride-dimension offset steps from one group of
+// 8 K rows to the next (1024 B); the leading offset steps from one 64-element
+// MN chunk to the next, i.e. from one box to the next (8 KB apart). One
+// K = 16 instruction reads 16 K rows, so successive instructions start
+// 2048 bytes apart.
+constexpr uint32_t kMnChunkBytes = 64 * 64 * 2;  // one 64 (MN) x 64 (K) box
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);        // start address
+  d |= static_cast<uint64_t>(kMnChunkBytes >> 4) << 16;       // leading byte offset: next 64-element MN chunk
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                // stride byte offset: next 8 K rows
+  d |= static_cast<uint64_t>(1u) << 46;                        // version
+  d |= static_cast<uint64_t>(2u) << 61;                        // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: bf16 A and B, fp32
+// accumulator, shape M x N. a_mn / b_mn (bits 15 / 16) mark an operand held
+// MN-major (M or N contiguous) instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, uint32_t a_mn = 0, uint32_t b_mn = 0) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
+         | ((a_mn & 1u) << 15)                       // A MN-major
+         | ((b_mn & 1u) << 16)                       // B MN-major
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Descriptor of the K = 16 slice k (0..3) of one 64-deep K block of an
+// operand tile at saddr: K-major tiles advance 32 bytes along the swizzled
+// row, MN-major tiles 16 K rows (2048 bytes).
+__device__ __forceinline__ uint64_t operand_desc(uint32_t saddr, int k, bool mn_major) {
+  return mn_major ? smem_desc_sw128_mn(saddr + 2048u * static_cast<uint32_t>(k))
+                  : smem_desc_sw128(saddr + 32u * static_cast<uint32_t>(k));
 }
 
 // ------------------------------------------------------------------ math

@@ -15,11 +15,10 @@ struct KParams {
   CUtensorMap map_a[kMaxGroups];
   CUtensorMap map_b[kMaxGroups];
   void* out[kMaxGroups];
-  void* out2[kMaxGroups];           // kEpiGeluSaveP: fp32 pre-activation per group (row pitch ldo)
+  void* out2[kMaxGroups];           // kEpiGeluSaveP: fp32 pre-activation; kEpiBwdAct: H (bf16); row pitch ldo
   CUtensorMap map_out[kMaxGroups];  // kEpiF32Tma: fp32 output per group, 32 x 32 boxes, 128-byte swizzle
   const void* aux_p[kMaxGroups];    // kEpiBwdAct: P per group (fp32, row pitch ldo)
-  void* aux_ht[kMaxGroups];         // kEpiBwdAct: H^T per group (bf16, row pitch ldt)
-  void* aux_dpt[kMaxGroups];        // kEpiBwdAct: dP^T per group (bf16, row pitch ldt)
+  void* aux_ht[kMaxGroups];         // kEpiBf16: V^T per group (bf16, row pitch ldt)
   int64_t ldo, ldt;
   int M, N;
   int groups;
@@ -36,6 +35,7 @@ struct KParams {
   const __nv_bfloat16* resid;  // kEpiF32 / kEpiF32Tma: residual [M][ldo] added to the accumulator, or null
   int64_t slice_rows;          // kEpiF32, chain: output row m goes to row m % slice_rows of out[m / slice_rows]
   int vt_col0;                 // kEpiBf16 with aux_ht: columns >= vt_col0 go transposed to aux_ht (row pitch ldt)
+  int mn_major;                // TcMajor bits: MN-major operands and their map form
 };
 
 // Maps a tile index to (group, M block, N block). The tiles form a grid of
@@ -49,7 +49,10 @@ struct KParams {
 //     M blocks stacked, cols = N blocks;
 //   otherwise each group's grid in turn (chain mode: the one output grid).
 // "Blocks" are the kernel's tile units.
-__device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
+struct TileGrid {
+  int chain, shared, groups, m_blocks, n_blocks, group_m;
+};
+__device__ __forceinline__ void decode_tile(const TileGrid& p, int tile, int& g, int& mb, int& nb) {
   int rows_total, cols, base = 0;
   if (p.chain || p.shared == kSharedNone) {
     const int per_group = p.m_blocks * p.n_blocks;
@@ -84,6 +87,9 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
     mb = row % p.m_blocks;
     nb = col;
   }
+}
+__device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, int& mb, int& nb) {
+  decode_tile(TileGrid{p.chain, p.shared, p.groups, p.m_blocks, p.n_blocks, p.group_m}, tile, g, mb, nb);
 }
 
 // 16-byte global stores; `stream` marks them evict-first so results that are
@@ -186,14 +192,11 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
     }
   } else {
     // Backward activation: acc = dH (row m = token t, column n = feature f).
-    // With P from aux_p: dP = dH * GeLU'(P) to out (bf16 [T][ldo]), and the
-    // transposes H^T = GeLU(P)^T to aux_ht and dP^T to aux_dpt (bf16 [F][ldt]).
-    // The 32 lanes of a warp hold 32 consecutive tokens, so each transposed
-    // store of one column is 64 contiguous bytes.
+    // With P from aux_p: dP = dH * GeLU'(P) to out and H = GeLU(P) to out2,
+    // both bf16 row-major [T][ldo].
     const float* P = static_cast<const float*>(p.aux_p[g]) + m * p.ldo + n0;
     __nv_bfloat16* dP = static_cast<__nv_bfloat16*>(p.out[g]) + m * p.ldo + n0;
-    __nv_bfloat16* Ht = static_cast<__nv_bfloat16*>(p.aux_ht[g]) + int64_t(n0) * p.ldt + m;
-    __nv_bfloat16* dPt = static_cast<__nv_bfloat16*>(p.aux_dpt[g]) + int64_t(n0) * p.ldt + m;
+    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out2[g]) + m * p.ldo + n0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (n0 + 8 * j + 8 > p.N) continue;
@@ -214,12 +217,11 @@ __device__ __forceinline__ void epilogue_store(const KParams& p, int g, int64_t 
       w.z = pack_bf16x2(d[4], d[5]);
       w.w = pack_bf16x2(d[6], d[7]);
       store16(dP + 8 * j, w, false);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int64_t o = int64_t(8 * j + e) * p.ldt;
-        Ht[o] = __float2bfloat16_rn(h[e]);
-        dPt[o] = __float2bfloat16_rn(d[e]);
-      }
+      w.x = pack_bf16x2(h[0], h[1]);
+      w.y = pack_bf16x2(h[2], h[3]);
+      w.z = pack_bf16x2(h[4], h[5]);
+      w.w = pack_bf16x2(h[6], h[7]);
+      store16(H + 8 * j, w, false);
     }
   }
 }

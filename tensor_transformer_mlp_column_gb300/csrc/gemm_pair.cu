@@ -3,7 +3,10 @@
 //
 // Per k-block each CTA brings in its 128 rows of the M x K operand and its
 // 128 of the 256 rows of the N x K operand (the pair MMA reads both CTAs'
-// shared memory); every CTA loads only into its own shared memory.
+// shared memory); every CTA loads only into its own shared memory. An
+// operand may be K-major (one 64 x 128 box) or MN-major (a row-major [K][M]
+// tensor: two 64-wide chunks of 64 K rows), so products with a transposed
+// operand read it in place.
 //   every CTA, warp 0 lane 0 : TMA producer; the pair's bytes are counted on
 //                              the full barrier of the pair's even CTA, which
 //                              its producer arms with both CTAs' bytes
@@ -150,10 +153,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
               parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
             }
             for (int u = 0; u < nsub; ++u) {
-              tma_load_2d_pair_hint(sA + stage * C::A_BYTES + u * kSubBytes, &p.map_a[gg], kk * BK, m0, full_lead,
-                                    pol_a);
-              tma_load_2d_pair_hint(sB + stage * C::B_BYTES + u * kSubBytes, &p.map_b[gg], kk * BK, n0, full_lead,
-                                    pol_b);
+              uint8_t* da = sA + stage * C::A_BYTES + u * kSubBytes;
+              uint8_t* db = sB + stage * C::B_BYTES + u * kSubBytes;
+              // MN-major operands ([K][M] tensors) arrive as two 64-wide chunks of
+              // 64 K rows: one box of a 3-D map (chunk index z = m0 / 64) or two
+              // boxes of a 2-D one.
+              if (p.mn_major & kMnA3d) {
+                tma_load_3d_pair_hint(da, &p.map_a[gg], 0, kk * BK, m0 / 64, full_lead, pol_a);
+              } else if (p.mn_major & kMnA) {
+                tma_load_2d_pair_hint(da, &p.map_a[gg], m0, kk * BK, full_lead, pol_a);
+                tma_load_2d_pair_hint(da + kMnChunkBytes, &p.map_a[gg], m0 + 64, kk * BK, full_lead, pol_a);
+              } else {
+                tma_load_2d_pair_hint(da, &p.map_a[gg], kk * BK, m0, full_lead, pol_a);
+              }
+              if (p.mn_major & kMnB3d) {
+                tma_load_3d_pair_hint(db, &p.map_b[gg], 0, kk * BK, n0 / 64, full_lead, pol_b);
+              } else if (p.mn_major & kMnB) {
+                tma_load_2d_pair_hint(db, &p.map_b[gg], n0, kk * BK, full_lead, pol_b);
+                tma_load_2d_pair_hint(db + kMnChunkBytes, &p.map_b[gg], n0 + 64, kk * BK, full_lead, pol_b);
+              } else {
+                tma_load_2d_pair_hint(db, &p.map_b[gg], kk * BK, n0, full_lead, pol_b);
+              }
               if (++kk == p.k_blocks) {
                 kk = 0;
                 ++gg;
@@ -189,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   } else if (warp == 1) {
     if (lane == 0 && pos == 0) {
       // ---------------- MMA issuer (even CTA of each pair)
-      constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
+      const bool a_mn = (p.mn_major & kMnA) != 0, b_mn = (p.mn_major & kMnB) != 0;
+      const uint32_t idesc = idesc_bf16_f32(256, BN, a_mn, b_mn);
       constexpr uint16_t kPairMask = 0x3;  // both CTAs: each holds half of every stage and of every accumulator
       int stage = 0;
       uint32_t phase = 0;
@@ -214,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
             const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES + u * kSubBytes);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+              tc_mma_bf16_pair(d_tmem, operand_desc(a0, k, a_mn), operand_desc(b0, k, b_mn), idesc,
                                (kb | u | k) != 0 ? 1u : 0u);
             }
           }

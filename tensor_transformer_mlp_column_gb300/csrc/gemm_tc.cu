@@ -121,10 +121,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (fill != p.inject) {
             mbar_arrive_expect_tx(full + stage, nsub * (C::A_SUB + C::B_SUB));
             for (int u = 0; u < nsub; ++u) {
-              tma_load_2d_hint(sA + stage * C::A_BYTES + u * C::A_SUB, &p.map_a[gg], kk * BK, mb * BM, full + stage,
-                               pol_a);
-              tma_load_2d_hint(sB + stage * C::B_BYTES + u * C::B_SUB, &p.map_b[gg], kk * BK, nb * BN, full + stage,
-                               pol_b);
+              uint8_t* da = sA + stage * C::A_BYTES + u * C::A_SUB;
+              uint8_t* db = sB + stage * C::B_BYTES + u * C::B_SUB;
+              // MN-major operands ([K][M] tensors): 64-wide chunks of 64 K rows,
+              // two per box of a 3-D map or one per box of a 2-D one.
+              if (p.mn_major & kMnA3d) {
+                tma_load_3d_hint(da, &p.map_a[gg], 0, kk * BK, mb * BM / 64, full + stage, pol_a);
+              } else if (p.mn_major & kMnA) {
+                for (int c = 0; c < BM / 64; ++c)
+                  tma_load_2d_hint(da + c * kMnChunkBytes, &p.map_a[gg], mb * BM + 64 * c, kk * BK, full + stage,
+                                   pol_a);
+              } else {
+                tma_load_2d_hint(da, &p.map_a[gg], kk * BK, mb * BM, full + stage, pol_a);
+              }
+              if (p.mn_major & kMnB3d) {
+                for (int c = 0; c < BN / 128; ++c)
+                  tma_load_3d_hint(db + c * 2 * kMnChunkBytes, &p.map_b[gg], 0, kk * BK, (nb * BN + 128 * c) / 64,
+                                   full + stage, pol_b);
+              } else if (p.mn_major & kMnB) {
+                for (int c = 0; c < BN / 64; ++c)
+                  tma_load_2d_hint(db + c * kMnChunkBytes, &p.map_b[gg], nb * BN + 64 * c, kk * BK, full + stage,
+                                   pol_b);
+              } else {
+                tma_load_2d_hint(db, &p.map_b[gg], kk * BK, nb * BN, full + stage, pol_b);
+              }
               if (++kk == p.k_blocks) {
                 kk = 0;
                 ++gg;
@@ -154,7 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer
-      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      const bool a_mn = (p.mn_major & kMnA) != 0, b_mn = (p.mn_major & kMnB) != 0;
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, a_mn, b_mn);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -179,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const uint32_t b0 = smem_addr(sB + stage * C::B_BYTES + u * C::B_SUB);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+              tc_mma_bf16(d_tmem, operand_desc(a0, k, a_mn), operand_desc(b0, k, b_mn), idesc,
                           (kb | u | k) != 0 ? 1u : 0u);
             }
           }
@@ -334,6 +355,8 @@ int* status_word() {
 
 int* device_status_word() { return status_word(); }
 
+bool tc_pairs_enabled() { return kernel_family() >= 1; }
+
 bool pdl_enabled() {
   static const bool v = env_int("TPMLP_PDL", 1) != 0;
   return v;
@@ -394,6 +417,30 @@ bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t 
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, pitch_elems * 2, BK, box_rows);
 }
 
+bool make_operand_map_mn3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems) {
+  if (cols % 64 != 0 || cols > pitch_elems) return false;
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
+  // Element (i, k, c) = base[k * pitch + 64 c + i]: the row-major [rows][cols]
+  // tensor seen as cols / 64 chunks of 64 columns.
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch_elems * 2), 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BK), 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems) {
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rows, cols, pitch_elems * 4, 32, 32);
 }
@@ -408,7 +455,6 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
     kp.out2[i] = g.out2[i];
     kp.aux_p[i] = g.aux_p[i];
     kp.aux_ht[i] = g.aux_ht[i];
-    kp.aux_dpt[i] = g.aux_dpt[i];
     if (g.map_out[i]) kp.map_out[i] = *g.map_out[i];
   }
   // CTA pairs with 256 x 256 tiles, unless the product has too few
@@ -459,6 +505,11 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   if (kp.resid && g.epi != kEpiF32) return cudaErrorInvalidValue;
   kp.slice_rows = g.slice_rows;
   kp.vt_col0 = g.vt_col0;
+  kp.mn_major = g.mn_major;
+  // No narrow or chained MN-major products; 3-D maps only with their operand MN-major.
+  if (g.mn_major && (g.chain || BN == 64)) return cudaErrorInvalidValue;
+  if (((g.mn_major & kMnA3d) && !(g.mn_major & kMnA)) || ((g.mn_major & kMnB3d) && !(g.mn_major & kMnB)))
+    return cudaErrorInvalidValue;
   if (g.slice_rows && (g.epi != kEpiF32 || !g.chain || g.resid)) return cudaErrorInvalidValue;
   if (!kp.status) return cudaErrorInvalidSymbol;
   if (kp.tiles == 0) return cudaSuccess;

@@ -25,7 +25,7 @@ enum WaitSite : int {
 enum TcEpilogue : int {
   kEpiGeluBf16 = 0,  // out bf16 = GeLU(acc)
   kEpiF32 = 1,       // out fp32 = acc
-  kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), aux_ht = GeLU(P)^T, aux_dpt = out^T (P from aux_p)
+  kEpiBwdAct = 2,    // acc = dH: out bf16 = dH * GeLU'(P), out2 bf16 = GeLU(P) (P from aux_p), row-major
   kEpiF32Tma = 3,    // out fp32 = acc through TMA stores (chosen by the launcher when map_out is given)
   kEpiGeluSaveP = 4, // out bf16 = GeLU(acc) and out2 fp32 = acc (the pre-activation), same row stride
   kEpiBf16 = 5,      // out bf16 = acc
@@ -37,19 +37,19 @@ enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
 //   out[g][m, n] = sum_k Aop_g[m, k] * Bop_g[n, k]        (chain == 0)
 // or, with chain == 1, a single output
 //   out[0][m, n] = sum_g sum_k Aop_g[m, k] * Bop_g[n, k]  (groups in order 0..G-1).
-// Both operands are bf16, K-major (row-major with K contiguous), described by
-// 2-D TMA maps made with make_operand_map().
+// Both operands are bf16, K-major (row-major with K contiguous) unless
+// mn_major says otherwise, described by 2-D TMA maps made with
+// make_operand_map().
 struct TcGemm {
   const CUtensorMap* map_a[kMaxGroups];  // M x K operand of each group
   const CUtensorMap* map_b[kMaxGroups];  // N x K operand of each group
   const CUtensorMap* map_b_narrow[kMaxGroups];  // optional: the same operands in 64-row boxes (narrow single-CTA
                                                 // tiles; used only when every group has one)
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
-  void* out2[kMaxGroups];                // kEpiGeluSaveP only: fp32 pre-activation, row stride ldo
+  void* out2[kMaxGroups];                // kEpiGeluSaveP: fp32 pre-activation; kEpiBwdAct: H (bf16); row stride ldo
   const CUtensorMap* map_out[kMaxGroups];  // optional fp32 output maps (make_output_map_f32) for TMA stores
   const void* aux_p[kMaxGroups];         // kEpiBwdAct only: P (fp32, row stride ldo)
-  void* aux_ht[kMaxGroups];              // kEpiBwdAct only: H^T (bf16, row stride ldt)
-  void* aux_dpt[kMaxGroups];             // kEpiBwdAct only: dP^T (bf16, row stride ldt)
+  void* aux_ht[kMaxGroups];              // kEpiBf16 only: V^T (bf16, row stride ldt)
   int64_t ldo;
   int64_t ldt;
   int M, N, K;
@@ -65,13 +65,45 @@ struct TcGemm {
                        // slice of slice_rows rows); 0 = off
   int vt_col0;         // kEpiBf16 with aux_ht[g]: output columns >= vt_col0 are written transposed to aux_ht[g]
                        // (bf16, row pitch ldt) instead of to out[g]
+  int mn_major;        // TcMajor bits: kMnA: map_a holds the M x K operand MN-major, i.e. a row-major [K][M]
+                       // tensor (M contiguous), either as a 2-D map in 64 x 64 boxes (make_operand_map with
+                       // 64-row boxes) or, with kMnA3d, as a 3-D map (make_operand_map_mn3d); kMnB, kMnB3d: the
+                       // same for map_b and the N x K operand
 };
+
+enum TcMajor : int { kMnA = 1, kMnB = 2, kMnA3d = 4, kMnB3d = 8 };
+
+// The backward's first step for every shard i in one kernel (gemm_dual.cu):
+// P_i = X A_i and dH_i = dY B_i^T accumulated in tensor memory, then
+// h[i] = GeLU(P_i) and dp[i] = dH_i * GeLU'(P_i), bf16 [M][ldo]. All four
+// operand maps are K-major with 128-row boxes: X, dY [M][K]; A_i^T, B_i [N][K].
+struct DualBwd {
+  const CUtensorMap* map_x;
+  const CUtensorMap* map_dy;
+  const CUtensorMap* map_at[kMaxGroups];
+  const CUtensorMap* map_b[kMaxGroups];
+  void* h[kMaxGroups];
+  void* dp[kMaxGroups];
+  int64_t ldo;
+  int M, N, K;
+  int groups;
+  int group_m;    // tile order (decode_tile), X and dY shared by every group
+  int load_hint;  // L2 policy kinds of the M x K loads (bits 0-1) and the N x K loads (2-3)
+};
+cudaError_t launch_dual_bwd(const DualBwd& d, uint64_t wait_ns, cudaStream_t s);
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
 // `pitch_elems` (cols contiguous), boxes of 64 columns x box_rows rows and
 // 128-byte swizzling. Returns false if the driver rejects it.
 bool make_operand_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems,
                       int box_rows);
+
+// Encodes a 3-D TMA map of a row-major bf16 matrix [rows, cols] (row pitch
+// pitch_elems) read as an MN-major operand: cols / 64 chunks of 64 columns,
+// each box two chunks x 64 rows (16 KB, one instruction where the 2-D map
+// takes two). Needs cols % 64 == 0; returns false otherwise or if the driver
+// rejects it.
+bool make_operand_map_mn3d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
 
 // Encodes a TMA map for an fp32 output matrix [rows, cols] (row pitch
 // pitch_elems) written in 32 x 32 boxes with 128-byte swizzling.
@@ -81,6 +113,9 @@ int tc_box_rows_a();       // M x K operand (rows of the output)
 int tc_box_rows_b(int N);  // N x K operand of a product with N output columns
 
 cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s);
+// Whether products with enough 256 x 256 tiles run on CTA pairs (the default;
+// TPMLP_TC_KERNEL=0 keeps every product on single CTAs).
+bool tc_pairs_enabled();
 
 // fp32 CUDA-core GEMM with arbitrary element strides:
 //   C[m, n] (op)= sum_k A[m*sam + k*sak] * B[k*sbk + n*sbn]

@@ -185,3 +185,19 @@ def test_attention_argument_errors_without_gpu(tp):
     assert l.tpmlp_attn_forward(FAKE, 2, 8, None, FAKE, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
     assert l.tpmlp_attn_shard_get(None, 0, None, None) == tp.TPMLP_ERR_ARG
     l.tpmlp_attn_shards_free(None)
+
+
+def test_trace_read_without_tracing(tp):
+    """With TPMLP_TRACE unset nothing is recorded: the read returns an empty
+    string and no records; a NULL buffer with a non-zero size is an argument
+    error."""
+    if os.environ.get("TPMLP_TRACE"):
+        pytest.skip("TPMLP_TRACE is set in this process")
+    assert tp.tpmlp_trace_enabled() is False
+    assert tp.tpmlp_trace_read() == []
+    buf = ctypes.create_string_buffer(b"x" * 15)
+    count = ctypes.c_int(-1)
+    assert tp.lib().tpmlp_trace_read(buf, 16, ctypes.byref(count)) == tp.TPMLP_OK
+    assert buf.value == b"" and count.value == 0
+    assert tp.lib().tpmlp_trace_read(None, 16, None) == tp.TPMLP_ERR_ARG
+    assert tp.lib().tpmlp_trace_read(None, 0, None) == tp.TPMLP_OK
