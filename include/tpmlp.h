@@ -67,8 +67,9 @@ typedef enum {
   TPMLP_ERR_TIMEOUT = -6,      /* a device-side wait ran out of time          */
   TPMLP_ERR_WORKSPACE = -7,    /* workspace missing or smaller than required  */
   TPMLP_ERR_UNSUPPORTED = -8,  /* e.g. bf16 with more than TPMLP_MAX_SHARDS   */
-  TPMLP_ERR_DEVICE = -9        /* current device is not sm_103 / shards handle
+  TPMLP_ERR_DEVICE = -9,       /* current device is not sm_103 / shards handle
                                   belongs to another device                   */
+  TPMLP_ERR_BOUNDS = -10       /* debug build: a device-side index check failed */
 } tpmlp_status;
 
 /* Largest shard count of the bf16 tensor-core path (the fp32 path has none). */
@@ -85,9 +86,28 @@ const char* tpmlp_last_error(void);
 
 /* Waits for `stream`, then reads and clears the current device's status word.
  * Returns TPMLP_OK, TPMLP_ERR_TIMEOUT if a kernel gave up on a wait since the
- * last check, or TPMLP_ERR_CUDA if the stream reports an error or a kernel
- * found its dynamic shared memory misaligned (it then did no work). */
+ * last check, TPMLP_ERR_BOUNDS if a device-side check of the debug build
+ * failed (see tpmlp_build_flags), or TPMLP_ERR_CUDA if the stream reports an
+ * error or a kernel found its dynamic shared memory misaligned (it then did
+ * no work). The first failure since the last check is the one reported. */
 int tpmlp_check_status(tpmlp_stream_t stream);
+
+/* Build flags of the loaded library: bit 0 is set in the debug build
+ * (compiled with TPMLP_DEBUG; the Python binding loads it as
+ * libtpmlp_debug.so when TPMLP_DEBUG=1 is set). In that build the kernels
+ * check their tile, TMA-coordinate, output, reduce-slice and attention-tile
+ * indices on the device; a failed check skips the access it guards (the
+ * kernel does not trap), stops the kernel's work where skipping would leave
+ * it waiting, and records TPMLP_ERR_BOUNDS for tpmlp_check_status. The
+ * results of the two builds are identical when no check fails. */
+int tpmlp_build_flags(void);
+
+/* Test hook for the debug build's checks: one block writes element `index`
+ * of a 32-element shared-memory array, guarded by a device-side check. With
+ * 0 <= index < 32 nothing is recorded; otherwise the check fails, the write
+ * is skipped and the next tpmlp_check_status() returns TPMLP_ERR_BOUNDS.
+ * Returns TPMLP_ERR_UNSUPPORTED (and launches nothing) in the normal build. */
+int tpmlp_selftest_bounds(int index, tpmlp_stream_t stream);
 
 /* gelu(x), elementwise: GeLU(x) = 1/2 x (1 + tanh u), u = sqrt(2/pi)(x + 0.044715 x^3)
  * ([P4] section "GeLU"; "What to implement", first bullet).

@@ -18,7 +18,10 @@ from typing import Optional, Sequence
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp.so")
+# TPMLP_DEBUG=1 loads the debug build (device-side index checks; build it with
+# build_lib.build(debug=True)) instead of the normal one.
+DEBUG = os.environ.get("TPMLP_DEBUG", "") not in ("", "0")
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtpmlp_debug.so" if DEBUG else "libtpmlp.so")
 
 TPMLP_F32, TPMLP_BF16 = 0, 1
 TPMLP_FAITHFUL, TPMLP_FUSED = 0, 1
@@ -35,6 +38,7 @@ STATUS_NAMES = {
     -7: "TPMLP_ERR_WORKSPACE",
     -8: "TPMLP_ERR_UNSUPPORTED",
     -9: "TPMLP_ERR_DEVICE",
+    -10: "TPMLP_ERR_BOUNDS",
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 
@@ -81,6 +85,8 @@ SIGNATURES = {
                                ctypes.POINTER(_P), ctypes.POINTER(_P), _I, _P, _SZ, _P]),
     "tpmlp_trace_read": (_I, [ctypes.c_char_p, _SZ, ctypes.POINTER(_I)]),
     "tpmlp_trace_enabled": (_I, []),
+    "tpmlp_build_flags": (_I, []),
+    "tpmlp_selftest_bounds": (_I, [_I, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -97,9 +103,9 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`"
-            )
+            how = ("`python -m tensor_transformer_mlp_column_gb300.build_lib --debug`" if DEBUG
+                   else "`python -c 'import __graft_entry__ as g; g.build()'`")
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with {how}")
         l = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in SIGNATURES.items():
             f = getattr(l, name)
@@ -545,3 +551,14 @@ def tpmlp_trace_read(max_bytes: int = 1 << 20):
         name, ms = line.rsplit(" ", 1)
         out.append((name, float(ms)))
     return out
+
+
+def tpmlp_build_flags() -> int:
+    """Bit 0: the loaded library is the debug build (device-side index checks)."""
+    return lib().tpmlp_build_flags()
+
+
+def tpmlp_selftest_bounds(index: int, stream=None) -> None:
+    """Debug build: a device-side check of `index` against a 32-element array
+    (test hook; a failed check shows in the next tpmlp_check_status)."""
+    _check(lib().tpmlp_selftest_bounds(index, _stream(stream)), "tpmlp_selftest_bounds")

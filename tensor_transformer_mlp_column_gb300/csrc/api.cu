@@ -419,7 +419,25 @@ int tpmlp_check_status(tpmlp_stream_t stream) {
   TRY_CUDA(read_and_clear_status(&v, stream));
   if (v == kSiteSmemAlign)
     return fail(TPMLP_ERR_CUDA, "a kernel found its dynamic shared memory misaligned and did no work");
+  if (v >= kSiteBoundsBase) {
+    static const char* const kNames[kChkCount] = {
+        "?", "GEMM tile outside the tile grid", "TMA coordinate not 16-byte aligned", "epilogue store outside the output",
+        "reduce index outside its slice", "attention tile outside the launch", "self-test index outside its array"};
+    const int c = v - kSiteBoundsBase;
+    return fail(TPMLP_ERR_BOUNDS, "a device-side check failed: %s (check %d)", c > 0 && c < kChkCount ? kNames[c] : "?",
+                c);
+  }
   if (v) return fail(TPMLP_ERR_TIMEOUT, "a device-side wait ran out of time (site %d)", v);
+  return TPMLP_OK;
+}
+
+int tpmlp_build_flags(void) { return kDebugBuild ? 1 : 0; }
+
+int tpmlp_selftest_bounds(int index, tpmlp_stream_t stream) {
+  if (!kDebugBuild) return fail(TPMLP_ERR_UNSUPPORTED, "the device-side checks exist in the debug build only");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  TRY_CUDA(launch_bounds_selftest(index, stream));
   return TPMLP_OK;
 }
 

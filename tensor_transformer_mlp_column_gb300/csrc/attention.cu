@@ -142,6 +142,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 
   const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
   const int shard = gh / p.local_heads, hl = gh % p.local_heads;
+  // Debug build: the CTA's query tile, rank and output must exist (CTA-uniform).
+  if (!TPMLP_DCHECK(qt * 128 < p.seq && shard < kMaxGroups && p.out[shard] != nullptr,
+                    threadIdx.x == 0 ? p.status : nullptr, kChkAttnTile))
+    return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3;      // TMEM lanes (= query rows) 32*quarter .. +31
   const int cgroup = warp >> 2;      // column group 0..3 of the score row
@@ -385,9 +389,14 @@ __device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const float (&v)[
 __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_addr(smem_raw) & 1023u) {  // the 128-byte-swizzled operands need 1024-byte alignment
-    if (threadIdx.x == 0) atomicExch(p.status, kSiteSmemAlign);
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteSmemAlign);
     return;  // CTA-uniform, before any barrier or TMEM allocation
   }
+  // Debug build: the CTA's query tile, rank and output must exist (CTA-uniform).
+  if (!TPMLP_DCHECK(int(blockIdx.x) * 128 < p.seq && int(blockIdx.y) / p.local_heads < kMaxGroups &&
+                        p.out[int(blockIdx.y) / p.local_heads] != nullptr,
+                    threadIdx.x == 0 ? p.status : nullptr, kChkAttnTile))
+    return;
   uint8_t* smem = smem_raw;
   uint8_t* sQ = smem;
   uint8_t* sRing = sQ + kQBytes;  // kStrmSlots slots of one K or V^T block

@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "internal.h"
+
 namespace tpmlp {
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -95,7 +97,7 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, con
       if (*g.abort_flag) return false;
       if (global_timer_ns() - t0 > g.limit_ns) {
         *g.abort_flag = 1;
-        atomicExch(g.status, site);
+        atomicCAS(g.status, 0, site);  // the first failure since the last check is the one reported
         return false;
       }
     }
@@ -111,6 +113,25 @@ __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity, uint6
   }
   return true;
 }
+
+// ------------------------------------------------------------------ debug checks
+//
+// In the library's debug build (TPMLP_DEBUG defined), TPMLP_DCHECK(cond,
+// status, check) tests an index or layout invariant on the device. A failed
+// check records kSiteBoundsBase + check in the status word (if no earlier
+// failure is recorded) and evaluates to false, and the caller skips the
+// access the check guards, so the kernel neither traps nor touches memory out
+// of range; tpmlp_check_status() then reports TPMLP_ERR_BOUNDS. In the normal
+// build the macro is the constant true and the checks compile away.
+#ifdef TPMLP_DEBUG
+__device__ __forceinline__ bool debug_fail(int* status, int check) {
+  if (status) atomicCAS(status, 0, kSiteBoundsBase + check);
+  return false;
+}
+#define TPMLP_DCHECK(cond, status, check) ((cond) ? true : ::tpmlp::debug_fail((status), (check)))
+#else
+#define TPMLP_DCHECK(cond, status, check) true
+#endif
 
 // ------------------------------------------------------------------ dependent launch
 //

@@ -77,7 +77,7 @@ __device__ __forceinline__ float residual1(const void* res, int res_kind, int64_
 template <int NMAX>
 __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __restrict__ Yp, int n, int64_t count,
                                                                const void* __restrict__ res, int res_kind,
-                                                               OutSlices out) {
+                                                               OutSlices out, int* status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t slice = count / gridDim.y;
@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
   const float4* P = reinterpret_cast<const float4*>(Yp) + base4;
   const int64_t shard_stride4 = count / 4;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    if (!TPMLP_DCHECK(base4 + i < count / 4 && Y != nullptr, status, kChkReduce)) break;
     float4 v[NMAX];
 #pragma unroll
     for (int s = 0; s < NMAX; ++s)
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kEwThreads) allreduce_kernel(const float* __re
 
 // Any n and any slice length: the same order, shards taken from memory one by one.
 __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_t count, const void* __restrict__ res,
-                                     int res_kind, OutSlices out) {
+                                     int res_kind, OutSlices out, int* status) {
   pdl_wait();
   pdl_launch_dependents();
   const int64_t slice = count / gridDim.y;
@@ -124,6 +125,7 @@ __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_
   float* __restrict__ Y = out.p[blockIdx.y];
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   for (int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; j < slice; j += stride) {
+    if (!TPMLP_DCHECK(base + j < count && Y != nullptr, status, kChkReduce)) break;
     float acc = Yp[base + j];
     for (int s = 1; s < n; ++s) acc += Yp[int64_t(s) * count + base + j];
     Y[j] = res_kind ? residual1(res, res_kind, base + j) + acc : acc;
@@ -135,9 +137,10 @@ __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_
 // out = the n input slices back to back (slice_bytes each), blockIdx.y = slice.
 // Each thread moves four words per pass, all four loads issued first.
 template <typename W>
-__global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__ out) {
+__global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__ out, int* status) {
   pdl_wait();
   pdl_launch_dependents();
+  if (!TPMLP_DCHECK(blockIdx.y < kMaxGroups && in.p[blockIdx.y] != nullptr, status, kChkReduce)) return;
   const W* __restrict__ src = static_cast<const W*>(in.p[blockIdx.y]);
   W* __restrict__ dst = out + int64_t(blockIdx.y) * words;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -243,14 +246,16 @@ cudaError_t launch_reduce_scatter(const float* Yp, int n, int64_t count, const O
   const unsigned gy = static_cast<unsigned>(nslices);
   if (slice % 4 != 0) {  // slices would not be 16-byte aligned
     dim3 g(static_cast<unsigned>((ew_grid(count, 1) + nslices - 1) / nslices), gy);
-    return launch_pdl(allreduce_any_kernel, g, dim3(kEwThreads), 0, s, Yp, n, count, res, res_kind, out);
+    return launch_pdl(allreduce_any_kernel, g, dim3(kEwThreads), 0, s, Yp, n, count, res, res_kind, out,
+                      device_status_word());
   }
   dim3 g(static_cast<unsigned>((ew_grid(count, 4) + nslices - 1) / nslices), gy);
   const dim3 b(kEwThreads);
-  if (n <= 4) return launch_pdl(allreduce_kernel<4>, g, b, 0, s, Yp, n, count, res, res_kind, out);
-  if (n <= 8) return launch_pdl(allreduce_kernel<8>, g, b, 0, s, Yp, n, count, res, res_kind, out);
-  if (n <= 16) return launch_pdl(allreduce_kernel<16>, g, b, 0, s, Yp, n, count, res, res_kind, out);
-  return launch_pdl(allreduce_any_kernel, g, b, 0, s, Yp, n, count, res, res_kind, out);
+  int* st = device_status_word();
+  if (n <= 4) return launch_pdl(allreduce_kernel<4>, g, b, 0, s, Yp, n, count, res, res_kind, out, st);
+  if (n <= 8) return launch_pdl(allreduce_kernel<8>, g, b, 0, s, Yp, n, count, res, res_kind, out, st);
+  if (n <= 16) return launch_pdl(allreduce_kernel<16>, g, b, 0, s, Yp, n, count, res, res_kind, out, st);
+  return launch_pdl(allreduce_any_kernel, g, b, 0, s, Yp, n, count, res, res_kind, out, st);
 }
 
 cudaError_t launch_allreduce(const float* Yp, int n, int64_t count, float* Y, cudaStream_t s, const void* res,
@@ -270,14 +275,17 @@ cudaError_t launch_all_gather(const InSlices& in, int nslices, int64_t slice_byt
   const dim3 b(kEwThreads);
   if (slice_bytes % 16 == 0) {
     const int64_t w = slice_bytes / 16;
-    return launch_pdl(gather_slices_kernel<uint4>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint4*>(out));
+    return launch_pdl(gather_slices_kernel<uint4>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint4*>(out),
+                      device_status_word());
   }
   if (slice_bytes % 4 == 0) {
     const int64_t w = slice_bytes / 4;
-    return launch_pdl(gather_slices_kernel<uint32_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint32_t*>(out));
+    return launch_pdl(gather_slices_kernel<uint32_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint32_t*>(out),
+                      device_status_word());
   }
   const int64_t w = slice_bytes / 2;
-  return launch_pdl(gather_slices_kernel<uint16_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint16_t*>(out));
+  return launch_pdl(gather_slices_kernel<uint16_t>, dim3(gx(w), gy), b, 0, s, in, w, static_cast<uint16_t*>(out),
+                      device_status_word());
 }
 
 cudaError_t launch_shard_copy(const void* A, const void* B, const ShardDesc* d_table, int64_t D, int64_t F,

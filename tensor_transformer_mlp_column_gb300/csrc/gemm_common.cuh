@@ -92,6 +92,16 @@ __device__ __forceinline__ void decode_tile(const KParams& p, int tile, int& g, 
   decode_tile(TileGrid{p.chain, p.shared, p.groups, p.m_blocks, p.n_blocks, p.group_m}, tile, g, mb, nb);
 }
 
+// Debug build: a decoded tile must lie inside the launch's tile grid. Every
+// role of a kernel checks the same tiles, so all of them skip a bad one alike.
+__device__ __forceinline__ bool tile_ok(const TileGrid& p, int* status, int g, int mb, int nb) {
+  return TPMLP_DCHECK(g >= 0 && g < p.groups && mb >= 0 && mb < p.m_blocks && nb >= 0 && nb < p.n_blocks, status,
+                      kChkTile);
+}
+__device__ __forceinline__ bool tile_ok(const KParams& p, int g, int mb, int nb) {
+  return tile_ok(TileGrid{p.chain, p.shared, p.groups, p.m_blocks, p.n_blocks, p.group_m}, p.status, g, mb, nb);
+}
+
 // 16-byte global stores; `stream` marks them evict-first so results that are
 // not read again soon do not push the operands out of L2.
 __device__ __forceinline__ void store16(void* dst, uint4 v, bool stream) {

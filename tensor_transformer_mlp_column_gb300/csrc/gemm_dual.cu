@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) tc_dual_bwd_kernel(const __gr
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
         int g, mb, nb;
         decode_tile(p.grid, tile, g, mb, nb);
+        if (!tile_ok(p.grid, p.status, g, mb, nb)) continue;
         const int m0 = mb * 256 + static_cast<int>(pos) * 128;
         const int n0 = nb * BN + static_cast<int>(pos) * 128;
         for (int prod = 0; !aborted && prod < 2; ++prod) {
@@ -192,6 +193,11 @@ __global__ void __launch_bounds__(kDualThreads, 1) tc_dual_bwd_kernel(const __gr
       uint32_t phase = 0;
       uint32_t acc_phase = 0;  // flips once per tile
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        if constexpr (kDebugBuild) {
+          int g, mb, nb;
+          decode_tile(p.grid, tile, g, mb, nb);
+          if (!tile_ok(p.grid, p.status, g, mb, nb)) continue;
+        }
         for (int prod = 0; !aborted && prod < 2; ++prod) {
           if (!wait_bounded(acc_empty + prod, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
             aborted = true;
@@ -245,6 +251,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) tc_dual_bwd_kernel(const __gr
     for (int tile = cluster; tile < p.tiles; tile += nclusters) {
       int g, mb, nb;
       decode_tile(p.grid, tile, g, mb, nb);
+      if (!tile_ok(p.grid, p.status, g, mb, nb)) continue;
       const int64_t m = int64_t(mb) * 256 + int64_t(pos) * 128 + quarter * 32 + lane;
       const bool row_ok = m < p.M;
       const int c0 = half * 128;  // first column of this warp's half of the tile

@@ -135,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
+        if (!tile_ok(p, g, mb, nb)) continue;
         const int m0 = mb * 256 + static_cast<int>(pos) * 128;
         const int n0 = nb * BN + static_cast<int>(pos) * 128;
         int gg = g, kk = 0;  // group and K block of the next load (chain mode walks the groups in order)
@@ -146,6 +147,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           const uint32_t full_lead = map_to_cta(smem_addr(full + stage), lead);
           const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;  // K blocks in this stage
           ++fill;
+          // Inner (x) coordinates of this stage's loads must be 16-byte aligned
+          // (K-major: kk * BK; MN-major: m0, n0; 3-D maps: chunk starts).
+          if (!TPMLP_DCHECK((kk * BK) % 8 == 0 && m0 % 64 == 0 && n0 % 64 == 0, p.status, kChkTmaX)) {
+            aborted = true;
+            break;
+          }
           if (fill != p.inject) {
             if (pos == 0) {
               mbar_arrive_expect_tx(full + stage, 2 * 2 * nsub * kSubBytes);  // both CTAs' A and B
@@ -217,6 +224,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
       int acc = 0;
       uint32_t acc_phase = 0;
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
+        if constexpr (kDebugBuild) {
+          int g, mb, nb;
+          decode_tile(p, tile, g, mb, nb);
+          if (!tile_ok(p, g, mb, nb)) continue;
+        }
         if (!wait_bounded(acc_empty + acc, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
           aborted = true;
           break;
@@ -268,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     for (int tile = cluster; tile < p.tiles; tile += nclusters) {
       int g, mb, nb;
       decode_tile(p, tile, g, mb, nb);
+      if (!tile_ok(p, g, mb, nb)) continue;
       bool ok = wait_bounded(acc_full + acc, acc_phase, guard, kSiteEpilogue);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) raise_abort_in_cluster();
@@ -302,6 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           // conflict-free for these row-per-lane writes), then one TMA store
           // writes it as whole 128-byte lines, clipped to M x N.
           if (n0 >= p.N || m_warp >= p.M) return;  // warp-uniform
+          if (!TPMLP_DCHECK(n0 % 32 == 0 && m_warp % 32 == 0 && n0 >= 0 && m_warp >= 0, p.status, kChkOutput)) return;
           uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
           if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
           __syncwarp();

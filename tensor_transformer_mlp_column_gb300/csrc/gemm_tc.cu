@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
         int g, mb, nb;
         decode_tile(p, tile, g, mb, nb);
+        if (!tile_ok(p, g, mb, nb)) continue;
         int gg = g, kk = 0;  // group and K block of the next load (chain mode walks the groups in order)
         for (int kb = 0; kb < kb_per_tile; kb += C::KSUB) {
           if (!wait_bounded(empty + stage, phase ^ 1u, guard, kSiteProducer)) {
@@ -118,6 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
           const int nsub = kb_per_tile - kb < C::KSUB ? kb_per_tile - kb : C::KSUB;  // K blocks in this stage
           ++fill;
+          // Inner (x) coordinates of this stage's loads must be 16-byte aligned.
+          if (!TPMLP_DCHECK((kk * BK) % 8 == 0 && (mb * BM) % 64 == 0 && (nb * BN) % 64 == 0, p.status, kChkTmaX)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
           if (fill != p.inject) {
             mbar_arrive_expect_tx(full + stage, nsub * (C::A_SUB + C::B_SUB));
             for (int u = 0; u < nsub; ++u) {
@@ -182,6 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.tiles; tile += gridDim.x) {
+        if constexpr (kDebugBuild) {
+          int g, mb, nb;
+          decode_tile(p, tile, g, mb, nb);
+          if (!tile_ok(p, g, mb, nb)) continue;
+        }
         if (!wait_bounded(acc_empty + acc, acc_phase ^ 1u, guard, kSiteMmaAcc)) {
           ok = false;
           break;
@@ -232,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x) {
       int g, mb, nb;
       decode_tile(p, tile, g, mb, nb);
+      if (!tile_ok(p, g, mb, nb)) continue;
       bool ok = wait_bounded(acc_full + acc, acc_phase, guard, kSiteEpilogue);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after_sync();
@@ -318,6 +331,23 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
   }
 }
 
+// The debug build's check in isolation: thread 0 writes element `index` of a
+// 32-element shared array only if the check passes. In the normal build the
+// kernel does nothing (and the C ABI never launches it).
+__global__ void bounds_selftest_kernel(int index, int* status) {
+#ifdef TPMLP_DEBUG
+  __shared__ int buf[32];
+  buf[threadIdx.x] = 0;
+  __syncthreads();
+  if (threadIdx.x == 0 && TPMLP_DCHECK(index >= 0 && index < 32, status, kChkSelftest)) buf[index] = 1;
+  __syncthreads();
+  if (buf[threadIdx.x] > 1) atomicAdd(status, 0);  // keeps the store from being removed
+#else
+  (void)index;
+  (void)status;
+#endif
+}
+
 int env_int(const char* name, int dflt) {
   const char* e = getenv(name);
   return e && *e ? atoi(e) : dflt;
@@ -360,6 +390,14 @@ bool tc_pairs_enabled() { return kernel_family() >= 1; }
 bool pdl_enabled() {
   static const bool v = env_int("TPMLP_PDL", 1) != 0;
   return v;
+}
+
+cudaError_t launch_bounds_selftest(int index, cudaStream_t s) {
+  if (!kDebugBuild) return cudaErrorNotSupported;
+  int* st = status_word();
+  if (!st) return cudaErrorInvalidSymbol;
+  bounds_selftest_kernel<<<1, 32, 0, s>>>(index, st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s) {

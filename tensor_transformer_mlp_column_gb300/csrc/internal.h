@@ -19,7 +19,27 @@ enum WaitSite : int {
   kSiteEpilogue = 4,
   kSiteSelftest = 5,
   kSiteSmemAlign = 6,  // a kernel found its dynamic shared memory misaligned and returned without work
+  kSiteBoundsBase = 16,  // debug build: a device-side check (DebugCheck) failed; the word holds 16 + the check
 };
+
+// Device-side checks of the debug build (TPMLP_DCHECK in device.cuh).
+enum DebugCheck : int {
+  kChkTile = 1,      // a GEMM tile index decoded outside the tile grid or the group count
+  kChkTmaX = 2,      // a TMA load's inner coordinate not on a 16-byte boundary
+  kChkOutput = 3,    // an epilogue store outside the output
+  kChkReduce = 4,    // a reduce / gather index outside its slice
+  kChkAttnTile = 5,  // an attention query tile, head or sequence outside the launch's bounds
+  kChkSelftest = 6,  // tpmlp_selftest_bounds: the requested index is outside its 32-element array
+  kChkCount = 7,
+};
+
+// Whether this library was built with the device-side checks (TPMLP_DEBUG).
+constexpr bool kDebugBuild =
+#ifdef TPMLP_DEBUG
+    true;
+#else
+    false;
+#endif
 
 // Output treatment of the tensor-core GEMM.
 enum TcEpilogue : int {
@@ -186,6 +206,9 @@ cudaError_t launch_transpose_u16(const void* in, int64_t rows, int64_t cols, int
 cudaError_t launch_bwd_act_f32(const float* P, float* H, float* dH, int64_t count, cudaStream_t s);
 
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+// Debug build only: one block writes element `index` of a 32-element shared
+// array behind a device-side check (kChkSelftest).
+cudaError_t launch_bounds_selftest(int index, cudaStream_t s);
 
 // Attention of head-split tensor parallelism (attention.cu), per rank i:
 // O_i = softmax(Q K^T / sqrt(d_h)) V for each of its local heads and each

@@ -201,3 +201,34 @@ def test_trace_read_without_tracing(tp):
     assert buf.value == b"" and count.value == 0
     assert tp.lib().tpmlp_trace_read(None, 16, None) == tp.TPMLP_ERR_ARG
     assert tp.lib().tpmlp_trace_read(None, 0, None) == tp.TPMLP_OK
+
+
+def test_normal_build_has_no_device_checks(tp):
+    """The normal build reports no debug flag and refuses the debug self test
+    before touching the device."""
+    if tp.DEBUG:
+        pytest.skip("TPMLP_DEBUG is set in this process")
+    assert tp.tpmlp_build_flags() == 0
+    assert tp.lib().tpmlp_selftest_bounds(40, None) == tp.TPMLP_ERR_UNSUPPORTED
+
+
+def test_debug_build_loads_under_its_switch():
+    """TPMLP_DEBUG=1 makes the binding load libtpmlp_debug.so, which exports
+    every declared symbol and reports the debug flag."""
+    import subprocess
+    import sys
+
+    from tensor_transformer_mlp_column_gb300 import build_lib
+
+    build_lib.build(debug=True, quiet=True)
+    code = (
+        "import re, tensor_transformer_mlp_column_gb300 as tp\n"
+        "assert tp.LIB_PATH.endswith('libtpmlp_debug.so'), tp.LIB_PATH\n"
+        "assert tp.tpmlp_build_flags() == 1\n"
+        "l = tp.lib()\n"
+        "assert all(hasattr(l, n) for n in tp.SIGNATURES)\n"
+        "print('ok')\n"
+    )
+    env = dict(os.environ, TPMLP_DEBUG="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
