@@ -521,6 +521,8 @@ def bench_backward(args, local_rank, peaks):
 
     dev = torch.device("cuda", local_rank)
     w = WORKLOADS["fwd_bwd"]
+    if args.T:  # a smaller profiling case of the same shapes
+        w = w.with_(T=args.T)
     inp = make_inputs(w, seed=0)
     X, dY = inp["X"].to(dev), inp["dY"].to(dev)
     sh = tp.tpmlp_shard(inp["A"].to(dev), inp["B"].to(dev), w.N)
