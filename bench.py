@@ -38,13 +38,13 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # by the tokens it processes; the capture commands are kept with the profiles).
 # Valid only for the CUDA sources they were measured on: TRAFFIC_SOURCE_HASH is
 # source_hash() of those sources, and a different hash reports null.
-TRAFFIC_SOURCE_HASH = "11c3a9176eab212d"
+TRAFFIC_SOURCE_HASH = "5b9a0d9b064a7b1f"
 TRAFFIC_BYTES = {
-    "gemm1_gelu(faithful)": 1_244_112_640,
-    "gemm2_partials": 2_994_391_808,
-    "allreduce": 2_400_751_104,
-    "gemm1_gelu(fused)": 1_242_578_944,
-    "gemm2_fused_sum": 2_762_342_400,
+    "gemm1_gelu(faithful)": 1_218_000_000,
+    "gemm2_partials": 3_050_000_000,
+    "allreduce": 2_390_000_000,
+    "gemm1_gelu(fused)": 1_224_000_000,
+    "gemm2_fused_sum": 2_638_000_000,
 }
 
 
