@@ -24,7 +24,7 @@ INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(REPO_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libtpmlp.so")
 DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libtpmlp_debug.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "gemm_dual.cu", "simt.cu", "elementwise.cu", "block.cu", "attention.cu", "attn_api.cu", "noalloc.cu", "trace.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "gemm_dual.cu", "gemm_fwd.cu", "simt.cu", "elementwise.cu", "block.cu", "attention.cu", "attn_api.cu", "noalloc.cu", "trace.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -98,9 +98,29 @@ int check_handle_device(const tpmlp_shards* sh) {
 
 // Workspace plan: byte offsets of every scratch buffer, 256-byte aligned.
 struct WsPlan {
-  size_t H = 0, Yp = 0, P = 0, dH = 0, dP = 0, dXp = 0;
+  size_t H = 0, Yp = 0, P = 0, dH = 0, dP = 0, dXp = 0, bands = 0;
   size_t total = 0;
 };
+
+// Whether the bf16 forward runs its two products in one persistent launch
+// (gemm_fwd.cu): when both have enough 256 x 256 tiles for CTA pairs (the
+// launcher's own rule) but together no more than 8 rounds of them over the
+// pairs, so that one product's partly filled last round and the other's
+// first can share the GPU. TPMLP_FWD_PERSIST=0 (read once per process) keeps
+// two launches for comparisons.
+bool use_persistent_forward(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode) {
+  static const bool on = [] {
+    const char* e = getenv("TPMLP_FWD_PERSIST");
+    return !(e && *e && atoi(e) == 0);
+  }();
+  if (!on || sh->dt != TPMLP_BF16 || !tc_pairs_enabled()) return false;
+  const int64_t mb = (T + 255) / 256;
+  const int64_t t1 = mb * ((sh->Fs + 255) / 256) * sh->n;
+  const int64_t t2 = mb * ((sh->D + 255) / 256) * (mode == TPMLP_FUSED ? 1 : sh->n);
+  const int64_t sms = num_sms();
+  const int pairs = fwd_persistent_clusters();
+  return pairs > 0 && t1 >= sms / 4 && t2 >= sms / 4 && t1 + t2 <= 8 * static_cast<int64_t>(pairs);
+}
 
 // Whether the bf16 recomputing backward runs its first step in the dual
 // kernel (gemm_dual.cu: P_i and dH_i in tensor memory, P never written): for
@@ -130,6 +150,7 @@ WsPlan plan_workspace(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode, int ba
   if (!backward) {
     w.H = take(n * t * Fs * es);
     if (mode == TPMLP_FAITHFUL) w.Yp = take(n * t * D * 4);
+    if (use_persistent_forward(T, sh, mode)) w.bands = take(((t + 255) / 256) * sizeof(int));
   } else {
     // backward == 2: the caller's saved P; the dual kernel keeps P in tensor memory.
     if (backward == 1 && !use_dual_backward(T, sh)) w.P = take(n * t * Fs * 4);
@@ -365,9 +386,41 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
     return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
   if ((rc = check_handle_device(sh))) return rc;
   void* H = at<char>(ws, w.H);
+  float* Yp = mode == TPMLP_FAITHFUL ? at<float>(ws, w.Yp) : nullptr;
+  if (!P && use_persistent_forward(T, sh, mode)) {
+    // Both products in one launch; the second product's tiles start on bands
+    // of H as they are completed.
+    const int64_t D = sh->D, Fs = sh->Fs;
+    const int n = sh->n;
+    CUtensorMap mx;
+    std::vector<CUtensorMap> mh(n), mo(n);
+    if ((rc = map_or_fail(&mx, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
+    FwdPersistent f{};
+    f.map_x = &mx;
+    for (int i = 0; i < n; ++i) {
+      f.h[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
+      if ((rc = map_or_fail(&mh[i], f.h[i], T, Fs, Fs, tc_box_rows_a(), "H_i"))) return rc;
+      f.map_at[i] = &sh->map_At[i];
+      f.map_h[i] = &mh[i];
+      f.map_bt[i] = &sh->map_Bt[i];
+      void* out = Yp ? static_cast<void*>(Yp + static_cast<size_t>(i) * T * D) : Y;
+      if ((i == 0 || Yp) && (rc = out_map(&mo[i], out, T, D, D, Yp ? "Y_i" : "Y"))) return rc;
+      f.map_out[i] = &mo[Yp ? i : 0];
+    }
+    f.M = static_cast<int>(T);
+    f.N1 = static_cast<int>(Fs);
+    f.N2 = static_cast<int>(D);
+    f.K1 = static_cast<int>(D);
+    f.groups = n;
+    f.chain = Yp ? 0 : 1;
+    f.band_done = at<int>(ws, w.bands);
+    TRACED("forward_persistent", stream, launch_fwd_persistent(f, wait_limit_ns(), stream));
+    if (!Yp) return TPMLP_OK;
+    TRACED("allreduce", stream, launch_allreduce(Yp, n, T * D, static_cast<float*>(Y), stream));
+    return TPMLP_OK;
+  }
   if ((rc = run_hidden(X, T, sh, H, stream, 0, 0, P))) return rc;
   if (mode == TPMLP_FUSED) return run_second(H, T, sh, Y, 1, stream);
-  float* Yp = at<float>(ws, w.Yp);
   if ((rc = run_second(H, T, sh, Yp, 0, stream))) return rc;
   TRACED("allreduce", stream, launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
   return TPMLP_OK;

@@ -19,6 +19,7 @@ enum WaitSite : int {
   kSiteEpilogue = 4,
   kSiteSelftest = 5,
   kSiteSmemAlign = 6,  // a kernel found its dynamic shared memory misaligned and returned without work
+  kSiteBand = 7,       // the persistent forward: a band of H was not complete in time
   kSiteBoundsBase = 16,  // debug build: a device-side check (DebugCheck) failed; the word holds 16 + the check
 };
 
@@ -111,6 +112,29 @@ struct DualBwd {
   int load_hint;  // L2 policy kinds of the M x K loads (bits 0-1) and the N x K loads (2-3)
 };
 cudaError_t launch_dual_bwd(const DualBwd& d, uint64_t wait_ns, cudaStream_t s);
+
+// The bf16 forward's two products in one persistent launch of CTA pairs
+// (gemm_fwd.cu): h[i] = GeLU(X A_i), then Y = sum_i H_i B_i (chain) or the
+// partials Y_i = H_i B_i, second-product tiles starting as soon as their band
+// of 256 rows of every H_i is written. Maps: X [M][K1], A_i^T [N1][K1], H_i
+// [M][N1] and B_i^T [N2][N1], all K-major with 128-row boxes; map_out the fp32
+// output(s) in 32 x 32 boxes (one with chain, else one per shard). band_done:
+// ceil(M / 256) ints of scratch, zeroed by the launch itself.
+struct FwdPersistent {
+  const CUtensorMap* map_x;
+  const CUtensorMap* map_at[kMaxGroups];
+  const CUtensorMap* map_h[kMaxGroups];
+  const CUtensorMap* map_bt[kMaxGroups];
+  const CUtensorMap* map_out[kMaxGroups];
+  void* h[kMaxGroups];
+  int M, N1, N2, K1;
+  int groups, chain;
+  int* band_done;
+};
+cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cudaStream_t s);
+// CTA pairs of the persistent forward that fit the device at once (0 if it
+// cannot be launched).
+int fwd_persistent_clusters();
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
 // `pitch_elems` (cols contiguous), boxes of 64 columns x box_rows rows and

@@ -26,8 +26,9 @@ d = {k: v.cuda() for k, v in make_inputs(w, seed=91).items()}
 sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
 torch.cuda.synchronize()
 tp.tpmlp_trace_read()  # forget set-up
+# (the faithful forward of this shape runs both products in one persistent launch)
 expect = {
-    ("forward", "faithful"): ["gemm1_gelu", "gemm2_partials", "allreduce"],
+    ("forward", "faithful"): ["forward_persistent", "allreduce"],
     ("forward", "fused"): ["gemm1_gelu", "gemm2_fused_sum"],
     ("backward", "faithful"): ["bwd_dual_P_dH", "bwd_dB", "bwd_dA", "bwd_dX_partials", "bwd_dx_allreduce"],
     ("backward", "fused"): ["bwd_dual_P_dH", "bwd_dB", "bwd_dA", "bwd_dX_fused_sum"],

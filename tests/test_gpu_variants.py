@@ -212,3 +212,68 @@ def test_narrow_single_cta_tiles_against_oracle_and_wide(tmp_path):
     for k in results["1"]:
         a, b = results["1"][k].double(), results["0"][k].double()
         assert (a - b).abs().max() <= 1e-5 * b.abs().max(), f"{k}: narrow and wide tiles differ"
+
+
+# The forward's two products in one persistent launch (the default for
+# products small enough) against two launches (TPMLP_FWD_PERSIST=0, read once
+# per process, so each setting runs in a child process): every tile sums the
+# same K blocks in the same order either way, so the outputs agree bit for
+# bit, and both match the oracle. Shapes: GPT-2-small and seq 512 (the
+# persistent launch in both modes), a ragged token count (last band partial)
+# and 8 shards.
+PERSIST_CHILD = r"""
+import sys, numpy as np, torch
+import oracle
+import tensor_transformer_mlp_column_gb300 as tp
+from tpmlp_inputs import Workload, make_inputs
+
+def check(got, ref, what):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    fro = np.linalg.norm(got - ref) / np.linalg.norm(ref); mx = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
+    assert fro <= 5e-3 and mx <= 2e-2, (what, fro, mx)
+
+f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+torch.cuda.set_device(0)
+out = {}
+for name, T, D, F, N in (("gpt2", 4096, 768, 3072, 4), ("seq512", 4096, 1024, 4096, 4),
+                         ("ragged", 3000, 768, 3072, 4), ("eight", 2048, 1024, 8192, 8)):
+    w = Workload(name, T, D, F, N, "bf16", 1.0, 0.02, 0.02)
+    inp = make_inputs(w, seed=93)
+    shards = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), N)
+    rows = list(range(0, T, 23))
+    idx = torch.tensor(rows, device="cuda")
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], N)
+    Y_ref = oracle.tp_mlp_rows(f64(inp["X"]), shards, rows)
+    for mode in ("faithful", "fused"):
+        Y = tp.tpmlp_forward(d["X"], sh, mode)
+        check(f64(Y.index_select(0, idx)), Y_ref, name + " " + mode)
+        out[name + "_" + mode] = Y
+        out[name + "_" + mode + "_again"] = tp.tpmlp_forward(d["X"], sh, mode)
+torch.cuda.synchronize()
+tp.tpmlp_check_status()
+torch.save({k: v.cpu() for k, v in out.items()}, sys.argv[1])
+print("ok")
+"""
+
+
+def test_persistent_forward_matches_two_launches(tmp_path):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    results = {}
+    for flag in ("1", "0"):
+        path = str(tmp_path / f"persist{flag}.pt")
+        env = dict(os.environ, TPMLP_FWD_PERSIST=flag)
+        r = subprocess.run([sys.executable, "-c", PERSIST_CHILD, path], env=env, cwd=ROOT, capture_output=True,
+                           text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), flag + r.stdout[-2000:] + r.stderr[-4000:]
+        results[flag] = torch.load(path)
+    for k in results["1"]:
+        assert torch.equal(results["1"][k], results["0"][k]), f"{k}: one launch and two launches differ"
+        if k.endswith("_again"):
+            assert torch.equal(results["1"][k], results["1"][k[:-6]]), f"{k}: not reproducible"
