@@ -215,6 +215,31 @@ int tpmlp_backward(const void* X, const void* dY, int64_t T, const tpmlp_shards*
 int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* shards, void* H, int fill,
                                       int limit_ms, tpmlp_stream_t stream);
 
+/* Test hook for the persistent forward's band waits (the one-launch form that
+ * tpmlp_forward takes for small bf16 products): runs it with every band of H
+ * needing one arrival more than its first-product tiles make, so the
+ * producer of every second-product tile waits for a band that is never
+ * complete and gives up after limit_ms (1..10000); the kernel drains its
+ * copies and products, frees its tensor memory and records TPMLP_ERR_TIMEOUT
+ * for the next tpmlp_check_status(). Y (and, FAITHFUL, the workspace's
+ * partials) are left partly written; no reduce runs. Arguments as
+ * tpmlp_forward; TPMLP_ERR_UNSUPPORTED if this forward would not run as one
+ * launch. */
+int tpmlp_selftest_forward_band_timeout(const void* X, int64_t T, const tpmlp_shards* shards, void* Y, tpmlp_mode mode,
+                                        void* workspace, size_t ws_bytes, int limit_ms, tpmlp_stream_t stream);
+
+/* Test hook for the recomputing backward's first step (the dual-accumulator
+ * kernel, used for bf16 products with enough CTA-pair tiles): runs that
+ * kernel alone with stage fill number `fill` (1-based, counted by each CTA's
+ * producer) never issued and a wait limit of limit_ms (1..10000). Every CTA
+ * pair that reaches the fill gives up, drains, frees its tensor memory and
+ * records TPMLP_ERR_TIMEOUT. Workspace as tpmlp_backward in FUSED mode (its
+ * H and dP parts are left partly written). TPMLP_ERR_UNSUPPORTED if this
+ * backward would not use the dual kernel. */
+int tpmlp_selftest_backward_withheld_fill(const void* X, const void* dY, int64_t T, const tpmlp_shards* shards,
+                                          int fill, int limit_ms, void* workspace, size_t ws_bytes,
+                                          tpmlp_stream_t stream);
+
 /* tpmlp_forward without any allocation: the same Y, but the scratch lives in
  * a fixed 64 MiB array of device memory that the library reserves on every
  * GPU where its device code is loaded and keeps until the process exits. (The

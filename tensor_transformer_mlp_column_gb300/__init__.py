@@ -86,6 +86,8 @@ SIGNATURES = {
     "tpmlp_trace_read": (_I, [ctypes.c_char_p, _SZ, ctypes.POINTER(_I)]),
     "tpmlp_trace_enabled": (_I, []),
     "tpmlp_build_flags": (_I, []),
+    "tpmlp_selftest_forward_band_timeout": (_I, [_P, _I64, _P, _P, _I, _P, _SZ, _I, _P]),
+    "tpmlp_selftest_backward_withheld_fill": (_I, [_P, _P, _I64, _P, _I, _I, _P, _SZ, _P]),
     "tpmlp_selftest_bounds": (_I, [_I, _P]),
 }
 
@@ -562,3 +564,22 @@ def tpmlp_selftest_bounds(index: int, stream=None) -> None:
     """Debug build: a device-side check of `index` against a 32-element array
     (test hook; a failed check shows in the next tpmlp_check_status)."""
     _check(lib().tpmlp_selftest_bounds(index, _stream(stream)), "tpmlp_selftest_bounds")
+
+
+def tpmlp_selftest_forward_band_timeout(X: torch.Tensor, shards: Shards, Y: torch.Tensor, mode, limit_ms: int,
+                                        workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Runs the one-launch forward with bands of H that never complete (test hook)."""
+    ws = _workspace(tpmlp_workspace_bytes(X.shape[0], shards, mode, 0), workspace)
+    _check(lib().tpmlp_selftest_forward_band_timeout(_dev(X, "X"), X.shape[0], shards.handle, _dev(Y, "Y"),
+                                                     _mode(mode), ws.data_ptr(), ws.numel() * ws.element_size(),
+                                                     limit_ms, _stream(stream)), "tpmlp_selftest_forward_band_timeout")
+
+
+def tpmlp_selftest_backward_withheld_fill(X: torch.Tensor, dY: torch.Tensor, shards: Shards, fill: int,
+                                          limit_ms: int, workspace: Optional[torch.Tensor] = None,
+                                          stream=None) -> None:
+    """Runs the backward's dual-accumulator kernel with stage fill `fill` withheld (test hook)."""
+    ws = _workspace(tpmlp_workspace_bytes(X.shape[0], shards, "fused", 1), workspace)
+    _check(lib().tpmlp_selftest_backward_withheld_fill(_dev(X, "X"), _dev(dY, "dY"), X.shape[0], shards.handle,
+                                                       fill, limit_ms, ws.data_ptr(), ws.numel() * ws.element_size(),
+                                                       _stream(stream)), "tpmlp_selftest_backward_withheld_fill")

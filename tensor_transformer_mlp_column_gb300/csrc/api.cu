@@ -372,6 +372,42 @@ int check_eps(float eps) {
   return TPMLP_OK;
 }
 
+// The bf16 forward's two products in one persistent launch: H_i into H, then
+// Y (Yp == NULL: the shard-ordered sum) or the partials Yp. band_extra and
+// wait_ns are the test hooks of tpmlp_selftest_forward_band_timeout (0 = off /
+// the default limit).
+int run_forward_persistent(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, float* Yp, void* H,
+                           int* bands, cudaStream_t stream, int band_extra = 0, uint64_t wait_ns = 0) {
+  const int64_t D = sh->D, Fs = sh->Fs;
+  const int n = sh->n;
+  int rc;
+  CUtensorMap mx;
+  std::vector<CUtensorMap> mh(n), mo(n);
+  if ((rc = map_or_fail(&mx, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
+  FwdPersistent f{};
+  f.map_x = &mx;
+  for (int i = 0; i < n; ++i) {
+    f.h[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
+    if ((rc = map_or_fail(&mh[i], f.h[i], T, Fs, Fs, tc_box_rows_a(), "H_i"))) return rc;
+    f.map_at[i] = &sh->map_At[i];
+    f.map_h[i] = &mh[i];
+    f.map_bt[i] = &sh->map_Bt[i];
+    void* out = Yp ? static_cast<void*>(Yp + static_cast<size_t>(i) * T * D) : Y;
+    if ((i == 0 || Yp) && (rc = out_map(&mo[i], out, T, D, D, Yp ? "Y_i" : "Y"))) return rc;
+    f.map_out[i] = &mo[Yp ? i : 0];
+  }
+  f.M = static_cast<int>(T);
+  f.N1 = static_cast<int>(Fs);
+  f.N2 = static_cast<int>(D);
+  f.K1 = static_cast<int>(D);
+  f.groups = n;
+  f.chain = Yp ? 0 : 1;
+  f.band_done = bands;
+  f.band_extra = band_extra;
+  TRACED("forward_persistent", stream, launch_fwd_persistent(f, wait_ns ? wait_ns : wait_limit_ns(), stream));
+  return TPMLP_OK;
+}
+
 // tpmlp_forward, and with P also tpmlp_forward_save.
 int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void* P, tpmlp_mode mode, void* ws,
                  size_t ws_bytes, cudaStream_t stream) {
@@ -390,33 +426,9 @@ int forward_impl(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, void
   if (!P && use_persistent_forward(T, sh, mode)) {
     // Both products in one launch; the second product's tiles start on bands
     // of H as they are completed.
-    const int64_t D = sh->D, Fs = sh->Fs;
-    const int n = sh->n;
-    CUtensorMap mx;
-    std::vector<CUtensorMap> mh(n), mo(n);
-    if ((rc = map_or_fail(&mx, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
-    FwdPersistent f{};
-    f.map_x = &mx;
-    for (int i = 0; i < n; ++i) {
-      f.h[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
-      if ((rc = map_or_fail(&mh[i], f.h[i], T, Fs, Fs, tc_box_rows_a(), "H_i"))) return rc;
-      f.map_at[i] = &sh->map_At[i];
-      f.map_h[i] = &mh[i];
-      f.map_bt[i] = &sh->map_Bt[i];
-      void* out = Yp ? static_cast<void*>(Yp + static_cast<size_t>(i) * T * D) : Y;
-      if ((i == 0 || Yp) && (rc = out_map(&mo[i], out, T, D, D, Yp ? "Y_i" : "Y"))) return rc;
-      f.map_out[i] = &mo[Yp ? i : 0];
-    }
-    f.M = static_cast<int>(T);
-    f.N1 = static_cast<int>(Fs);
-    f.N2 = static_cast<int>(D);
-    f.K1 = static_cast<int>(D);
-    f.groups = n;
-    f.chain = Yp ? 0 : 1;
-    f.band_done = at<int>(ws, w.bands);
-    TRACED("forward_persistent", stream, launch_fwd_persistent(f, wait_limit_ns(), stream));
+    if ((rc = run_forward_persistent(X, T, sh, Y, Yp, H, at<int>(ws, w.bands), stream))) return rc;
     if (!Yp) return TPMLP_OK;
-    TRACED("allreduce", stream, launch_allreduce(Yp, n, T * D, static_cast<float*>(Y), stream));
+    TRACED("allreduce", stream, launch_allreduce(Yp, sh->n, T * sh->D, static_cast<float*>(Y), stream));
     return TPMLP_OK;
   }
   if ((rc = run_hidden(X, T, sh, H, stream, 0, 0, P))) return rc;
@@ -708,6 +720,35 @@ int tpmlp_backward_saved(const void* X, const void* dY, const void* P, int64_t T
 // the input gradient is finished by the tail kernel instead of the reduce:
 // from the partials in FAITHFUL mode, from dX (then a scratch buffer) in
 // FUSED mode.
+// The recomputing backward's first step in the dual kernel: H_i = GeLU(X A_i)
+// and dP_i = dY B_i^T * GeLU'(X A_i) into H and dP (bf16 [n][T][Fs]). inject
+// and wait_ns are the test hooks of tpmlp_selftest_backward_withheld_fill
+// (0 = off / the default limit).
+static int run_dual(const CUtensorMap* mX, const CUtensorMap* mdY, int64_t T, const tpmlp_shards* sh, uint16_t* H,
+                    uint16_t* dP, cudaStream_t s, int inject = 0, uint64_t wait_ns = 0) {
+  const int n = sh->n;
+  const int64_t Fs = sh->Fs;
+  DualBwd d{};
+  d.map_x = mX;
+  d.map_dy = mdY;
+  for (int i = 0; i < n; ++i) {
+    d.map_at[i] = &sh->map_At[i];
+    d.map_b[i] = &sh->map_B[i];
+    d.h[i] = H + static_cast<size_t>(i) * T * Fs;
+    d.dp[i] = dP + static_cast<size_t>(i) * T * Fs;
+  }
+  d.ldo = Fs;
+  d.M = static_cast<int>(T);
+  d.N = static_cast<int>(Fs);
+  d.K = static_cast<int>(sh->D);
+  d.groups = n;
+  d.group_m = 16;  // X and dY feed every shard
+  d.load_hint = 1 | (1 << 2);
+  d.inject = inject;
+  TRACED("bwd_dual_P_dH", s, launch_dual_bwd(d, wait_ns ? wait_ns : wait_limit_ns(), s));
+  return TPMLP_OK;
+}
+
 static int backward_impl(const void* X, const void* dY, const void* P_saved, int64_t T, const tpmlp_shards* sh,
                          void* dX, void* const* dA, void* const* dB, tpmlp_mode mode, void* ws, size_t ws_bytes,
                          cudaStream_t stream, const LnTail* tail, const OutSlices* dx_slices) {
@@ -799,23 +840,7 @@ static int backward_impl(const void* X, const void* dY, const void* P_saved, int
   if (!P_saved && use_dual_backward(T, sh)) {
     // P_i = X A_i and dH_i = dY B_i^T in tensor memory; H_i and dP_i = dH_i *
     // GeLU'(P_i) from the epilogue.
-    DualBwd d{};
-    d.map_x = &mX;
-    d.map_dy = &mdY;
-    for (int i = 0; i < n; ++i) {
-      d.map_at[i] = &sh->map_At[i];
-      d.map_b[i] = &sh->map_B[i];
-      d.h[i] = H + static_cast<size_t>(i) * T * Fs;
-      d.dp[i] = dP + static_cast<size_t>(i) * T * Fs;
-    }
-    d.ldo = Fs;
-    d.M = static_cast<int>(T);
-    d.N = static_cast<int>(Fs);
-    d.K = static_cast<int>(D);
-    d.groups = n;
-    d.group_m = 16;  // X and dY feed every shard
-    d.load_hint = 1 | (1 << 2);
-    TRACED("bwd_dual_P_dH", s, launch_dual_bwd(d, wl, s));
+    if ((rc = run_dual(&mX, &mdY, T, sh, H, dP, s))) return rc;
   } else {
     TcGemm g{};
     g.groups = n;
@@ -1089,6 +1114,46 @@ int tpmlp_backward_sp(const void* const* X_slices, const void* const* dY_slices,
   // the product writes the slices (FUSED); slice 0 stands in for the pointer.
   return backward_impl(at<char>(ws, p.x), at<char>(ws, p.dy), nullptr, T, sh, dX_slices[0], dA, dB, mode,
                        at<char>(ws, p.inner), p.w.total, stream, nullptr, &out);
+}
+
+int tpmlp_selftest_forward_band_timeout(const void* X, int64_t T, const tpmlp_shards* sh, void* Y, tpmlp_mode mode,
+                                        void* ws, size_t ws_bytes, int limit_ms, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (mode != TPMLP_FAITHFUL && mode != TPMLP_FUSED) return fail(TPMLP_ERR_ARG, "unknown mode %d", int(mode));
+  if (!X || !Y || !ws) return fail(TPMLP_ERR_ARG, "X, Y and workspace must not be NULL");
+  if (!aligned16(X) || !aligned16(Y) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "X, Y and workspace must be 16-byte aligned");
+  if (limit_ms < 1 || limit_ms > 10000) return fail(TPMLP_ERR_ARG, "limit_ms = %d outside 1..10000", limit_ms);
+  if ((rc = check_handle_device(sh))) return rc;
+  if (!use_persistent_forward(T, sh, mode))
+    return fail(TPMLP_ERR_UNSUPPORTED, "this forward does not run as one persistent launch");
+  const WsPlan w = plan_workspace(T, sh, mode, 0);
+  if (ws_bytes < w.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  float* Yp = mode == TPMLP_FAITHFUL ? at<float>(ws, w.Yp) : nullptr;
+  return run_forward_persistent(X, T, sh, Y, Yp, at<char>(ws, w.H), at<int>(ws, w.bands),
+                                static_cast<cudaStream_t>(stream), 1, static_cast<uint64_t>(limit_ms) * 1000000ull);
+}
+
+int tpmlp_selftest_backward_withheld_fill(const void* X, const void* dY, int64_t T, const tpmlp_shards* sh, int fill,
+                                          int limit_ms, void* ws, size_t ws_bytes, tpmlp_stream_t stream) {
+  int rc = check_common(sh, T);
+  if (rc) return rc;
+  if (!X || !dY || !ws) return fail(TPMLP_ERR_ARG, "X, dY and workspace must not be NULL");
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(ws))
+    return fail(TPMLP_ERR_ALIGN, "X, dY and workspace must be 16-byte aligned");
+  if (fill < 1) return fail(TPMLP_ERR_ARG, "fill = %d must be >= 1", fill);
+  if (limit_ms < 1 || limit_ms > 10000) return fail(TPMLP_ERR_ARG, "limit_ms = %d outside 1..10000", limit_ms);
+  if ((rc = check_handle_device(sh))) return rc;
+  if (!use_dual_backward(T, sh)) return fail(TPMLP_ERR_UNSUPPORTED, "this backward does not use the dual kernel");
+  const WsPlan w = plan_workspace(T, sh, TPMLP_FUSED, 1);
+  if (ws_bytes < w.total) return fail(TPMLP_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, w.total);
+  const int64_t D = sh->D;
+  CUtensorMap mX, mdY;
+  if ((rc = map_or_fail(&mX, X, T, D, D, tc_box_rows_a(), "X"))) return rc;
+  if ((rc = map_or_fail(&mdY, dY, T, D, D, tc_box_rows_a(), "dY"))) return rc;
+  return run_dual(&mX, &mdY, T, sh, at<uint16_t>(ws, w.H), at<uint16_t>(ws, w.dP), static_cast<cudaStream_t>(stream),
+                  fill, static_cast<uint64_t>(limit_ms) * 1000000ull);
 }
 
 int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shards* sh, void* H, int fill,

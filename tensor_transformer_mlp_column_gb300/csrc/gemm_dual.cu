@@ -67,6 +67,7 @@ struct DualParams {
   uint64_t wait_ns;
   int* status;
   int load_hint;
+  int inject;  // test hook: > 0 withholds that stage fill (1-based) in every CTA
 };
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(kDualThreads, 1) tc_dual_bwd_kernel(const __gr
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed = 0, parity_bits = 0;
+      int fill = 0;
       const uint64_t pol_a = l2_policy(p.load_hint & 3), pol_b = l2_policy((p.load_hint >> 2) & 3);
       for (int tile = cluster; !aborted && tile < p.tiles; tile += nclusters) {
         int g, mb, nb;
@@ -156,14 +158,17 @@ __global__ void __launch_bounds__(kDualThreads, 1) tc_dual_bwd_kernel(const __gr
             }
             const uint32_t full_lead = map_to_cta(smem_addr(full + stage), lead);
             const int nsub = p.k_blocks - kb < kDualKsub ? p.k_blocks - kb : kDualKsub;
-            if (pos == 0) {
-              mbar_arrive_expect_tx(full + stage, 2 * 2 * nsub * kDualSub);  // both CTAs' two operands
-              armed |= 1u << stage;
-              parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
-            }
-            for (int u = 0; u < nsub; ++u) {
-              tma_load_2d_pair_hint(sA + stage * kDualA + u * kDualSub, ma, (kb + u) * BK, m0, full_lead, pol_a);
-              tma_load_2d_pair_hint(sB + stage * kDualA + u * kDualSub, mbmap, (kb + u) * BK, n0, full_lead, pol_b);
+            if (++fill != p.inject) {
+              if (pos == 0) {
+                mbar_arrive_expect_tx(full + stage, 2 * 2 * nsub * kDualSub);  // both CTAs' two operands
+                armed |= 1u << stage;
+                parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+              }
+              for (int u = 0; u < nsub; ++u) {
+                tma_load_2d_pair_hint(sA + stage * kDualA + u * kDualSub, ma, (kb + u) * BK, m0, full_lead, pol_a);
+                tma_load_2d_pair_hint(sB + stage * kDualA + u * kDualSub, mbmap, (kb + u) * BK, n0, full_lead,
+                                      pol_b);
+              }
             }
             if (++stage == kDualStages) {
               stage = 0;
@@ -356,6 +361,7 @@ cudaError_t launch_dual_bwd(const DualBwd& d, uint64_t wait_ns, cudaStream_t s) 
   p.wait_ns = wait_ns;
   p.status = device_status_word();
   p.load_hint = d.load_hint;
+  p.inject = d.inject;
   if (!p.status) return cudaErrorInvalidSymbol;
   if (p.tiles == 0) return cudaSuccess;
 

@@ -482,7 +482,7 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
   p.k_blocks2 = (f.N1 + BK - 1) / BK;
   p.tiles1 = p.m_blocks * p.n_blocks1 * f.groups;
   p.tiles = p.tiles1 + p.m_blocks * p.n_blocks2 * (f.chain ? 1 : f.groups);
-  p.band_arrivals = p.n_blocks1 * f.groups * 8;  // 4 epilogue warps in each CTA of the pair
+  p.band_arrivals = p.n_blocks1 * f.groups * 8 + f.band_extra;  // 4 epilogue warps in each CTA of the pair
   p.band_done = f.band_done;
   p.wait_ns = wait_ns;
   p.status = device_status_word();

@@ -110,6 +110,7 @@ struct DualBwd {
   int groups;
   int group_m;    // tile order (decode_tile), X and dY shared by every group
   int load_hint;  // L2 policy kinds of the M x K loads (bits 0-1) and the N x K loads (2-3)
+  int inject;     // test hook: > 0 withholds that stage fill (1-based) in every CTA
 };
 cudaError_t launch_dual_bwd(const DualBwd& d, uint64_t wait_ns, cudaStream_t s);
 
@@ -130,6 +131,7 @@ struct FwdPersistent {
   int M, N1, N2, K1;
   int groups, chain;
   int* band_done;
+  int band_extra;  // test hook: arrivals a band needs beyond its epilogue warps' (> 0: never complete)
 };
 cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cudaStream_t s);
 // CTA pairs of the persistent forward that fit the device at once (0 if it
