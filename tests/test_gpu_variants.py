@@ -219,8 +219,9 @@ def test_narrow_single_cta_tiles_against_oracle_and_wide(tmp_path):
 # per process, so each setting runs in a child process): every tile sums the
 # same K blocks in the same order either way, so the outputs agree bit for
 # bit, and both match the oracle. Shapes: GPT-2-small and seq 512 (the
-# persistent launch in both modes), a ragged token count (last band partial)
-# and 8 shards.
+# persistent launch in both modes), a ragged token count (last band partial),
+# 8 shards, ragged T, D and F/n together (T=2500, D=1288, F/n=1000) and 16
+# shards (faithful only: its shard-ordered sum has too few pair tiles).
 PERSIST_CHILD = r"""
 import sys, numpy as np, torch
 import oracle
@@ -236,7 +237,8 @@ f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
 torch.cuda.set_device(0)
 out = {}
 for name, T, D, F, N in (("gpt2", 4096, 768, 3072, 4), ("seq512", 4096, 1024, 4096, 4),
-                         ("ragged", 3000, 768, 3072, 4), ("eight", 2048, 1024, 8192, 8)):
+                         ("ragged", 3000, 768, 3072, 4), ("eight", 2048, 1024, 8192, 8),
+                         ("ragged_all", 2500, 1288, 4000, 4), ("sixteen", 1024, 1024, 4096, 16)):
     w = Workload(name, T, D, F, N, "bf16", 1.0, 0.02, 0.02)
     inp = make_inputs(w, seed=93)
     shards = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), N)
@@ -277,3 +279,61 @@ def test_persistent_forward_matches_two_launches(tmp_path):
         assert torch.equal(results["1"][k], results["0"][k]), f"{k}: one launch and two launches differ"
         if k.endswith("_again"):
             assert torch.equal(results["1"][k], results["1"][k[:-6]]), f"{k}: not reproducible"
+
+
+# The backward's first step in the dual-accumulator kernel (the default for
+# products with CTA-pair tiles) against two products (TPMLP_BWD_DUAL=0, read
+# once per process): both match the oracle on every gradient, on ragged T, D
+# and F/n and on 16 shards. (They are not bit-identical: the dual kernel keeps
+# GeLU'(P) in fp16 between its two phases.)
+DUAL_CHILD = r"""
+import sys, numpy as np, torch
+import oracle
+import tensor_transformer_mlp_column_gb300 as tp
+from tpmlp_inputs import Workload, make_inputs
+
+def check(got, ref, what):
+    got = np.asarray(got, np.float64); ref = np.asarray(ref, np.float64)
+    fro = np.linalg.norm(got - ref) / np.linalg.norm(ref); mx = np.max(np.abs(got - ref)) / np.max(np.abs(ref))
+    assert fro <= 5e-3 and mx <= 2e-2, (what, fro, mx)
+
+f64 = lambda t: t.detach().to("cpu", torch.float64).numpy()
+torch.cuda.set_device(0)
+for name, T, D, F, N in (("ragged_all", 2500, 1288, 4000, 4), ("sixteen", 1024, 1024, 4096, 16),
+                         ("tall", 6000, 512, 2048, 2)):
+    w = Workload(name, T, D, F, N, "bf16", 1.0, 0.03, 0.03, 1.0, True)
+    inp = make_inputs(w, seed=95)
+    X, A, B, dY = (f64(inp[k]) for k in ("X", "A", "B", "dY"))
+    shards = oracle.shard_mlp(A, B, N)
+    rows = list(range(0, T, 29))
+    cols = list(range(0, w.Fs, 31))
+    idx, cidx = torch.tensor(rows, device="cuda"), torch.tensor(cols, device="cuda")
+    d = {k: v.cuda() for k, v in inp.items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], N)
+    dX_ref = oracle.tp_mlp_backward_dx_rows(X, dY, shards, rows)
+    for mode in ("faithful", "fused"):
+        dX, dA, dB = tp.tpmlp_backward(d["X"], d["dY"], sh, mode)
+        check(f64(dX.index_select(0, idx)), dX_ref, f"{name} {mode} dX")
+        for i in (0, N - 1):
+            check(f64(dA[i].index_select(1, cidx)), oracle.grad_A_cols(X, dY, shards[i][0], shards[i][1], cols),
+                  f"{name} {mode} dA_{i}")
+            check(f64(dB[i].index_select(0, cidx)), oracle.grad_B_rows(X, dY, shards[i][0], cols),
+                  f"{name} {mode} dB_{i}")
+    tp.tpmlp_check_status()
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("flag", ["1", "0"], ids=["dual", "two_products"])
+def test_dual_and_two_product_backward_against_oracle(flag):
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    env = dict(os.environ, TPMLP_BWD_DUAL=flag)
+    r = subprocess.run([sys.executable, "-c", DUAL_CHILD], env=env, cwd=ROOT, capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
