@@ -14,8 +14,8 @@
 //
 // A second-product tile of band b reads H rows of band b, written by the
 // epilogues of that band's first-product tiles on other SMs. Each epilogue
-// warp, after its stores of a first-product tile, fences them to GPU scope
-// and adds one to the band's counter in global memory; the producer of a
+// warp, once its TMA stores of a first-product tile have completed, fences
+// them to GPU scope and adds one to the band's counter in global memory; the producer of a
 // second-product tile waits (bounded) until the counter shows every warp of
 // every tile of the band, then orders its coming TMA reads after that
 // observation with a proxy fence. A pair's tiles come in increasing list
@@ -25,8 +25,10 @@
 //
 // Roles per CTA as in gemm_pair.cu: warp 0 lane 0 the TMA producer, the even
 // CTA's warp 1 lane 0 the MMA issuer (M = 256, N = 256, K = 16), warps 2..5
-// the epilogue (GeLU -> bf16 H for the first product; fp32 through TMA
-// stores for the second). Every wait is bounded.
+// the epilogue (GeLU -> bf16 H for the first product, fp32 for the second,
+// both through shared-memory staging and TMA stores). Every wait is bounded.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <cstring>
 
@@ -52,6 +54,7 @@ struct FwdParams {
   CUtensorMap map_h[kMaxGroups];    // H_i [T][Fs], 64 x 128 boxes (the second product's M x K operand)
   CUtensorMap map_bt[kMaxGroups];   // B_i^T [D][Fs], 64 x 128 boxes
   CUtensorMap map_out[kMaxGroups];  // fp32 outputs in 32 x 32 boxes: Y ([0], chain) or Y_i
+  CUtensorMap map_hs[kMaxGroups];   // H_i as the first product's output, bf16 in 64 x 32 boxes
   void* h[kMaxGroups];              // H_i, bf16 [T][Fs]
   int M, N1, N2;                    // T, F/n, D
   int groups, chain;
@@ -120,6 +123,8 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int target, const W
     __nanosleep(200);
   }
 }
+
+static_assert(sizeof(FwdParams) <= 32764, "kernel parameters above the 32764-byte limit");
 
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
   constexpr int BN = 256;
@@ -325,26 +330,41 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
       }
       tc_fence_after_sync();
       const int64_t m_warp = int64_t(f.mb) * 256 + int64_t(pos) * 128 + quarter * 32;
-      const int64_t m = m_warp + lane;
-      const bool row_ok = m < p.M;
       const int N = f.second ? p.N2 : p.N1;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(p.h[f.g]) + m * p.N1;
       auto finish = [&](int c, const uint32_t (&r)[32]) {
         const int n0 = f.nb * BN + c;
         if (!f.second) {
-          // H = GeLU(acc), bf16, row-major.
-          if (!row_ok || n0 >= N) return;
+          // H = GeLU(acc) in bf16, staged as the warp's 32 x 64 block (128-byte
+          // rows, 128-byte swizzle: 16-byte unit u of row r at u ^ (r % 8)),
+          // two 32-column chunks per block, then one TMA store of the block
+          // (clipped to T x F/n): whole lines instead of each lane writing its
+          // own row.
+          const int half = (c >> 5) & 1;
+          const int nb0 = n0 - 32 * half;  // the block's first column (a multiple of 64)
+          if (nb0 >= N || m_warp >= p.M) return;  // warp-uniform, the same for both chunks of a block
+          uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * kFwdOutBlock;
+          if (half == 0) {
+            if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // the buffer's previous store has read it
+            __syncwarp();
+          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            if (n0 + 8 * j + 8 > N) continue;
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = gelu_bf16_fast(__uint_as_float(r[8 * j + e]));
-            store16(hrow + n0 + 8 * j,
-                    make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                               pack_bf16x2(x[6], x[7])),
-                    false);
+            *reinterpret_cast<uint4*>(buf + lane * 128 + (((4 * half + j) ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                           pack_bf16x2(x[6], x[7]));
+          }
+          if (half == 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.map_hs[f.g], buf, nb0, static_cast<int32_t>(m_warp));
+              bulk_commit_group();
+            }
+            ++blocks_out;
           }
           return;
         }
@@ -392,11 +412,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
         }
       }
       if (!f.second) {
-        // This warp's rows of the band are written: make them visible at GPU
-        // scope, then count the warp in the band.
-        __threadfence();
+        // This warp's rows of the band are written once its TMA stores have
+        // completed: then make them visible at GPU scope (the async-proxy
+        // writes ordered before the generic release) and count the warp in
+        // the band.
+        if (lane == 0) {
+          bulk_wait_group_all();
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          atomicAdd(p.band_done + f.mb, 1);
+        }
         __syncwarp();
-        if (lane == 0) atomicAdd(p.band_done + f.mb, 1);
       }
       if (++acc == 2) {
         acc = 0;
@@ -427,6 +453,28 @@ __global__ void zero_counters_kernel(int* ctr, int n) {
 }
 
 }  // namespace
+
+// TMA map of H_i [rows][cols] (bf16, row pitch cols) as an output written in
+// 64 x 32 boxes with the 128-byte swizzle of the staging blocks.
+bool encode_h_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!encode) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int fwd_persistent_clusters() {
   static std::atomic<int> cached[64] = {};
@@ -470,6 +518,8 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
     p.h[i] = f.h[i];
   }
   for (int i = 0; i < (f.chain ? 1 : f.groups); ++i) p.map_out[i] = *f.map_out[i];
+  for (int i = 0; i < f.groups; ++i)
+    if (!encode_h_store_map(&p.map_hs[i], f.h[i], f.M, f.N1)) return cudaErrorInvalidValue;
   p.M = f.M;
   p.N1 = f.N1;
   p.N2 = f.N2;
