@@ -27,8 +27,6 @@
 // CTA's warp 1 lane 0 the MMA issuer (M = 256, N = 256, K = 16), warps 2..5
 // the epilogue (GeLU -> bf16 H for the first product, fp32 for the second,
 // both through shared-memory staging and TMA stores). Every wait is bounded.
-#include <cudaTypedefs.h>
-
 #include <atomic>
 #include <cstring>
 
@@ -454,28 +452,6 @@ __global__ void zero_counters_kernel(int* ctr, int n) {
 
 }  // namespace
 
-// TMA map of H_i [rows][cols] (bf16, row pitch cols) as an output written in
-// 64 x 32 boxes with the 128-byte swizzle of the staging blocks.
-bool encode_h_store_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
-  static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      fn = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }();
-  if (!encode) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
-  const cuuint32_t box[2] = {64, 32};
-  const cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int fwd_persistent_clusters() {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -519,7 +495,7 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
   }
   for (int i = 0; i < (f.chain ? 1 : f.groups); ++i) p.map_out[i] = *f.map_out[i];
   for (int i = 0; i < f.groups; ++i)
-    if (!encode_h_store_map(&p.map_hs[i], f.h[i], f.M, f.N1)) return cudaErrorInvalidValue;
+    if (!make_output_map_bf16(&p.map_hs[i], f.h[i], f.M, f.N1, f.N1)) return cudaErrorInvalidValue;
   p.M = f.M;
   p.N1 = f.N1;
   p.N2 = f.N2;

@@ -49,11 +49,12 @@ struct PairCfg {
   static constexpr uint32_t B_BYTES = KSUB * kSubBytes;  // this CTA's half of the 256 N rows
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;  // two accumulators of 256 fp32 columns
-  // kEpiF32Tma: two 32 x 32 fp32 staging blocks (4 KB each) per epilogue warp.
-  static constexpr uint32_t OUT_BLOCK = 32 * 32 * 4;
+  // TMA-store epilogues: two 4 KB staging blocks per epilogue warp (32 rows
+  // of 128 bytes: 32 fp32 or 64 bf16 columns).
+  static constexpr uint32_t OUT_BLOCK = 32 * 128;
   template <int EPI>
   static constexpr uint32_t staging() {
-    return EPI == kEpiF32Tma ? 4 * 2 * OUT_BLOCK : 0;
+    return (EPI == kEpiF32Tma || EPI == kEpiGeluTma) ? 4 * 2 * OUT_BLOCK : 0;
   }
   template <int EPI>
   static constexpr size_t smem() {
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  uint8_t* s_out = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned staging of kEpiF32Tma
+  uint8_t* s_out = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned staging of the TMA-store epilogues
   uint64_t* full = reinterpret_cast<uint64_t*>(s_out + C::template staging<EPI>());
   uint64_t* empty = full + C::STAGES;
   uint64_t* acc_full = empty + C::STAGES;
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
     const uint32_t acc_empty_lead = map_to_cta(smem_addr(acc_empty), lead);
     int acc = 0;
     uint32_t acc_phase = 0;
-    int blocks_out = 0;  // kEpiF32Tma: 32 x 32 blocks this warp has handed to TMA so far
+    int blocks_out = 0;  // TMA-store epilogues: staging blocks this warp has handed to TMA so far
     for (int tile = cluster; tile < p.tiles; tile += nclusters) {
       int g, mb, nb;
       decode_tile(p, tile, g, mb, nb);
@@ -335,6 +336,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
             bulk_commit_group();
           }
           ++blocks_out;
+        } else if constexpr (EPI == kEpiGeluTma) {
+          // GeLU'd bf16: the warp's 32 x 64 block (128-byte rows, the same
+          // swizzle) takes two 32-column chunks, then one TMA store writes it,
+          // clipped to M x N.
+          const int half = (c >> 5) & 1;
+          const int nb0 = n0 - 32 * half;  // the block's first column, a multiple of 64
+          if (nb0 >= p.N || m_warp >= p.M) return;  // warp-uniform, the same for both chunks of a block
+          uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
+          if (half == 0) {
+            if (!TPMLP_DCHECK(nb0 % 64 == 0 && m_warp % 32 == 0 && nb0 >= 0 && m_warp >= 0, p.status, kChkOutput))
+              return;
+            if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+            __syncwarp();
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + (((4 * half + j) ^ (lane & 7)) << 4)) =
+                make_uint4(pack_bf16x2(gelu_bf16_fast(v[8 * j]), gelu_bf16_fast(v[8 * j + 1])),
+                           pack_bf16x2(gelu_bf16_fast(v[8 * j + 2]), gelu_bf16_fast(v[8 * j + 3])),
+                           pack_bf16x2(gelu_bf16_fast(v[8 * j + 4]), gelu_bf16_fast(v[8 * j + 5])),
+                           pack_bf16x2(gelu_bf16_fast(v[8 * j + 6]), gelu_bf16_fast(v[8 * j + 7])));
+          if (half == 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.map_out[g], buf, nb0, static_cast<int32_t>(m_warp));
+              bulk_commit_group();
+            }
+            ++blocks_out;
+          }
         } else {
           if (!row_ok || n0 >= p.N) return;
           epilogue_store<EPI>(p, g, m, n0, v);
@@ -371,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
         acc_phase ^= 1u;
       }
     }
-    if constexpr (EPI == kEpiF32Tma) {
+    if constexpr (EPI == kEpiF32Tma || EPI == kEpiGeluTma) {
       if (lane == 0) bulk_wait_group_all();  // every store has left shared memory and landed
       __syncwarp();
     }
@@ -443,6 +474,8 @@ cudaError_t launch_epi(const KParams& kp, int epi, cudaStream_t s) {
       return launch_impl<kEpiGeluSaveP, stages_of<kEpiGeluSaveP>()>(kp, s);
     case kEpiBf16:
       return launch_impl<kEpiBf16, stages_of<kEpiBf16>()>(kp, s);
+    case kEpiGeluTma:
+      return launch_impl<kEpiGeluTma, stages_of<kEpiGeluTma>()>(kp, s);
     default:
       return cudaErrorInvalidValue;
   }

@@ -483,6 +483,10 @@ bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t col
   return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rows, cols, pitch_elems * 4, 32, 32);
 }
 
+bool make_output_map_bf16(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems) {
+  return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, cols, pitch_elems * 2, 64, 32);
+}
+
 cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   KParams kp;
   memset(&kp, 0, sizeof(kp));
@@ -554,9 +558,12 @@ cudaError_t launch_tc_gemm(const TcGemm& g, uint64_t wait_ns, cudaStream_t s) {
   if (pair) {
     // Outputs with TMA maps leave the pair kernels through TMA stores.
     // (with rank slices only when no warp's 32 rows straddle two slices)
-    const bool tma_out = g.epi == kEpiF32 && g.map_out[0] != nullptr && g.slice_rows % 32 == 0 &&
-                         env_int("TPMLP_TMA_STORE", 1) != 0;
-    return launch_pair(kp, tma_out ? kEpiF32Tma : g.epi, s);
+    // TPMLP_TMA_STORE: bit 0 the fp32 outputs, bit 1 the GeLU'd bf16 H (default both).
+    const int tma_bits = env_int("TPMLP_TMA_STORE", 3);
+    const bool tma_out = g.map_out[0] != nullptr && g.slice_rows % 32 == 0 &&
+                         ((g.epi == kEpiF32 && (tma_bits & 1)) || (g.epi == kEpiGeluBf16 && (tma_bits & 2)));
+    const int epi = !tma_out ? g.epi : g.epi == kEpiF32 ? kEpiF32Tma : kEpiGeluTma;
+    return launch_pair(kp, epi, s);
   }
   if (BN == 64) return launch_single_epi<64>(kp, g.epi, s);
   return BN == 256 ? launch_single_epi<256>(kp, g.epi, s) : launch_single_epi<128>(kp, g.epi, s);

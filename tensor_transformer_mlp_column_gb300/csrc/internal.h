@@ -50,6 +50,7 @@ enum TcEpilogue : int {
   kEpiF32Tma = 3,    // out fp32 = acc through TMA stores (chosen by the launcher when map_out is given)
   kEpiGeluSaveP = 4, // out bf16 = GeLU(acc) and out2 fp32 = acc (the pre-activation), same row stride
   kEpiBf16 = 5,      // out bf16 = acc
+  kEpiGeluTma = 6,   // out bf16 = GeLU(acc) through TMA stores (chosen by the launcher when map_out is given)
 };
 
 enum TcShared : int { kSharedNone = 0, kSharedA = 1, kSharedB = 2 };
@@ -68,7 +69,7 @@ struct TcGemm {
                                                 // tiles; used only when every group has one)
   void* out[kMaxGroups];                 // row-major outputs, row stride ldo
   void* out2[kMaxGroups];                // kEpiGeluSaveP: fp32 pre-activation; kEpiBwdAct: H (bf16); row stride ldo
-  const CUtensorMap* map_out[kMaxGroups];  // optional fp32 output maps (make_output_map_f32) for TMA stores
+  const CUtensorMap* map_out[kMaxGroups];  // optional output maps for TMA stores (fp32: make_output_map_f32; GeLU: _bf16)
   const void* aux_p[kMaxGroups];         // kEpiBwdAct only: P (fp32, row stride ldo)
   void* aux_ht[kMaxGroups];              // kEpiBf16 only: V^T (bf16, row stride ldt)
   int64_t ldo;
@@ -154,6 +155,8 @@ bool make_operand_map_mn3d(CUtensorMap* map, const void* base, int64_t rows, int
 // Encodes a TMA map for an fp32 output matrix [rows, cols] (row pitch
 // pitch_elems) written in 32 x 32 boxes with 128-byte swizzling.
 bool make_output_map_f32(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
+// The same for a bf16 output matrix, written in 64-column x 32-row boxes.
+bool make_output_map_bf16(CUtensorMap* map, void* base, int64_t rows, int64_t cols, int64_t pitch_elems);
 // Box heights of the two operands used by the tensor-core kernel.
 int tc_box_rows_a();       // M x K operand (rows of the output)
 int tc_box_rows_b(int N);  // N x K operand of a product with N output columns
