@@ -23,10 +23,13 @@
 // and the grid never exceeds the clusters that can be resident at once:
 // every counter a pair waits on is completed by pairs that never wait.
 //
-// Roles per CTA as in gemm_pair.cu: warp 0 lane 0 the TMA producer, the even
-// CTA's warp 1 lane 0 the MMA issuer (M = 256, N = 256, K = 16), warps 2..5
-// the epilogue (GeLU -> bf16 H for the first product, fp32 for the second,
-// both through shared-memory staging and TMA stores). Every wait is bounded.
+// Roles per CTA: warp 0 lane 0 the TMA producer, the even CTA's warp 1 lane 0
+// the MMA issuer (M = 256, N = 256, K = 16), warps 2..9 the epilogue (GeLU ->
+// bf16 H for the first product, fp32 for the second, both through
+// shared-memory staging and TMA stores): two warps per TMEM lane quarter, one
+// for each half of the 256 accumulator columns, so that the short tiles'
+// epilogues (K = 768..1024 is only 12..16 K blocks of MMAs) keep up with the
+// tensor cores. Every wait is bounded.
 #include <atomic>
 #include <cstring>
 
@@ -41,8 +44,10 @@ constexpr int kFwdKsub = 2;                              // K blocks per stage
 constexpr int kFwdStages = 3;
 constexpr uint32_t kFwdHalf = kFwdKsub * kFwdSub;        // a stage's M x K (or N x K) part
 constexpr uint32_t kFwdStageBytes = 2 * kFwdHalf;
-constexpr uint32_t kFwdOutBlock = 32 * 32 * 4;           // one 32 x 32 fp32 staging block
-constexpr uint32_t kFwdStaging = 4 * 2 * kFwdOutBlock;   // two per epilogue warp
+constexpr int kFwdEpiWarps = 8;                          // two per TMEM lane quarter
+constexpr int kFwdThreads = 64 + 32 * kFwdEpiWarps;      // producer warp, MMA warp, epilogue warps
+constexpr uint32_t kFwdOutBlock = 32 * 128;              // 32 rows of 128 bytes: 32 fp32 or 64 bf16 columns
+constexpr uint32_t kFwdStaging = kFwdEpiWarps * kFwdOutBlock;  // one per epilogue warp
 constexpr uint32_t kFwdTmemCols = 512;                   // two accumulators of 256 columns
 constexpr size_t kFwdSmem = 1024 + size_t(kFwdStages) * kFwdStageBytes + kFwdStaging + 256;
 
@@ -124,7 +129,7 @@ __device__ __forceinline__ bool wait_counter(const int* ctr, int target, const W
 
 static_assert(sizeof(FwdParams) <= 32764, "kernel parameters above the 32764-byte limit");
 
-__global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
   constexpr int BN = 256;
   constexpr uint32_t kCtas = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full + b, 1);
-      mbar_init(acc_empty + b, 8);
+      mbar_init(acc_empty + b, 2 * kFwdEpiWarps);  // every epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -312,12 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5 of every CTA)
-    const int quarter = warp & 3;
+    // ---------------- epilogue (warps 2..9 of every CTA)
+    const int quarter = warp & 3;                 // TMEM lanes (rows) quarter*32 .. +31
+    const int col0 = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the accumulator columns
+    uint8_t* const buf = s_out + (warp - 2) * kFwdOutBlock;
     const uint32_t acc_empty_lead = map_to_cta(smem_addr(acc_empty), lead);
     int acc = 0;
     uint32_t acc_phase = 0;
-    int blocks_out = 0;  // 32 x 32 blocks this warp has handed to TMA so far
+    int blocks_out = 0;  // staging blocks this warp has handed to TMA so far
     for (int tile = cluster; tile < p.tiles; tile += nclusters) {
       const FwdTile f = decode_fwd(p, tile);
       if (!fwd_tile_ok(p, f)) continue;
@@ -341,9 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
           const int half = (c >> 5) & 1;
           const int nb0 = n0 - 32 * half;  // the block's first column (a multiple of 64)
           if (nb0 >= N || m_warp >= p.M) return;  // warp-uniform, the same for both chunks of a block
-          uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * kFwdOutBlock;
           if (half == 0) {
-            if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // the buffer's previous store has read it
+            if (blocks_out >= 1 && lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
             __syncwarp();
           }
 #pragma unroll
@@ -369,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
         // fp32 through a TMA store of the warp's 32 x 32 block (128-byte swizzled staging).
         if (n0 >= N || m_warp >= p.M) return;  // warp-uniform
         if (!TPMLP_DCHECK(n0 % 32 == 0 && m_warp % 32 == 0, p.status, kChkOutput)) return;
-        uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * kFwdOutBlock;
-        if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+        if (blocks_out >= 1 && lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
         __syncwarp();
 #pragma unroll
         for (int j = 0; j < 8; ++j)
@@ -386,16 +391,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
       };
       uint32_t ra[32], rb[32];
       __syncwarp();
-      tmem_ld_32cols_issue(t_row, ra);
+      tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(col0), ra);
       tmem_ld_wait(ra);
 #pragma unroll 1
-      for (int c = 0; c < BN; c += 64) {
+      for (int c = col0; c < col0 + BN / 2; c += 64) {
         __syncwarp();
         tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c + 32), rb);
         finish(c, ra);
         __syncwarp();
         tmem_ld_wait(rb);
-        if (c + 64 == BN) {
+        if (c + 64 == col0 + BN / 2) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
@@ -404,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_persistent_kernel(const __
           tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c + 64), ra);
         }
         finish(c + 32, rb);
-        if (c + 64 < BN) {
+        if (c + 64 < col0 + BN / 2) {
           __syncwarp();
           tmem_ld_wait(ra);
         }
@@ -469,7 +474,7 @@ int fwd_persistent_clusters() {
     attr[0].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kFwdThreads, 1, 1);
     cfg.dynamicSmemBytes = kFwdSmem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -508,7 +513,7 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
   p.k_blocks2 = (f.N1 + BK - 1) / BK;
   p.tiles1 = p.m_blocks * p.n_blocks1 * f.groups;
   p.tiles = p.tiles1 + p.m_blocks * p.n_blocks2 * (f.chain ? 1 : f.groups);
-  p.band_arrivals = p.n_blocks1 * f.groups * 8 + f.band_extra;  // 4 epilogue warps in each CTA of the pair
+  p.band_arrivals = p.n_blocks1 * f.groups * 2 * kFwdEpiWarps + f.band_extra;  // every epilogue warp of the pair
   p.band_done = f.band_done;
   p.wait_ns = wait_ns;
   p.status = device_status_word();
@@ -530,7 +535,7 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
   // that other pairs write.
   const int clusters = p.tiles < clusters_max ? p.tiles : clusters_max;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
   cfg.dynamicSmemBytes = kFwdSmem;
   cfg.stream = s;
   cfg.attrs = attr;
