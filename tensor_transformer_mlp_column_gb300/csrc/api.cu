@@ -116,7 +116,9 @@ bool use_persistent_forward(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode) 
   if (!on || sh->dt != TPMLP_BF16 || !tc_pairs_enabled()) return false;
   const int64_t mb = (T + 255) / 256;
   const int64_t t1 = mb * ((sh->Fs + 255) / 256) * sh->n;
-  const int64_t t2 = mb * ((sh->D + 255) / 256) * (mode == TPMLP_FUSED ? 1 : sh->n);
+  const int chain = mode == TPMLP_FUSED ? 1 : 0;
+  const int w2 = fwd_second_width(T, sh->D, chain);
+  const int64_t t2 = mb * ((sh->D + w2 - 1) / w2) * (chain ? 1 : sh->n);
   const int64_t sms = num_sms();
   const int pairs = fwd_persistent_clusters();
   return pairs > 0 && t1 >= sms / 4 && t2 >= sms / 4 && t1 + t2 <= 8 * static_cast<int64_t>(pairs);
@@ -392,6 +394,7 @@ int run_forward_persistent(const void* X, int64_t T, const tpmlp_shards* sh, voi
     f.map_at[i] = &sh->map_At[i];
     f.map_h[i] = &mh[i];
     f.map_bt[i] = &sh->map_Bt[i];
+    f.map_bt64[i] = &sh->map_Bt64[i];
     void* out = Yp ? static_cast<void*>(Yp + static_cast<size_t>(i) * T * D) : Y;
     if ((i == 0 || Yp) && (rc = out_map(&mo[i], out, T, D, D, Yp ? "Y_i" : "Y"))) return rc;
     f.map_out[i] = &mo[Yp ? i : 0];

@@ -31,6 +31,7 @@
 // epilogues (K = 768..1024 is only 12..16 K blocks of MMAs) keep up with the
 // tensor cores. Every wait is bounded.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "gemm_common.cuh"
@@ -56,12 +57,14 @@ struct FwdParams {
   CUtensorMap map_at[kMaxGroups];   // A_i^T [Fs][D], 64 x 128 boxes
   CUtensorMap map_h[kMaxGroups];    // H_i [T][Fs], 64 x 128 boxes (the second product's M x K operand)
   CUtensorMap map_bt[kMaxGroups];   // B_i^T [D][Fs], 64 x 128 boxes
+  CUtensorMap map_bt64[kMaxGroups]; // the same in 64 x 64 boxes (second-product tiles 128 wide)
   CUtensorMap map_out[kMaxGroups];  // fp32 outputs in 32 x 32 boxes: Y ([0], chain) or Y_i
   CUtensorMap map_hs[kMaxGroups];   // H_i as the first product's output, bf16 in 64 x 32 boxes
   void* h[kMaxGroups];              // H_i, bf16 [T][Fs]
   int M, N1, N2;                    // T, F/n, D
   int groups, chain;
   int m_blocks, n_blocks1, n_blocks2, k_blocks1, k_blocks2;
+  int bn2;            // width of the second product's tiles: 256, or 128 for a short shard-ordered sum
   int tiles1, tiles;
   int band_arrivals;  // epilogue-warp arrivals that complete a band of H
   int* band_done;     // [m_blocks] counters, zero at launch
@@ -214,8 +217,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
           }
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
+        const int tbn = f.second ? p.bn2 : BN;  // the tile's width; each CTA loads half of its N x K rows
+        const bool narrow = tbn != BN;
         const int m0 = f.mb * 256 + static_cast<int>(pos) * 128;
-        const int n0 = f.nb * BN + static_cast<int>(pos) * 128;
+        const int n0 = f.nb * tbn + static_cast<int>(pos) * (tbn / 2);
         const int kb_tile = k_blocks_of(f);
         const int kb_group = f.second ? p.k_blocks2 : p.k_blocks1;
         int gg = f.g, kk = 0;
@@ -231,13 +236,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
             break;
           }
           if (pos == 0) {
-            mbar_arrive_expect_tx(full + stage, 2 * 2 * nsub * kFwdSub);  // both CTAs' A and B
+            mbar_arrive_expect_tx(full + stage, 2 * nsub * (kFwdSub + (narrow ? kFwdSub / 2 : kFwdSub)));  // both CTAs' A and B
             armed |= 1u << stage;
             parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
           }
           for (int u = 0; u < nsub; ++u) {
             const CUtensorMap* ma = f.second ? &p.map_h[gg] : &p.map_x;
-            const CUtensorMap* mbm = f.second ? &p.map_bt[gg] : &p.map_at[gg];
+            const CUtensorMap* mbm = !f.second ? &p.map_at[gg] : narrow ? &p.map_bt64[gg] : &p.map_bt[gg];
             tma_load_2d_pair_hint(sA + stage * kFwdHalf + u * kFwdSub, ma, kk * BK, m0, full_lead, pol_a);
             tma_load_2d_pair_hint(sB + stage * kFwdHalf + u * kFwdSub, mbm, kk * BK, n0, full_lead, pol_b);
             if (++kk == kb_group) {
@@ -267,6 +272,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
     if (lane == 0 && pos == 0) {
       // ---------------- MMA issuer (even CTA of each pair)
       constexpr uint32_t IDESC = idesc_bf16_f32(256, BN);
+      constexpr uint32_t IDESC_NARROW = idesc_bf16_f32(256, BN / 2);
       constexpr uint16_t kPairMask = 0x3;
       int stage = 0;
       uint32_t phase = 0;
@@ -282,6 +288,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         const int kb_tile = k_blocks_of(f);
+        const uint32_t idesc = (f.second && p.bn2 != BN) ? IDESC_NARROW : IDESC;
         for (int kb = 0; kb < kb_tile; kb += kFwdKsub) {
           if (!wait_bounded(full + stage, phase, guard, kSiteMmaFull)) {
             aborted = true;
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
             const uint32_t b0 = smem_addr(sB + stage * kFwdHalf + u * kFwdSub);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
-              tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), IDESC,
+              tc_mma_bf16_pair(d_tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc,
                                (kb | u | k) != 0 ? 1u : 0u);
           }
           tc_commit_pair_multicast(empty + stage, kPairMask);
@@ -318,8 +325,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
     }
   } else {
     // ---------------- epilogue (warps 2..9 of every CTA)
-    const int quarter = warp & 3;                 // TMEM lanes (rows) quarter*32 .. +31
-    const int col0 = ((warp - 2) >> 2) * (BN / 2);  // this warp's half of the accumulator columns
+    const int quarter = warp & 3;      // TMEM lanes (rows) quarter*32 .. +31
+    const int half_col = (warp - 2) >> 2;  // which half of the tile's accumulator columns this warp takes
     uint8_t* const buf = s_out + (warp - 2) * kFwdOutBlock;
     const uint32_t acc_empty_lead = map_to_cta(smem_addr(acc_empty), lead);
     int acc = 0;
@@ -336,9 +343,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
       tc_fence_after_sync();
       const int64_t m_warp = int64_t(f.mb) * 256 + int64_t(pos) * 128 + quarter * 32;
       const int N = f.second ? p.N2 : p.N1;
+      const int tbn = f.second ? p.bn2 : BN;
+      const int col0 = half_col * (tbn / 2), col1 = col0 + tbn / 2;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
       auto finish = [&](int c, const uint32_t (&r)[32]) {
-        const int n0 = f.nb * BN + c;
+        const int n0 = f.nb * tbn + c;
         if (!f.second) {
           // H = GeLU(acc) in bf16, staged as the warp's 32 x 64 block (128-byte
           // rows, 128-byte swizzle: 16-byte unit u of row r at u ^ (r % 8)),
@@ -394,13 +403,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
       tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(col0), ra);
       tmem_ld_wait(ra);
 #pragma unroll 1
-      for (int c = col0; c < col0 + BN / 2; c += 64) {
+      for (int c = col0; c < col1; c += 64) {
         __syncwarp();
         tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c + 32), rb);
         finish(c, ra);
         __syncwarp();
         tmem_ld_wait(rb);
-        if (c + 64 == col0 + BN / 2) {
+        if (c + 64 == col1) {
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster_relaxed(acc_empty_lead + 8u * static_cast<uint32_t>(acc));
@@ -409,7 +418,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
           tmem_ld_32cols_issue(t_row + static_cast<uint32_t>(c + 64), ra);
         }
         finish(c + 32, rb);
-        if (c + 64 < col0 + BN / 2) {
+        if (c + 64 < col1) {
           __syncwarp();
           tmem_ld_wait(ra);
         }
@@ -457,6 +466,20 @@ __global__ void zero_counters_kernel(int* ctr, int n) {
 
 }  // namespace
 
+int fwd_second_width(int64_t M, int64_t N2, int chain) {
+  static const int narrow = [] {
+    const char* e = getenv("TPMLP_FWD_NARROW2");
+    return (e && *e) ? atoi(e) : 1;
+  }();
+  if (!chain || !narrow) return 256;
+  // Half-width tiles load 1.5 times the bytes per MMA of full ones: they pay
+  // only while the sum's tiles leave most pairs idle (the narrow tiles still
+  // fit one round), not when every SM is loading from L2 at once.
+  const int64_t tiles = ((M + 255) / 256) * ((N2 + 255) / 256);
+  const int pairs = fwd_persistent_clusters();
+  return 2 * tiles <= pairs ? 128 : 256;
+}
+
 int fwd_persistent_clusters() {
   static std::atomic<int> cached[64] = {};
   int dev = 0;
@@ -496,6 +519,7 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
     p.map_at[i] = *f.map_at[i];
     p.map_h[i] = *f.map_h[i];
     p.map_bt[i] = *f.map_bt[i];
+    p.map_bt64[i] = *f.map_bt64[i];
     p.h[i] = f.h[i];
   }
   for (int i = 0; i < (f.chain ? 1 : f.groups); ++i) p.map_out[i] = *f.map_out[i];
@@ -508,7 +532,8 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
   p.chain = f.chain;
   p.m_blocks = (f.M + 255) / 256;
   p.n_blocks1 = (f.N1 + 255) / 256;
-  p.n_blocks2 = (f.N2 + 255) / 256;
+  p.bn2 = fwd_second_width(f.M, f.N2, f.chain);
+  p.n_blocks2 = (f.N2 + p.bn2 - 1) / p.bn2;
   p.k_blocks1 = (f.K1 + BK - 1) / BK;
   p.k_blocks2 = (f.N1 + BK - 1) / BK;
   p.tiles1 = p.m_blocks * p.n_blocks1 * f.groups;

@@ -127,6 +127,7 @@ struct FwdPersistent {
   const CUtensorMap* map_at[kMaxGroups];
   const CUtensorMap* map_h[kMaxGroups];
   const CUtensorMap* map_bt[kMaxGroups];
+  const CUtensorMap* map_bt64[kMaxGroups];  // B_i^T in 64-row boxes
   const CUtensorMap* map_out[kMaxGroups];
   void* h[kMaxGroups];
   int M, N1, N2, K1;
@@ -138,6 +139,11 @@ cudaError_t launch_fwd_persistent(const FwdPersistent& f, uint64_t wait_ns, cuda
 // CTA pairs of the persistent forward that fit the device at once (0 if it
 // cannot be launched).
 int fwd_persistent_clusters();
+// Width of the persistent forward's second-product tiles: 128 for a
+// shard-ordered sum (chain) whose 256 x 256 tiles number at most half the CTA
+// pairs (twice the tiles, each half as long), else 256
+// (TPMLP_FWD_NARROW2=0: always 256).
+int fwd_second_width(int64_t M, int64_t N2, int chain);
 
 // Encodes a TMA map for a row-major bf16 matrix [rows, cols] with row pitch
 // `pitch_elems` (cols contiguous), boxes of 64 columns x box_rows rows and
