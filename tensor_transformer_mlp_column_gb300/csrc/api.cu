@@ -213,6 +213,7 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
   const int64_t D = sh->D, Fs = sh->Fs;
   if (sh->dt == TPMLP_BF16) {
     CUtensorMap mx;
+    std::vector<CUtensorMap> mo(sh->n);
     int rc = map_or_fail(&mx, X, T, D, D, tc_box_rows_a(), "X");
     if (rc) return rc;
     TcGemm g{};
@@ -221,7 +222,15 @@ int run_hidden(const void* X, int64_t T, const tpmlp_shards* sh, void* H, cudaSt
       g.map_a[i] = &mx;
       g.map_b[i] = &sh->map_At[i];
       g.out[i] = at<uint16_t>(H, 0) + static_cast<size_t>(i) * T * Fs;
-      if (P_out) g.out2[i] = static_cast<float*>(P_out) + static_cast<size_t>(i) * T * Fs;
+      if (P_out) {
+        g.out2[i] = static_cast<float*>(P_out) + static_cast<size_t>(i) * T * Fs;
+      } else {
+        // H_i leaves the pair kernel through TMA stores.
+        if (!make_output_map_bf16(&mo[i], g.out[i], T, Fs, Fs))
+          return fail(TPMLP_ERR_CUDA, "cuTensorMapEncodeTiled rejected the output map of H_%d [%lld x %lld]", i,
+                      static_cast<long long>(T), static_cast<long long>(Fs));
+        g.map_out[i] = &mo[i];
+      }
     }
     g.ldo = Fs;
     g.M = static_cast<int>(T);

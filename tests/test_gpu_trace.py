@@ -26,10 +26,10 @@ d = {k: v.cuda() for k, v in make_inputs(w, seed=91).items()}
 sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
 torch.cuda.synchronize()
 tp.tpmlp_trace_read()  # forget set-up
-# (the faithful forward of this shape runs both products in one persistent launch)
+# (both forwards of this shape run both products in one persistent launch)
 expect = {
     ("forward", "faithful"): ["forward_persistent", "allreduce"],
-    ("forward", "fused"): ["gemm1_gelu", "gemm2_fused_sum"],
+    ("forward", "fused"): ["forward_persistent"],
     ("backward", "faithful"): ["bwd_dual_P_dH", "bwd_dB", "bwd_dA", "bwd_dX_partials", "bwd_dx_allreduce"],
     ("backward", "fused"): ["bwd_dual_P_dH", "bwd_dB", "bwd_dA", "bwd_dX_fused_sum"],
 }
@@ -47,6 +47,16 @@ for (call, mode), names in expect.items():
         assert [s for s, _ in steps] == names, (call, mode, steps)
         assert all(ms > 0 for _, ms in steps), steps
         assert sum(ms for _, ms in steps) <= total * 1.02 + 0.01, (steps, total)
+# A shard-ordered sum too short for the one-launch form (T=1024): two launches.
+w2 = Workload("trace2", 1024, 1024, 4096, 4, "bf16", 1.0, 0.02, 0.02, 1.0, True)
+d2 = {k: v.cuda() for k, v in make_inputs(w2, seed=92).items()}
+sh2 = tp.tpmlp_shard(d2["A"], d2["B"], w2.N)
+torch.cuda.synchronize()
+tp.tpmlp_trace_read()
+tp.tpmlp_forward(d2["X"], sh2, "fused")
+steps = tp.tpmlp_trace_read()
+assert [s for s, _ in steps] == ["gemm1_gelu", "gemm2_fused_sum"], steps
+assert all(ms > 0 for _, ms in steps), steps
 # Graph capture records nothing; replay matches the eager result.
 Y = torch.empty(w.T, w.D, device="cuda")
 ws = torch.empty(tp.tpmlp_workspace_bytes(w.T, sh, "fused"), dtype=torch.uint8, device="cuda")
