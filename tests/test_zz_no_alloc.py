@@ -86,3 +86,38 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(tp):
     assert "64 MiB" in tp.tpmlp_last_error()
     torch.cuda.synchronize()
     assert not Y.any()  # nothing was enqueued
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["faithful", "fused"])
+def test_noalloc_forward_captures_without_allocating(tp, mode):
+    """After a first call (which caches the scratch address), a call captured
+    into a CUDA graph in global capture mode: a device allocation or free, or
+    any other call the capture forbids, would fail the capture. The replay
+    must match tpmlp_forward. (The eager call leaves the caching allocator's
+    count of allocated bytes where it was; around the capture that count
+    also moves with the graph's own bookkeeping, so it is not compared there.)"""
+    w = Workload("noalloc_graph", 1000, 512, 2048, 4, "bf16", 1.0, 0.04, 0.02)
+    d = {k: v.cuda() for k, v in make_inputs(w, seed=33).items()}
+    sh = tp.tpmlp_shard(d["A"], d["B"], w.N)
+    Y = torch.empty((w.T, w.D), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    allocated = torch.cuda.memory_allocated()
+    with torch.cuda.stream(s):
+        assert _call_noalloc(tp, d["X"], sh, Y, mode) == tp.TPMLP_OK, tp.tpmlp_last_error()
+    s.synchronize()
+    assert torch.cuda.memory_allocated() == allocated
+    Y.fill_(float("nan"))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="global"):
+        assert _call_noalloc(tp, d["X"], sh, Y, mode) == tp.TPMLP_OK, tp.tpmlp_last_error()
+    g.replay()
+    torch.cuda.synchronize()
+    ref = tp.tpmlp_forward(d["X"], sh, "fused" if mode else "faithful")
+    torch.cuda.synchronize()
+    assert torch.isfinite(Y).all()
+    _close(Y, ref, "bf16")
+    if mode == 0:
+        assert torch.equal(Y, ref)
+    tp.tpmlp_check_status()
