@@ -459,9 +459,10 @@ def bench_gelu(local_rank, peaks):
     return out
 
 
-def bench_small_workloads(local_rank):
+def bench_small_workloads(local_rank, only=None):
     """Forward time of the GPT-2-small and the sequence-sweep workloads (both
-    modes), and the linear fit of forward time against seq for the sweep."""
+    modes), and the linear fit of forward time against seq for the sweep
+    (`only`: that one workload alone, no fit)."""
     import torch
 
     import tensor_transformer_mlp_column_gb300 as tp
@@ -470,7 +471,7 @@ def bench_small_workloads(local_rank):
     dev = torch.device("cuda", local_rank)
     stream = torch.cuda.current_stream(dev)
     out = {}
-    for name in ("gpt2_small", "seq128", "seq256", "seq512"):
+    for name in (only,) if only else ("gpt2_small", "seq128", "seq256", "seq512"):
         w = WORKLOADS[name]
         inp = make_inputs(w, seed=0)
         X = inp["X"].to(dev)
@@ -496,6 +497,8 @@ def bench_small_workloads(local_rank):
         tp.tpmlp_check_status(stream)
         sh.free()
         out[name] = res
+    if only:
+        return out
     # FFN time against sequence length (batch 8): a least-squares line and its R^2.
     seqs = [128, 256, 512]
     for mode in ("faithful", "fused"):
@@ -804,6 +807,8 @@ def main():
     ap.add_argument("--no-backward", action="store_true", help="skip the backward measurement (fwd+bwd workload)")
     ap.add_argument("--only", choices=["backward", "gelu", "block", "sp", "attention", "small"], default=None,
                     help="run one secondary measurement alone and print it (smaller profiling commands)")
+    ap.add_argument("--small", choices=["gpt2_small", "seq128", "seq256", "seq512"], default=None,
+                    help="with --only small: that workload alone")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.only:
@@ -813,7 +818,7 @@ def main():
         peaks = load_peaks()
         fn = {"backward": lambda: bench_backward(args, 0, peaks), "gelu": lambda: bench_gelu(0, peaks),
               "block": lambda: bench_block(args, 0, peaks), "sp": lambda: bench_sp(args, 0, peaks),
-              "attention": lambda: bench_attention(args, 0, peaks), "small": lambda: bench_small_workloads(0)}
+              "attention": lambda: bench_attention(args, 0, peaks), "small": lambda: bench_small_workloads(0, args.small)}
         print(json.dumps({"only": args.only, args.only: fn[args.only]()}))
         return
 
