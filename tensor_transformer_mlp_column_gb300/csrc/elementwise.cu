@@ -135,7 +135,8 @@ __global__ void allreduce_any_kernel(const float* __restrict__ Yp, int n, int64_
 // ------------------------------------------------------------------ all-gather
 
 // out = the n input slices back to back (slice_bytes each), blockIdx.y = slice.
-// Each thread moves four words per pass, all four loads issued first.
+// Each thread moves eight words per pass, all eight loads issued first; the
+// output is written with the streaming (evict-first) hint like the reduce's.
 template <typename W>
 __global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__ out, int* status) {
   pdl_wait();
@@ -145,14 +146,14 @@ __global__ void gather_slices_kernel(InSlices in, int64_t words, W* __restrict__
   W* __restrict__ dst = out + int64_t(blockIdx.y) * words;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (; i + 3 * stride < words; i += 4 * stride) {
-    W w[4];
+  for (; i + 7 * stride < words; i += 8 * stride) {
+    W w[8];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = __ldcs(src + i + k * stride);
+    for (int k = 0; k < 8; ++k) w[k] = __ldcs(src + i + k * stride);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) dst[i + k * stride] = w[k];
+    for (int k = 0; k < 8; ++k) __stcs(dst + i + k * stride, w[k]);
   }
-  for (; i < words; i += stride) dst[i] = __ldcs(src + i);
+  for (; i < words; i += stride) __stcs(dst + i, __ldcs(src + i));
 }
 
 // ------------------------------------------------------------------ shard copies
