@@ -357,9 +357,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) tc_fwd_persistent_kernel(const
           const int half = (c >> 5) & 1;
           const int nb0 = n0 - 32 * half;  // the block's first column (a multiple of 64)
           if (nb0 >= N || m_warp >= p.M) return;  // warp-uniform, the same for both chunks of a block
+          // (checked for both chunks, so that a failed check skips the whole block)
+          if (!TPMLP_DCHECK(nb0 % 64 == 0 && m_warp % 32 == 0 && nb0 >= 0 && m_warp >= 0, p.status, kChkOutput))
+            return;
           if (half == 0) {
-            if (!TPMLP_DCHECK(nb0 % 64 == 0 && m_warp % 32 == 0 && nb0 >= 0 && m_warp >= 0, p.status, kChkOutput))
-              return;
             if (blocks_out >= 1 && lane == 0) bulk_wait_group_read<0>();  // the previous store has read the buffer
             __syncwarp();
           }

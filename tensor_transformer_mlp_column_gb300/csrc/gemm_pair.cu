@@ -343,10 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_pair_kernel(const __grid_
           const int half = (c >> 5) & 1;
           const int nb0 = n0 - 32 * half;  // the block's first column, a multiple of 64
           if (nb0 >= p.N || m_warp >= p.M) return;  // warp-uniform, the same for both chunks of a block
+          // (checked for both chunks, so that a failed check skips the whole block)
+          if (!TPMLP_DCHECK(nb0 % 64 == 0 && m_warp % 32 == 0 && nb0 >= 0 && m_warp >= 0, p.status, kChkOutput))
+            return;
           uint8_t* buf = s_out + (quarter * 2 + (blocks_out & 1)) * C::OUT_BLOCK;
           if (half == 0) {
-            if (!TPMLP_DCHECK(nb0 % 64 == 0 && m_warp % 32 == 0 && nb0 >= 0 && m_warp >= 0, p.status, kChkOutput))
-              return;
             if (blocks_out >= 2 && lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
             __syncwarp();
           }
