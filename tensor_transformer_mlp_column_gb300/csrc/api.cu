@@ -104,10 +104,13 @@ struct WsPlan {
 
 // Whether the bf16 forward runs its two products in one persistent launch
 // (gemm_fwd.cu): when both have enough 256 x 256 tiles for CTA pairs (the
-// launcher's own rule) but together no more than 8 rounds of them over the
-// pairs, so that one product's partly filled last round and the other's
-// first can share the GPU. TPMLP_FWD_PERSIST=0 (read once per process) keeps
-// two launches for comparisons.
+// launcher's own rule), together no more than 32 rounds of them over the
+// pairs, and all shards' weights (A_i^T and B_i^T, 4 D F bytes) within
+// 64 MiB: the one launch walks its tiles band by band (256 token rows), so
+// every band streams the whole of the weights, which must stay in L2. There
+// one product's partly filled last round and the other's first share the GPU
+// and no launch separates them. TPMLP_FWD_PERSIST=0 (read once per process)
+// keeps two launches for comparisons.
 bool use_persistent_forward(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode) {
   static const bool on = [] {
     const char* e = getenv("TPMLP_FWD_PERSIST");
@@ -121,7 +124,9 @@ bool use_persistent_forward(int64_t T, const tpmlp_shards* sh, tpmlp_mode mode) 
   const int64_t t2 = mb * ((sh->D + w2 - 1) / w2) * (chain ? 1 : sh->n);
   const int64_t sms = num_sms();
   const int pairs = fwd_persistent_clusters();
-  return pairs > 0 && t1 >= sms / 4 && t2 >= sms / 4 && t1 + t2 <= 8 * static_cast<int64_t>(pairs);
+  const int64_t weight_bytes = 4 * sh->D * static_cast<int64_t>(sh->Fs) * sh->n;
+  return pairs > 0 && t1 >= sms / 4 && t2 >= sms / 4 && t1 + t2 <= 32 * static_cast<int64_t>(pairs) &&
+         weight_bytes <= (int64_t(64) << 20);
 }
 
 // Whether the bf16 recomputing backward runs its first step in the dual

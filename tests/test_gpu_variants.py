@@ -223,7 +223,8 @@ def test_narrow_single_cta_tiles_against_oracle_and_wide(tmp_path):
 # 8 shards, ragged T, D and F/n together (T=2500, D=1288, F/n=1000), 16
 # shards (faithful only: its shard-ordered sum has too few pair tiles), and a
 # ragged D whose shard-ordered sum runs in 256 x 128 tiles (T=1700, D=1160;
-# the ragged-T and 8-shard shapes take those tiles as well).
+# the ragged-T and 8-shard shapes take those tiles as well), and a mid-size
+# shape of 20 rounds of tiles in faithful mode (T=8192, D=1024, F=4096, N=8).
 PERSIST_CHILD = r"""
 import sys, numpy as np, torch
 import oracle
@@ -241,7 +242,7 @@ out = {}
 for name, T, D, F, N in (("gpt2", 4096, 768, 3072, 4), ("seq512", 4096, 1024, 4096, 4),
                          ("ragged", 3000, 768, 3072, 4), ("eight", 2048, 1024, 8192, 8),
                          ("ragged_all", 2500, 1288, 4000, 4), ("sixteen", 1024, 1024, 4096, 16),
-                         ("ragged_narrow", 1700, 1160, 4096, 4)):
+                         ("ragged_narrow", 1700, 1160, 4096, 4), ("mid", 8192, 1024, 4096, 8)):
     w = Workload(name, T, D, F, N, "bf16", 1.0, 0.02, 0.02)
     inp = make_inputs(w, seed=93)
     shards = oracle.shard_mlp(f64(inp["A"]), f64(inp["B"]), N)
