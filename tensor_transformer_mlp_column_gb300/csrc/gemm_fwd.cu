@@ -1,13 +1,14 @@
 // gemm_fwd.cu — the bf16 forward's two products in one persistent launch of
-// CTA pairs, for products too small to fill the GPU one after the other
-// (scratchllm.com "Tensor-Parallel MLP (Megatron)", "The split": H_i =
-// GeLU(X A_i), Y_i = H_i B_i, summed in shard order).
+// CTA pairs, for forwards of a few to a few tens of rounds of tiles whose
+// weights stay in L2 (scratchllm.com "Tensor-Parallel MLP (Megatron)", "The
+// split": H_i = GeLU(X A_i), Y_i = H_i B_i, summed in shard order).
 //
 // The tile list holds every tile of the first product (256 x 256 tiles of
 // each shard's H_i = GeLU(X A_i), in bands of 256 token rows: all shards'
 // column blocks of a band before the next band), then every tile of the
 // second (the shard-ordered sum Y = sum_i H_i B_i, or the partials Y_i = H_i
-// B_i, also band by band). Each CTA pair walks the list from its own index
+// B_i, also band by band; a sum with fewer tiles than half the pairs in
+// 256 x 128 tiles). Each CTA pair walks the list from its own index
 // in steps of the pair count, so a pair whose first-product tiles are done
 // starts on second-product tiles while other pairs finish the first product:
 // the idle SMs of one product's last round work on the other.
@@ -15,10 +16,10 @@
 // A second-product tile of band b reads H rows of band b, written by the
 // epilogues of that band's first-product tiles on other SMs. Each epilogue
 // warp, once its TMA stores of a first-product tile have completed, fences
-// them to GPU scope and adds one to the band's counter in global memory; the producer of a
-// second-product tile waits (bounded) until the counter shows every warp of
-// every tile of the band, then orders its coming TMA reads after that
-// observation with a proxy fence. A pair's tiles come in increasing list
+// them to GPU scope and adds one to the band's counter in global memory; the
+// producer of a second-product tile waits (bounded) until the counter shows
+// every warp of every tile of the band, then orders its coming TMA reads
+// after that observation with a proxy fence. A pair's tiles come in increasing list
 // order, so all of its first-product tiles precede its second-product ones,
 // and the grid never exceeds the clusters that can be resident at once:
 // every counter a pair waits on is completed by pairs that never wait.
