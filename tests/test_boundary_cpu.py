@@ -101,6 +101,17 @@ def test_calls_reject_null_handles(tp):
     l.tpmlp_shards_free(None)  # no-op
 
 
+def test_token_count_outside_its_range(tp):
+    # T >= 1 (and at most 2^30) by the header's contract: an empty or negative
+    # token count is an argument error, reported before the handle is read.
+    l = tp.lib()
+    for T in (0, -1, (1 << 30) + 1):
+        assert l.tpmlp_forward(FAKE, T, FAKE, FAKE, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+        assert "T = " in tp.tpmlp_last_error()
+        assert l.tpmlp_hidden(FAKE, T, FAKE, FAKE, None) == tp.TPMLP_ERR_ARG
+        assert l.tpmlp_backward(FAKE, FAKE, T, FAKE, FAKE, None, None, 0, FAKE, 1 << 20, None) == tp.TPMLP_ERR_ARG
+
+
 def test_gelu_and_allreduce_argument_errors(tp):
     l = tp.lib()
     assert l.tpmlp_gelu(FAKE, FAKE, -1, 0, None) == tp.TPMLP_ERR_ARG
