@@ -216,7 +216,8 @@ int tpmlp_selftest_gemm_withheld_fill(const void* X, int64_t T, const tpmlp_shar
                                       int limit_ms, tpmlp_stream_t stream);
 
 /* Test hook for the persistent forward's band waits (the one-launch form that
- * tpmlp_forward takes for small bf16 products): runs it with every band of H
+ * tpmlp_forward takes for small and mid-size bf16 products whose weights fit
+ * in L2): runs it with every band of H
  * needing one arrival more than its first-product tiles make, so the
  * producer of every second-product tile waits for a band that is never
  * complete and gives up after limit_ms (1..10000); the kernel drains its
