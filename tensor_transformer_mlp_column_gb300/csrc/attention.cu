@@ -48,6 +48,7 @@ struct AttnParams {
   CUtensorMap map_vt[kMaxGroups];   // V_i^T [Dn, T] bf16 (row pitch T8), boxes 64 x 64
   void* out[kMaxGroups];            // O_i [T, Dn]
   int seq, Dn, local_heads;
+  int q_tiles, heads, items;  // streaming kernel: query tiles per head, heads of all ranks, work items
   float scale_log2;  // log2(e) / sqrt(d_h)
   uint64_t wait_ns;
   int* status;
@@ -312,10 +313,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_tc_kernel(const __grid_c
 
 // ------------------------------------------------------------------ streaming form (any seq)
 //
-// One CTA of 8 softmax warps, an MMA warp and a load warp per (128-query tile,
-// head, sequence), 112 KB of shared memory and 256 TMEM columns, so two CTAs
-// share an SM and one's loads and products overlap the other's softmax. Keys
-// go in blocks of 128 with a running maximum m and sum l per query row:
+// CTAs of 8 softmax warps, an MMA warp and a load warp, 112 KB of shared
+// memory and 256 TMEM columns, so two CTAs share an SM and one's loads and
+// products overlap the other's softmax. The work items (128-query tile, head,
+// sequence) go to a persistent grid of two CTAs per SM, each running its
+// items through one pipeline: the ring runs on from item to item, an item's
+// Q lands once the previous item's last score product has read the buffer,
+// and its first P V product waits until the previous item's O is in the
+// softmax warps' registers (6-8 % faster at seq 512 than a CTA per item, 1-3 %
+// at 1024-4096). Keys go in blocks of 128 with a running maximum m and sum l
+// per query row:
 //   load thread: Q once, then K_j and V_j^T (16 KB each) through a ring of
 //     two slots in the order the products read them (K_0, then K_j, V_{j-1}
 //     for j = 1.., then the last V), each slot refilled as soon as the product
@@ -348,7 +355,7 @@ constexpr uint32_t kStrmPBufBytes = 2 * kPChunkBytes;  // P of 128 keys
 constexpr uint32_t kStrmPBytes = 2 * kStrmPBufBytes;   // two P buffers, blocks alternating
 // No alignment slack: the dynamic shared memory is declared 1024-aligned (and
 // checked), so two CTAs fit an SM with both P buffers.
-constexpr uint32_t kStrmSmem = kQBytes + kStrmSlots * kStrmSlotBytes + kStrmPBytes + 128;
+constexpr uint32_t kStrmSmem = kQBytes + kStrmSlots * kStrmSlotBytes + kStrmPBytes + 256;
 static_assert(2 * kVtChunkBytes == kStrmSlotBytes, "V^T of a key block fills one ring slot");
 
 // 32 TMEM columns of this warp's lanes without waiting: the registers are valid
@@ -392,20 +399,12 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     if (threadIdx.x == 0) atomicCAS(p.status, 0, kSiteSmemAlign);
     return;  // CTA-uniform, before any barrier or TMEM allocation
   }
-  // Debug build: the CTA's query tile, rank and output must exist (CTA-uniform).
-  if (!TPMLP_DCHECK(int(blockIdx.x) * 128 < p.seq && int(blockIdx.y) / p.local_heads < kMaxGroups &&
-                        p.out[int(blockIdx.y) / p.local_heads] != nullptr,
-                    threadIdx.x == 0 ? p.status : nullptr, kChkAttnTile))
-    return;
   uint8_t* smem = smem_raw;
   uint8_t* sQ = smem;
   uint8_t* sRing = sQ + kQBytes;  // kStrmSlots slots of one K or V^T block
   uint8_t* sP = sRing + kStrmSlots * kStrmSlotBytes;  // two buffers of kStrmPBufBytes
-  // The halves' final maxima and sums, in ring slot 0 (free once the last product is done).
-  float* red_max = reinterpret_cast<float*>(sRing);  // [2][128]
-  float* red_sum = red_max + 256;                    // [2][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kStrmPBytes);
-  uint64_t* bar_q = bars + 0;
+  uint64_t* bar_q = bars + 0;                     // the item's Q has landed (phase = item count)
   uint64_t* ring_full = bars + 1;                 // [kStrmSlots]
   uint64_t* ring_empty = bars + 1 + kStrmSlots;   // [kStrmSlots]: the product that read the slot has finished
   uint64_t* s_full = bars + 1 + 2 * kStrmSlots;
@@ -413,21 +412,40 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   // even / odd (phase k / 2 of s_free[k % 2]). Two barriers because a warp
   // may finish block k+1 (it waits only for P_{k-1} V_{k-1}) before the MMA
   // thread has waited for block k: one barrier could then be two phases
-  // ahead of that wait.
+  // ahead of that wait. Block indices k count on across the CTA's items.
   uint64_t* s_free = s_full + 1;
   uint64_t* x_bar = s_full + 3;   // one arrival per softmax warp: the halves' partial maxima (sums) written
   uint64_t* drain = s_full + 4;
   uint64_t* s_read = s_full + 5;  // one arrival per softmax warp: its S columns are in registers
   uint64_t* o_done = s_full + 6;  // [2]: P_k V_k done, k even / odd (phase k / 2 of o_done[k % 2])
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 9);
+  uint64_t* q_free = s_full + 8;  // the item's last score product has finished reading Q
+  uint64_t* o_read = s_full + 9;  // one arrival per softmax warp: the item's O is in registers
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_full + 10);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 11);
 
   const int nkv = (p.seq + 127) / 128;
-  const int qt = blockIdx.x, gh = blockIdx.y, b = blockIdx.z;
-  const int shard = gh / p.local_heads, hl = gh % p.local_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr uint32_t kCols = 256;  // S: columns 0..127; O_0, O_1 (the two key halves): 128..191, 192..255
   constexpr int kMmaWarp = kStrmSoftmaxWarps, kLoadWarp = kStrmSoftmaxWarps + 1;
+  // Item i of the launch: query tile i % q_tiles of head (i / q_tiles) % heads
+  // of sequence i / (q_tiles * heads), so that items taken together share
+  // their keys and values. The CTA takes items blockIdx.x, + gridDim.x, ...
+  struct Item {
+    int qt, shard, hl;
+    int32_t row0;
+  };
+  auto decode = [&](int i, Item& it) {
+    it.qt = i % p.q_tiles;
+    const int r = i / p.q_tiles;
+    const int gh = r % p.heads;
+    it.shard = gh / p.local_heads;
+    it.hl = gh % p.local_heads;
+    it.row0 = (r / p.heads) * p.seq;
+    // Debug build: the item's query tile, rank and output exist (the same
+    // answer in every role, so all of them skip a bad item alike).
+    return TPMLP_DCHECK(it.qt * 128 < p.seq && it.shard < kMaxGroups && p.out[it.shard] != nullptr,
+                        tid == 0 ? p.status : nullptr, kChkAttnTile);
+  };
 
   if (tid == 0) {
     mbar_init(bar_q, 1);
@@ -443,6 +461,8 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     mbar_init(o_done + 1, 1);
     mbar_init(x_bar, kStrmSoftmaxWarps);
     mbar_init(drain, 1);
+    mbar_init(q_free, 1);
+    mbar_init(o_read, kStrmSoftmaxWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -455,77 +475,100 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
   pdl_launch_dependents();
   const uint32_t tS = tmem, tO = tmem + 128;
   const WaitGuard guard{abort_flag, p.wait_ns, p.status};
-  const int32_t row0 = b * p.seq;
 
   if (warp == kLoadWarp) {
     if (lane == 0) {
-      // ---------------- loads: Q, then the ring in the order the products read it
-      const CUtensorMap* mq = &p.map_qkv[shard];
-      const CUtensorMap* mv = &p.map_vt[shard];
-      const int kx = p.Dn + hl * 64;
-      mbar_arrive_expect_tx(bar_q, kQBytes);
-      tma_load_2d(sQ, mq, hl * 64, row0 + qt * 128, bar_q);
+      // ---------------- loads: per item Q (once the previous item's last
+      // score product has read the buffer), then the ring in the order the
+      // products read it; the ring runs on from item to item.
       int n = 0;  // ring position of the next load
-      auto put = [&](bool is_v, int blk) {
-        const int slot = n % kStrmSlots;
-        if (!wait_bounded(ring_empty + slot, ((n / kStrmSlots) & 1) ^ 1u, guard, kSiteProducer)) return false;
-        uint8_t* dst = sRing + slot * kStrmSlotBytes;
-        mbar_arrive_expect_tx(ring_full + slot, kStrmSlotBytes);
-        if (is_v) {
-          tma_load_2d(dst, mv, row0 + blk * 128, hl * 64, ring_full + slot);
-          tma_load_2d(dst + kVtChunkBytes, mv, row0 + blk * 128 + 64, hl * 64, ring_full + slot);
-        } else {
-          tma_load_2d(dst, mq, kx, row0 + blk * 128, ring_full + slot);
-        }
-        ++n;
-        return true;
-      };
-      bool ok = put(false, 0);
-      for (int j = 1; ok && j < nkv; ++j) ok = put(false, j) && put(true, j - 1);
-      if (ok) put(true, nkv - 1);
+      int k = 0;  // items done by this CTA
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < p.items; i += gridDim.x) {
+        Item it;
+        if (!decode(i, it)) continue;
+        const CUtensorMap* mq = &p.map_qkv[it.shard];
+        const CUtensorMap* mv = &p.map_vt[it.shard];
+        const int kx = p.Dn + it.hl * 64;
+        if (k > 0 && !wait_bounded(q_free, (k - 1) & 1, guard, kSiteProducer)) break;
+        mbar_arrive_expect_tx(bar_q, kQBytes);
+        tma_load_2d(sQ, mq, it.hl * 64, it.row0 + it.qt * 128, bar_q);
+        auto put = [&](bool is_v, int blk) {
+          const int slot = n % kStrmSlots;
+          if (!wait_bounded(ring_empty + slot, ((n / kStrmSlots) & 1) ^ 1u, guard, kSiteProducer)) return false;
+          uint8_t* dst = sRing + slot * kStrmSlotBytes;
+          mbar_arrive_expect_tx(ring_full + slot, kStrmSlotBytes);
+          if (is_v) {
+            tma_load_2d(dst, mv, it.row0 + blk * 128, it.hl * 64, ring_full + slot);
+            tma_load_2d(dst + kVtChunkBytes, mv, it.row0 + blk * 128 + 64, it.hl * 64, ring_full + slot);
+          } else {
+            tma_load_2d(dst, mq, kx, it.row0 + blk * 128, ring_full + slot);
+          }
+          ++n;
+          return true;
+        };
+        ok = put(false, 0);
+        for (int j = 1; ok && j < nkv; ++j) ok = put(false, j) && put(true, j - 1);
+        if (ok) ok = put(true, nkv - 1);
+        ++k;
+      }
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       // ---------------- products
-      bool ok = wait_bounded(bar_q, 0, guard, kSiteProducer);
       const uint64_t dq = smem_desc_sw128(smem_addr(sQ));
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, 64);
-      int n = 0;  // ring position of the next operand
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          // S_j overwrites S_{j-1} once every softmax warp holds its columns,
-          // so this product overlaps the softmax of block j-1.
-          const int slot = n % kStrmSlots;
-          ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull);
-          if (ok && j > 0) ok = wait_bounded(s_read, (j - 1) & 1, guard, kSiteMmaAcc);
-          if (!ok) break;
-          ++n;
-          tc_fence_after_sync();
-          const uint64_t dk = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes));
+      int n = 0;   // ring position of the next operand
+      int k = 0;   // items done by this CTA
+      int jb = 0;  // blocks done by this CTA (all items): the phase counter of s_read, s_free and o_done
+      bool ok = true;
+      for (int i = blockIdx.x; ok && i < p.items; i += gridDim.x) {
+        Item it;
+        if (!decode(i, it)) continue;
+        ok = wait_bounded(bar_q, k & 1, guard, kSiteProducer);
+        for (int j = 0; ok && j <= nkv; ++j) {
+          if (j < nkv) {
+            // S_j overwrites the previous block's S once every softmax warp
+            // holds its columns, so this product overlaps that softmax.
+            const int slot = n % kStrmSlots;
+            ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull);
+            if (ok && jb + j > 0) ok = wait_bounded(s_read, (jb + j - 1) & 1, guard, kSiteMmaAcc);
+            if (!ok) break;
+            ++n;
+            tc_fence_after_sync();
+            const uint64_t dk = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes));
 #pragma unroll
-          for (int k = 0; k < 4; ++k) tc_mma_bf16(tS, dq + 2 * k, dk + 2 * k, kIdS, k > 0 ? 1u : 0u);
-          tc_commit(s_full);
-          tc_commit(ring_empty + slot);
-        }
-        if (j > 0) {  // O (+)= P_{j-1} V_{j-1}, once P_{j-1} is written and O rescaled
-          const int slot = n % kStrmSlots;
-          ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull) &&
-               wait_bounded(s_free + ((j - 1) & 1), ((j - 1) >> 1) & 1, guard, kSiteMmaAcc);
-          if (!ok) break;
-          ++n;
-          tc_fence_after_sync();
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint64_t dp = smem_desc_sw128(smem_addr(sP + ((j - 1) & 1) * kStrmPBufBytes + c * kPChunkBytes));
-            const uint64_t dv = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes + c * kVtChunkBytes));
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              tc_mma_bf16(tO + 64u * c, dp + 2 * k, dv + 2 * k, kIdO, (j > 1 || k > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) tc_mma_bf16(tS, dq + 2 * kk, dk + 2 * kk, kIdS, kk > 0 ? 1u : 0u);
+            tc_commit(s_full);
+            tc_commit(ring_empty + slot);
+            if (j == nkv - 1) tc_commit(q_free);  // the next item's Q may land once this product is done
           }
-          tc_commit(o_done + ((j - 1) & 1));
-          tc_commit(ring_empty + slot);
+          if (j > 0) {  // O (+)= P_{j-1} V_{j-1}, once P_{j-1} is written and O rescaled
+            const int b = jb + j - 1;  // the block's index among the CTA's blocks
+            const int slot = n % kStrmSlots;
+            ok = wait_bounded(ring_full + slot, (n / kStrmSlots) & 1, guard, kSiteMmaFull) &&
+                 wait_bounded(s_free + (b & 1), (b >> 1) & 1, guard, kSiteMmaAcc);
+            // The item's first product overwrites O: the previous item's
+            // merge must hold its O in registers.
+            if (ok && j == 1 && k > 0) ok = wait_bounded(o_read, (k - 1) & 1, guard, kSiteMmaAcc);
+            if (!ok) break;
+            ++n;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint64_t dp = smem_desc_sw128(smem_addr(sP + (b & 1) * kStrmPBufBytes + c * kPChunkBytes));
+              const uint64_t dv = smem_desc_sw128(smem_addr(sRing + slot * kStrmSlotBytes + c * kVtChunkBytes));
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_bf16(tO + 64u * c, dp + 2 * kk, dv + 2 * kk, kIdO, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(o_done + (b & 1));
+            tc_commit(ring_empty + slot);
+          }
         }
+        jb += nkv;
+        ++k;
       }
     }
   } else {
@@ -534,125 +577,141 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
     // its half of every block, with a running maximum, a row sum and an
     // output accumulator O_half of its own, so the two warps of a row never
     // wait for each other inside the loop; their partial results are merged
-    // once at the end.
+    // once at the end of the item.
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tOh = tO + lane_off + 64u * half;  // this warp's rows of O_half
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, ok && wait_bounded(s_full, j & 1, guard, kSiteMmaFull));
-      if (!ok) break;
-      tc_fence_after_sync();
-      float v[64];
-      {
-        uint32_t r0[32], r1[32];
-        tmem_ld_32cols_async(tS + lane_off + half * 64, r0);
-        tmem_ld_32cols_async(tS + lane_off + half * 64 + 32, r1);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = __uint_as_float(r0[i]);
-          v[32 + i] = __uint_as_float(r1[i]);
-        }
-      }
-      tc_fence_before_sync();  // S may be overwritten by the next block's product now
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_read);
-      const int kbase = j * 128 + half * 64;  // key of column 0 of this half
-      const bool full = kbase + 64 <= p.seq;
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (full) {  // every column a key of the sequence: two values per max
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) m4[(i >> 1) & 3] = fmax3(m4[(i >> 1) & 3], v[i], v[i + 1]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (kbase + i < p.seq) m4[i & 3] = fmaxf(m4[i & 3], v[i]);
-      }
-      const float m_blk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-      // The running maximum moves only when the block's exceeds it by more
-      // than 8 in log2 units: until then the weights stay <= 2^8 (well inside
-      // fp32 and bf16 range) and O needs no rescale; the final division by l
-      // is the same either way. A half without keys so far keeps -inf and
-      // weight 0 (alpha 1, nothing to rescale).
-      const float m_new = (m_blk - m_run) * p.scale_log2 > 8.0f ? m_blk : m_run;  // m_blk on its first keys
-      const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx((m_run - m_new) * p.scale_log2);
-      const float mb = m_new * p.scale_log2;
-      uint32_t w[32];
-      float s2[2] = {0.f, 0.f};
-      if (full) {
-        // Exponent arguments and the row sum on packed fp32 pairs (half the
-        // FMA-pipe instructions); the two lanes of a pair are the even and
-        // odd columns, so the sums are the same two partial sums as below.
-        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nmb2 = f2_pack(-mb, -mb);
-        uint64_t acc2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          float x0, x1;
-          f2_unpack(f2_fma(f2_pack(v[i], v[i + 1]), sc2, nmb2), x0, x1);
-          const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-          acc2 = f2_add(acc2, f2_pack(e0, e1));
-          w[i / 2] = pack2_bf16(e0, e1);
-        }
-        f2_unpack(acc2, s2[0], s2[1]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float e0 = kbase + i < p.seq ? ex2_approx(fmaf(v[i], p.scale_log2, -mb)) : 0.f;
-          const float e1 = kbase + i + 1 < p.seq ? ex2_approx(fmaf(v[i + 1], p.scale_log2, -mb)) : 0.f;
-          s2[0] += e0;
-          s2[1] += e1;
-          w[i / 2] = pack2_bf16(e0, e1);
-        }
-      }
-      l_run = l_run * alpha + (s2[0] + s2[1]);
-      if (j > 1) {  // P buffer j % 2 was last read by P_{j-2} V_{j-2}
-        ok = __all_sync(0xffffffffu, wait_bounded(o_done + (j & 1), ((j >> 1) - 1) & 1, guard, kSiteMmaAcc));
-        if (!ok) break;
-      }
-      uint8_t* prow = sP + (j & 1) * kStrmPBufBytes + half * kPChunkBytes + row * 128;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
-            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's rows of O_half
-        // once P_{j-1} V_{j-1} has finished writing O
-        ok = __all_sync(0xffffffffu, wait_bounded(o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, guard, kSiteMmaAcc));
+    int k = 0;   // items done by this CTA
+    int jb = 0;  // blocks done by this CTA
+    for (int i = blockIdx.x; ok && i < p.items; i += gridDim.x) {
+      Item it;
+      if (!decode(i, it)) continue;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        const int b = jb + j;  // the block's index among the CTA's blocks
+        ok = __all_sync(0xffffffffu, ok && wait_bounded(s_full, b & 1, guard, kSiteMmaFull));
         if (!ok) break;
         tc_fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < 64; c += 32) {
-          float o[32];
-          tmem_ld_32cols(tOh + c, o);
+        float v[64];
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32cols_async(tS + lane_off + half * 64, r0);
+          tmem_ld_32cols_async(tS + lane_off + half * 64 + 32, r1);
+          tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st_32cols(tOh + c, o);
+          for (int q = 0; q < 32; ++q) {
+            v[q] = __uint_as_float(r0[q]);
+            v[32 + q] = __uint_as_float(r1[q]);
+          }
         }
+        tc_fence_before_sync();  // S may be overwritten by the next block's product now
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_read);
+        const int kbase = j * 128 + half * 64;  // key of column 0 of this half
+        const bool full = kbase + 64 <= p.seq;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (full) {  // every column a key of the sequence: two values per max
+#pragma unroll
+          for (int q = 0; q < 64; q += 2) m4[(q >> 1) & 3] = fmax3(m4[(q >> 1) & 3], v[q], v[q + 1]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 64; ++q)
+            if (kbase + q < p.seq) m4[q & 3] = fmaxf(m4[q & 3], v[q]);
+        }
+        const float m_blk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        // The running maximum moves only when the block's exceeds it by more
+        // than 8 in log2 units: until then the weights stay <= 2^8 (well inside
+        // fp32 and bf16 range) and O needs no rescale; the final division by l
+        // is the same either way. A half without keys so far keeps -inf and
+        // weight 0 (alpha 1, nothing to rescale).
+        const float m_new = (m_blk - m_run) * p.scale_log2 > 8.0f ? m_blk : m_run;  // m_blk on its first keys
+        const float alpha = m_new == -INFINITY ? 1.0f : ex2_approx((m_run - m_new) * p.scale_log2);
+        const float mb = m_new * p.scale_log2;
+        uint32_t w[32];
+        float s2[2] = {0.f, 0.f};
+        if (full) {
+          // Exponent arguments and the row sum on packed fp32 pairs (half the
+          // FMA-pipe instructions); the two lanes of a pair are the even and
+          // odd columns, so the sums are the same two partial sums as below.
+          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nmb2 = f2_pack(-mb, -mb);
+          uint64_t acc2 = f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < 64; q += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(v[q], v[q + 1]), sc2, nmb2), x0, x1);
+            const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+            acc2 = f2_add(acc2, f2_pack(e0, e1));
+            w[q / 2] = pack2_bf16(e0, e1);
+          }
+          f2_unpack(acc2, s2[0], s2[1]);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 64; q += 2) {
+            const float e0 = kbase + q < p.seq ? ex2_approx(fmaf(v[q], p.scale_log2, -mb)) : 0.f;
+            const float e1 = kbase + q + 1 < p.seq ? ex2_approx(fmaf(v[q + 1], p.scale_log2, -mb)) : 0.f;
+            s2[0] += e0;
+            s2[1] += e1;
+            w[q / 2] = pack2_bf16(e0, e1);
+          }
+        }
+        l_run = l_run * alpha + (s2[0] + s2[1]);
+        if (b > 1) {  // P buffer b % 2 was last read by the product of block b - 2
+          ok = __all_sync(0xffffffffu, wait_bounded(o_done + (b & 1), ((b >> 1) - 1) & 1, guard, kSiteMmaAcc));
+          if (!ok) break;
+        }
+        uint8_t* prow = sP + (b & 1) * kStrmPBufBytes + half * kPChunkBytes + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(prow + ((u ^ (row & 7)) << 4)) =
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {  // rescale this warp's rows of O_half
+          // once the previous block's product has finished writing O
+          ok = __all_sync(0xffffffffu,
+                          wait_bounded(o_done + ((b - 1) & 1), ((b - 1) >> 1) & 1, guard, kSiteMmaAcc));
+          if (!ok) break;
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < 64; c += 32) {
+            float o[32];
+            tmem_ld_32cols(tOh + c, o);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) o[q] *= alpha;
+            tmem_st_32cols(tOh + c, o);
+          }
+        }
+        m_run = m_new;
+        fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free + (b & 1));
       }
-      m_run = m_new;
-      fence_proxy_async_smem();  // P, written by threads, is read by the tensor cores
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_free + (j & 1));
-    }
-    // ---- merge the halves: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), f_h = 2^((m_h - m) s), m = max m_h
-    if (ok)
-      ok = __all_sync(0xffffffffu, wait_bounded(o_done + ((nkv - 1) & 1), ((nkv - 1) >> 1) & 1, guard, kSiteEpilogue));
-    if (ok) {
-      red_max[half * 128 + row] = m_run;
-      red_sum[half * 128 + row] = l_run;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(x_bar);
-      ok = __all_sync(0xffffffffu, wait_bounded(x_bar, 0, guard, kSiteEpilogue));
-    }
-    if (ok) {
+      if (!ok) break;
+      // ---- merge the halves: O = (f_0 O_0 + f_1 O_1) / (f_0 l_0 + f_1 l_1), f_h = 2^((m_h - m) s), m = max m_h.
+      // The halves' maxima and sums meet in the P buffer of the item's last
+      // block: its product is done, and it is next written two blocks on,
+      // after every warp has passed this merge.
+      const int bl = jb + nkv - 1;
+      float* red_max = reinterpret_cast<float*>(sP + (bl & 1) * kStrmPBufBytes);  // [2][128]
+      float* red_sum = red_max + 256;                                            // [2][128]
+      ok = __all_sync(0xffffffffu, wait_bounded(o_done + (bl & 1), (bl >> 1) & 1, guard, kSiteEpilogue));
+      if (ok) {
+        red_max[half * 128 + row] = m_run;
+        red_sum[half * 128 + row] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x_bar);
+        ok = __all_sync(0xffffffffu, wait_bounded(x_bar, k & 1, guard, kSiteEpilogue));
+      }
+      if (!ok) break;
       tc_fence_after_sync();
       float o0[32], o1[32];
       tmem_ld_32cols(tO + lane_off + half * 32, o0);       // O_0, this warp's 32 output columns
       tmem_ld_32cols(tO + lane_off + 64 + half * 32, o1);  // O_1, the same columns
-      const int qi = qt * 128 + row;
+      tc_fence_before_sync();  // O may be overwritten by the next item's first product now
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_read);
+      const int qi = it.qt * 128 + row;
       if (qi < p.seq) {
         const float m0 = red_max[row], m1 = red_max[128 + row];
         const float m = fmaxf(m0, m1);  // finite: key 0 lies in half 0 of block 0
@@ -660,8 +719,8 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
         const float f1 = m1 == -INFINITY ? 0.0f : ex2_approx((m1 - m) * p.scale_log2);
         const float inv = 1.0f / (f0 * red_sum[row] + f1 * red_sum[128 + row]);
         const float g0 = f0 * inv, g1 = f1 * inv;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[shard]) + (static_cast<int64_t>(row0) + qi) * p.Dn +
-                             hl * 64 + half * 32;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out[it.shard]) +
+                             (static_cast<int64_t>(it.row0) + qi) * p.Dn + it.hl * 64 + half * 32;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           float y[8];
@@ -671,6 +730,8 @@ __global__ void __launch_bounds__(kStrmThreads, 2) attn_stream_kernel(const __gr
               make_uint4(pack2_bf16(y[0], y[1]), pack2_bf16(y[2], y[3]), pack2_bf16(y[4], y[5]), pack2_bf16(y[6], y[7]));
         }
       }
+      jb += nkv;
+      ++k;
     }
   }
 
@@ -783,7 +844,21 @@ cudaError_t launch_attention_tc(const AttnLaunch& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(attn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kStrmSmem));
     if (e != cudaSuccess) return e;
-    return launch_pdl(attn_stream_kernel, grid, dim3(kStrmThreads), kStrmSmem, s, p);
+    // Work items (query tile, head, sequence) taken by a persistent grid of
+    // the CTAs that fit at once (two per SM), each running its items through
+    // one pipeline; TPMLP_ATTN_PERSIST=0 (read at every launch) launches one
+    // CTA per item instead.
+    p.q_tiles = static_cast<int>(grid.x);
+    p.heads = static_cast<int>(grid.y);
+    p.items = static_cast<int>(grid.x * grid.y * grid.z);
+    // Two CTAs per SM by design (launch bounds, 112 KB of shared memory and
+    // 256 TMEM columns each); the occupancy calculator reports one here, so
+    // the grid is sized from the design. CTAs share nothing, so a grid that
+    // did not fit at once would only run in two waves.
+    int ctas = p.items;
+    const char* pv = getenv("TPMLP_ATTN_PERSIST");
+    if (!(pv && *pv && atoi(pv) == 0) && int64_t(2) * num_sms() < ctas) ctas = 2 * num_sms();
+    return launch_pdl(attn_stream_kernel, dim3(static_cast<unsigned>(ctas)), dim3(kStrmThreads), kStrmSmem, s, p);
   }
   const int nkv = (a.seq + 127) / 128, nch = (a.seq + 63) / 64;
   const uint32_t smem = attn_smem_bytes(nkv, nch);
